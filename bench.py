@@ -1,0 +1,346 @@
+#!/usr/bin/env python
+"""Throughput of the GB300 MoE-LoRA layer (tokens/s per layer) and its roofline fraction.
+
+One step = one pass of the whole hot path over one batch of seeded synthetic input:
+route -> align -> forward (gather, gate_up shrink, gate_up GEMM + expand + SiLU,
+down shrink, down GEMM + expand + weighted combine, finalize).  Default workload:
+the decode-sized layer (T=16 tokens, H=I=2880, E=32 top-4, 8 adapters of rank 32).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+N > 1 runs N independent replicas (one process per GPU via torch.distributed.run),
+each on its own batch; value = tokens of all ranks / max-over-ranks time.
+--impl reference times the fp64 CPU oracle on the host cores on a bounded sample of
+the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from expert_gemm_gb300 import workloads as W  # noqa: E402
+
+METRIC = "MoE-LoRA layer tokens/s"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", 0)) or None, "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# --------------------------------------------------------------- accounting --
+
+def algorithmic(wl: W.Workload, ids: np.ndarray, lora: np.ndarray):
+    """Algorithmic bytes and flops of one layer pass and of its gate_up launch.
+
+    Bytes: weights of the distinct touched experts and distinct touched (adapter>=0,
+    expert) pairs, x in and out once; padding rows, S tiles, h and zero rank padding
+    are not counted.  Flops: 2 * valid pairs * (H*2I + I*H) + LoRA 2 * r * (H + 2I + I + H)
+    per pair with an adapter.
+    """
+    T, H, I, E, k = wl.T, wl.H, wl.I, wl.E, wl.k
+    ranks = np.asarray(wl.ranks)
+    valid = (ids >= 0) & (ids < E)
+    experts = np.unique(ids[valid])
+    a_tok = np.repeat(lora, k).reshape(T, k)
+    with_a = valid & (a_tok >= 0)
+    ae = np.unique(a_tok[with_a].astype(np.int64) * E + ids[with_a])
+    r_ae = ranks[ae // E] if len(ae) else np.zeros(0)
+    w_gu = len(experts) * 2 * I * H * 2
+    w_dn = len(experts) * H * I * 2
+    lora_gu = int(np.sum(r_ae * (H + 2 * I))) * 2
+    lora_dn = int(np.sum(r_ae * (I + H))) * 2
+    act = 2 * T * H * 2
+    n_pairs = int(valid.sum())
+    r_pairs = ranks[a_tok[with_a]] if with_a.any() else np.zeros(0)
+    flops = 2 * n_pairs * (H * 2 * I + I * H) + 2 * int(np.sum(r_pairs)) * (H + 2 * I + I + H)
+    gate_up_bytes = w_gu + int(np.sum(r_ae * 2 * I)) * 2 + T * H * 2 + n_pairs * I * 2
+    return {"bytes": w_gu + w_dn + lora_gu + lora_dn + act, "flops": flops, "gate_up_bytes": gate_up_bytes,
+            "gate_up_flops": 2 * n_pairs * H * 2 * I + 2 * int(np.sum(r_pairs)) * 2 * I,
+            "experts": int(len(experts)), "adapter_expert_pairs": int(len(ae)), "valid_pairs": n_pairs}
+
+
+# ------------------------------------------------------------------- clocks --
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu: int):
+        self.gpu, self.proc = gpu, None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.gpu), "-lms", "200"], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            return None
+        rows = [[c.strip() for c in line.split(",")] for line in out.strip().splitlines() if line.strip()]
+        rows = [r for r in rows if len(r) >= 9]
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# -------------------------------------------------------------- our arm -----
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    from expert_gemm_gb300 import build, moe_lora as ml
+    torch.cuda.set_device(local_rank)
+    build.build()
+    ml.load()
+    wl = W.get(args.workload)
+    seed_w, seed_b = 0, rank                      # same weights on every replica, own batch per rank
+    logits, lora = W.make_routing(wl, seed_b)
+    x = W.make_activations(wl, seed_b)
+    w = W.make_weights(wl, seed_w)
+    bm = args.block_m or ml.pick_block_m(wl.T, wl.k, wl.E)
+    d = ml.LayerDims(T=wl.T, H=wl.H, I=wl.I, E=wl.E, k=wl.k, L=wl.L, r_max=wl.r_max, block_m=bm, ranks=wl.ranks)
+    dev = lambda a: (torch.from_numpy(a.view(np.int16)).cuda().view(torch.bfloat16) if a.dtype == np.uint16  # noqa
+                     else torch.from_numpy(np.ascontiguousarray(a)).cuda())
+    wd = {n: dev(w[n]) for n in ("W_gu", "W_dn", "A_gu", "Bt_gu", "A_dn", "Bt_dn")}
+    del w
+    layer = ml.Layer(d, wd)
+    lg, lr, xd = dev(logits), dev(lora), dev(x)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    K, Wm = args.steps, args.warmup
+    nst = ml.NUM_STAGES + 1
+    stage_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nst)] for _ in range(K)]
+    step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for evs in stage_ev:                          # create the CUDA events before handing them to the library
+        for e in evs:
+            e.record()
+    for _ in range(Wm):
+        layer.step(lg, lr, xd)
+        flush.zero_()
+    torch.cuda.synchronize()
+    if int(layer.status.item()) != 0:
+        raise RuntimeError(f"device status {int(layer.status.item())}")
+    ids = layer.topk_ids.cpu().numpy()
+    tot = layer.bufs["totals"].cpu().numpy()
+    nchunks_launched = 3 if wl.T * wl.k > 0 else 1
+    launches_per_step = 1 + nchunks_launched + 4 + (2 if wl.L > 0 else 0)
+    acct = algorithmic(wl, ids, lora)
+
+    clocks = ClockSampler(local_rank)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    t_wall0 = time.perf_counter()
+    for i in range(K):
+        step_ev[i][0].record()
+        layer.step(lg, lr, xd, stage_events=stage_ev[i])
+        step_ev[i][1].record()
+        flush.zero_()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    step_ms = [a.elapsed_time(b) for a, b in step_ev]
+    stage_ms = np.array([[evs[j].elapsed_time(evs[j + 1]) for j in range(nst - 1)] for evs in stage_ev])
+    ms = float(np.sum(step_ms)) / K
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    if int(layer.status.item()) != 0:
+        raise RuntimeError(f"device status {int(layer.status.item())}")
+
+    # end to end through the host-buffer entry point (pinned host memory)
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
+    lg_h, lr_h, x_h = pin(logits), pin(lora), pin(x.view(np.int16))
+    out_h = torch.empty((wl.T, wl.H), dtype=torch.int16).pin_memory()
+    for _ in range(max(2, min(Wm, 10))):
+        layer.step_host(lg_h, lr_h, x_h, out_h)
+    ke = max(1, min(K, 500))
+    if world > 1:
+        torch.distributed.barrier()
+    t0 = time.perf_counter()
+    for _ in range(ke):
+        layer.step_host(lg_h, lr_h, x_h, out_h)
+    e2e_s = (time.perf_counter() - t0) / ke
+    if world > 1:
+        t = torch.tensor([e2e_s], dtype=torch.float64, device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_s = float(t.item())
+
+    hbm, tc, tc_sus, src = peaks()
+    gu_ms = float(np.mean(stage_ms[:, 2]))
+    gu_gbs = acct["gate_up_bytes"] / (gu_ms * 1e-3) / 1e9
+    layer_s = ms * 1e-3
+    roof_s = max(acct["bytes"] / (hbm * 1e9), acct["flops"] / (tc * 1e12))
+    res = {
+        "metric": METRIC, "value": world * wl.T / layer_s, "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": Wm, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded normals, bf16)",
+        "config": {"workload": f"{wl.name}: T={wl.T} H={wl.H} I={wl.I} E={wl.E} top-{wl.k} L={wl.L} "
+                               f"ranks={sorted(set(wl.ranks))}", "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E,
+                   "k": wl.k, "L": wl.L, "block_m": bm, "global_batch": world * wl.T,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "flushed between timed steps (256 MiB write)"},
+        "roofline": {"bound": "hbm", "kernel": "gate_up (tcgen05 grouped GEMM + LoRA expand + SiLU)",
+                     "achieved": gu_gbs, "peak": hbm, "unit": "GB/s", "frac": gu_gbs / hbm,
+                     "peak_source": src, "traffic": None, "launch_ms": gu_ms,
+                     "algorithmic_bytes_per_launch": acct["gate_up_bytes"]},
+        "layer_roofline": {"alg_bytes": acct["bytes"], "alg_flops": acct["flops"], "t_roof_ms": roof_s * 1e3,
+                           "frac": roof_s / layer_s, "hbm_gbs_peak": hbm, "bf16_tflops_peak": tc},
+        "stage_ms": {n: float(np.mean(stage_ms[:, j])) for j, n in enumerate(ml.STAGES)},
+        "touched": {k_: acct[k_] for k_ in ("experts", "adapter_expert_pairs", "valid_pairs")},
+        "e2e": {"value": world * wl.T / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": wl.T * (wl.E * 4 + 4 + wl.H * 2),
+                "d2h_bytes_per_step": wl.T * wl.H * 2 + 4 + 16, "ms_per_step": e2e_s * 1e3,
+                "entry": "moe_lora_layer_host (pinned host buffers)"},
+        "gpu_launches": launches_per_step * K,
+        "clocks": clk,
+        "wall_s_timed": t_wall,
+        "align_totals": [int(v) for v in tot],
+    }
+    return res
+
+
+# --------------------------------------------------------- oracle timings ---
+
+def oracle_sample_rate(wl: W.Workload, n_tokens: int, budget_s: float, seed: int = 0):
+    """Oracle (route + align + fp64 forward) on the first n_tokens tokens, repeated for ~budget_s."""
+    from oracle import Oracle
+    o = Oracle()
+    logits, lora = W.make_routing(wl, seed)
+    x = W.make_activations(wl, seed)
+    w = W.make_weights(wl, seed)
+    n = max(1, min(n_tokens, wl.T))
+    lg, lr, xs = logits[:n], lora[:n], x[:n]
+    bm = 16
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        ids, tw = o.route(lg, wl.k)
+        o.align(ids, lr, wl.E, wl.L, bm)
+        o.forward(xs, ids, tw.astype(np.float32), lr, w)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return n * reps / el, n, reps, el
+
+
+def cores_used():
+    try:
+        n = len(os.sched_getaffinity(0))
+    except Exception:
+        n = os.cpu_count() or 1
+    return int(os.environ.get("OMP_NUM_THREADS", n))
+
+
+def run_reference(args):
+    """The fp64 oracle as the reference arm: each step is a bounded token sample of the workload."""
+    from oracle import Oracle
+    wl = W.get(args.workload)
+    o = Oracle()
+    logits, lora = W.make_routing(wl, 0)
+    x = W.make_activations(wl, 0)
+    w = W.make_weights(wl, 0)
+    # calibrate: cost of one token, then size the per-step sample to ~150 s in total
+    def one_step(n):
+        ids, tw = o.route(logits[:n], wl.k)
+        o.align(ids, lora[:n], wl.E, wl.L, 16)
+        o.forward(x[:n], ids, tw.astype(np.float32), lora[:n], w)
+    n_cal = min(wl.T, 8)
+    t0 = time.perf_counter()
+    one_step(n_cal)
+    per_tok = (time.perf_counter() - t0) / n_cal
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    n = int(max(1, min(wl.T, budget / max(per_tok, 1e-9))))
+    for _ in range(args.warmup):
+        one_step(n)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one_step(n)
+    el = time.perf_counter() - t0
+    v = n * args.steps / el
+    return {"metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded normals, bf16)",
+            "impl": "reference",
+            "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k, "L": wl.L},
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores_used(), "kind": "oracle",
+                             "sample": f"first {n} of {wl.T} tokens per step (route + align + fp64 forward)"},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="decode", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--block-m", type=int, default=0)
+    ap.add_argument("--cpu-baseline-s", type=float, default=12.0, help="seconds of oracle time (0 = skip)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    res = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        if world == 1 and args.cpu_baseline_s > 0:
+            wl = W.get(args.workload)
+            v, n, reps, el = oracle_sample_rate(wl, min(wl.T, 16), args.cpu_baseline_s)
+            res["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": cores_used(), "kind": "oracle",
+                                   "sample": f"first {n} of {wl.T} tokens, {reps} passes in {el:.1f} s "
+                                             f"(route + align + fp64 forward)"}
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

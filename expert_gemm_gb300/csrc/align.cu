@@ -1,0 +1,267 @@
+// align.cu -- align-and-sort of the (expert, adapter) compound sparsity.
+//
+// The pages give the problem, not a layout: default fused-MoE configurations ignore
+// the extra grid dimension of the LoRA index and the compound sparsity of many
+// adapters (AWS ML Blog "Efficiently serve dozens of fine-tuned models with vLLM on
+// Amazon SageMaker AI and Amazon Bedrock", section "Tuning kernel configurations for
+// Amazon SageMaker AI and Amazon Bedrock"; agentlenshq.com "vLLM MoE 모델을 위한
+// Multi-LoRA 서빙", section "MoE 모델을 위한 Multi-LoRA 서빙").  This library's layout
+// (see moe_lora.h): valid pairs sorted by (expert, adapter, pair), each expert padded
+// to a multiple of block_m rows, plus per-block adapter runs.
+//
+// A stable counting sort in three launches:
+//   1. chunk:   each CTA sorts its chunk of pair keys (bucket << log2(CH) | local index)
+//               with a bitonic network in shared memory and writes per-bucket counts;
+//   2. scan:    one CTA turns counts into per-(chunk, bucket) offsets, expert starts
+//               (padded), bucket starts, runs, block experts, padding sentinels;
+//   3. scatter: each CTA places its pairs; rank inside the chunk = index - first index
+//               of the bucket in the sorted chunk, so equal keys keep pair order.
+// Integer work only; the result is bit-identical to the sequential definition.
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr uint32_t kInvalidKey = 0xFFFFFFFFu;
+
+__device__ __forceinline__ int lower_bound_u32(const uint32_t* a, int lo, int hi, uint32_t key) {
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (a[mid] < key) lo = mid + 1;
+    else hi = mid;
+  }
+  return lo;
+}
+
+__global__ void __launch_bounds__(1024) align_chunk_kernel(AlignLaunch a) {
+  extern __shared__ uint32_t keys[];
+  __shared__ int32_t s_invalid;
+  const int CH = 1 << a.ch_log2;
+  const int chunk = blockIdx.x;
+  const int64_t p0 = static_cast<int64_t>(chunk) << a.ch_log2;
+  const int LB = a.L + 1;
+  const int NB = a.E * LB;
+  if (threadIdx.x == 0) s_invalid = 0;
+  for (int b = threadIdx.x; b < NB; b += blockDim.x) a.counts[static_cast<int64_t>(chunk) * NB + b] = 0;
+  __syncthreads();
+  int inval = 0;
+  for (int i = threadIdx.x; i < CH; i += blockDim.x) {
+    const int64_t p = p0 + i;
+    uint32_t key = kInvalidKey;
+    if (p < a.P) {
+      const int e = a.topk_ids[p];
+      const int ad = a.lora_ids[p / a.k];
+      if (e >= 0 && e < a.E && ad >= -1 && ad < a.L)
+        key = (static_cast<uint32_t>(e * LB + ad + 1) << a.ch_log2) | static_cast<uint32_t>(i);
+      else
+        ++inval;
+    }
+    keys[i] = key;
+  }
+  if (inval) atomicAdd(&s_invalid, inval);
+  // bitonic sort, ascending
+  for (int size = 2; size <= CH; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      __syncthreads();
+      for (int i = threadIdx.x; i < CH / 2; i += blockDim.x) {
+        const int lo = 2 * i - (i & (stride - 1));
+        const int hi = lo + stride;
+        const bool asc = (lo & size) == 0;
+        const uint32_t x = keys[lo], y = keys[hi];
+        if ((x > y) == asc) {
+          keys[lo] = y;
+          keys[hi] = x;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < CH; i += blockDim.x) {
+    const uint32_t key = keys[i];
+    a.chunk_keys[p0 + i] = key;
+    if (key == kInvalidKey) continue;
+    const uint32_t bkt = key >> a.ch_log2;
+    const bool last = (i == CH - 1) || (keys[i + 1] >> a.ch_log2) != bkt;
+    if (last) {
+      const int first = lower_bound_u32(keys, 0, i, bkt << a.ch_log2);
+      a.counts[static_cast<int64_t>(chunk) * NB + bkt] = i - first + 1;
+    }
+  }
+  if (threadIdx.x == 0) a.chunk_invalid[chunk] = s_invalid;
+}
+
+// Block-wide exclusive scan over n values produced by getv(i); put(i, prefix) receives
+// each exclusive prefix.  Returns the total (same value in every thread).
+template <class GetV, class Put>
+__device__ int block_exclusive_scan(int n, GetV getv, Put put, int32_t* s_warp) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+  int carry = 0;
+  for (int base = 0; base < n; base += blockDim.x) {
+    const int i = base + tid;
+    const int v = i < n ? getv(i) : 0;
+    int x = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, off);
+      if (lane >= off) x += y;
+    }
+    if (lane == 31) s_warp[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+      int w = lane < nwarps ? s_warp[lane] : 0;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, w, off);
+        if (lane >= off) w += y;
+      }
+      if (lane < nwarps) s_warp[lane] = w;
+    }
+    __syncthreads();
+    const int excl = carry + (warp > 0 ? s_warp[warp - 1] : 0) + x - v;
+    if (i < n) put(i, excl);
+    carry += s_warp[nwarps - 1];
+    __syncthreads();
+  }
+  return carry;
+}
+
+__global__ void __launch_bounds__(1024) align_scan_kernel(AlignLaunch a) {
+  __shared__ int32_t s_warp[32];
+  __shared__ int32_t s_rows, s_runs;
+  const int LB = a.L + 1;
+  const int NB = a.E * LB;
+  const int BM = a.BM;
+  const int tid = threadIdx.x, nt = blockDim.x;
+  const moe_lora_align_buf& o = a.out;
+
+  // 1. bucket totals; counts[c][b] becomes the offset of chunk c inside bucket b
+  for (int b = tid; b < NB; b += nt) {
+    int run = 0;
+    for (int c = 0; c < a.nchunks; ++c) {
+      const int64_t ix = static_cast<int64_t>(c) * NB + b;
+      const int v = a.counts[ix];
+      a.counts[ix] = run;
+      run += v;
+    }
+    a.bucket_total[b] = run;
+  }
+  __syncthreads();
+  // 2. pairs per expert
+  for (int e = tid; e < a.E; e += nt) {
+    int n = 0;
+    for (int j = 0; j < LB; ++j) n += a.bucket_total[e * LB + j];
+    a.expert_n[e] = n;
+  }
+  __syncthreads();
+  // 3. padded expert starts
+  const int rows = block_exclusive_scan(
+      a.E, [&](int e) { return (a.expert_n[e] + BM - 1) / BM * BM; },
+      [&](int e, int pre) { o.expert_begin[e] = pre; }, s_warp);
+  if (tid == 0) {
+    o.expert_begin[a.E] = rows;
+    s_rows = rows;
+  }
+  __syncthreads();
+  // 4. bucket starts: expert start + earlier adapters of the same expert
+  for (int e = tid; e < a.E; e += nt) {
+    int base = o.expert_begin[e];
+    for (int j = 0; j < LB; ++j) {
+      a.bucket_base[e * LB + j] = base;
+      base += a.bucket_total[e * LB + j];
+    }
+  }
+  __syncthreads();
+  // 5. runs: a bucket of adapter >= 0 splits at block boundaries
+  auto nruns_of = [&](int b) -> int {
+    const int tot = a.bucket_total[b];
+    if (tot == 0 || (b % LB) == 0) return 0;
+    const int s = a.bucket_base[b];
+    return (s + tot - 1) / BM - s / BM + 1;
+  };
+  const int nruns = block_exclusive_scan(NB, nruns_of, [&](int b, int pre) { a.run_base[b] = pre; }, s_warp);
+  if (tid == 0) s_runs = nruns;
+  __syncthreads();
+  // 6. write runs; 7. block experts; 8. padding sentinels
+  for (int b = tid; b < NB; b += nt) {
+    const int cnt = nruns_of(b);
+    if (!cnt) continue;
+    const int s = a.bucket_base[b], end = s + a.bucket_total[b];
+    const int adapter = (b % LB) - 1;
+    const int r0 = a.run_base[b];
+    for (int i = 0; i < cnt; ++i) {
+      const int blk = s / BM + i;
+      int* r = o.runs + 4 * static_cast<int64_t>(r0 + i);
+      r[0] = blk;
+      r[1] = adapter;
+      r[2] = max(s, blk * BM);
+      r[3] = min(end, (blk + 1) * BM);
+    }
+  }
+  for (int e = tid; e < a.E; e += nt) {
+    const int s = o.expert_begin[e], end = o.expert_begin[e + 1];
+    for (int blk = s / BM; blk < end / BM; ++blk) o.block_expert[blk] = e;
+    for (int r = s + a.expert_n[e]; r < end; ++r) o.sorted_p[r] = static_cast<int32_t>(a.P);
+  }
+  if (tid == 0) {
+    int dropped = 0;
+    for (int c = 0; c < a.nchunks; ++c) dropped += a.chunk_invalid[c];
+    o.totals[0] = s_rows;
+    o.totals[1] = s_rows / BM;
+    o.totals[2] = s_runs;
+    o.totals[3] = dropped;
+  }
+  __syncthreads();
+  // 9. first run of each block (runs are in block order)
+  const int nblocks = s_rows / BM;
+  for (int blk = tid; blk <= nblocks; blk += nt) {
+    int lo = 0, hi = s_runs;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (o.runs[4 * static_cast<int64_t>(mid)] < blk) lo = mid + 1;
+      else hi = mid;
+    }
+    o.block_runs[blk] = lo;
+  }
+}
+
+__global__ void __launch_bounds__(1024) align_scatter_kernel(AlignLaunch a) {
+  extern __shared__ uint32_t keys[];
+  const int CH = 1 << a.ch_log2;
+  const int chunk = blockIdx.x;
+  const int64_t p0 = static_cast<int64_t>(chunk) << a.ch_log2;
+  const int NB = a.E * (a.L + 1);
+  for (int i = threadIdx.x; i < CH; i += blockDim.x) keys[i] = a.chunk_keys[p0 + i];
+  __syncthreads();
+  for (int i = threadIdx.x; i < CH; i += blockDim.x) {
+    const uint32_t key = keys[i];
+    if (key == kInvalidKey) continue;
+    const uint32_t bkt = key >> a.ch_log2;
+    const int local = static_cast<int>(key & static_cast<uint32_t>(CH - 1));
+    const int first = lower_bound_u32(keys, 0, i, bkt << a.ch_log2);
+    const int pos = a.bucket_base[bkt] + a.counts[static_cast<int64_t>(chunk) * NB + bkt] + (i - first);
+    a.out.sorted_p[pos] = static_cast<int32_t>(p0 + local);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_align(const AlignLaunch& a, cudaStream_t s) {
+  const int CH = 1 << a.ch_log2;
+  const int threads = CH < 1024 ? CH : 1024;
+  const size_t smem = static_cast<size_t>(CH) * sizeof(uint32_t);
+  if (a.nchunks > 0) {
+    align_chunk_kernel<<<a.nchunks, threads, smem, s>>>(a);
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+  }
+  align_scan_kernel<<<1, 1024, 0, s>>>(a);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  if (a.nchunks > 0) {
+    align_scatter_kernel<<<a.nchunks, threads, smem, s>>>(a);
+    err = cudaGetLastError();
+  }
+  return err;
+}
+
+}  // namespace moe

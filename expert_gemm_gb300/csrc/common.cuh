@@ -1,0 +1,79 @@
+// common.cuh -- types shared by the host orchestration and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "../../include/moe_lora.h"
+
+namespace moe {
+
+// Which stage of the layer one grouped-GEMM launch computes.
+enum GemmMode : int {
+  kShrink = 0,   // S_run = X_block * A[a,e]^T       (gate_up_shrink / down_shrink)
+  kGateUp = 1,   // h = silu(gate) * up, gate/up = X W_gu[e]^T + S_run Bt_gu[a,e]^T (gate_up + expand)
+  kDown = 2,     // out_acc[t] += w * (h W_dn[e]^T + S_run Bt_dn[a,e]^T)            (down + expand)
+};
+
+constexpr int kKTile = 64;      // K elements per pipeline stage (one 128-byte swizzle row of bf16)
+constexpr int kRankChunk = 16;  // LoRA rank elements per MMA K-step
+
+// Parameters of one grouped-GEMM launch (passed by value, read-only on the device).
+struct GemmParams {
+  const int32_t* block_expert;  // [blocks]
+  const int32_t* block_runs;    // [blocks+1]
+  const int32_t* runs;          // [runs][4] {block, adapter, begin, end}
+  const int32_t* totals;        // {rows, blocks, runs, dropped}
+  const int32_t* sorted_p;      // [rows]
+  const float* topk_w;          // [T*k]
+  uint16_t* h_out;              // kGateUp: h rows in sorted order [rows][I] (bf16)
+  float* out_acc;               // kDown:   [T][H] fp32 accumulation
+  uint16_t* s_out;              // kShrink: [runs][BT][r_pad] (bf16), rows outside the run zero
+  int32_t* status;              // device status word (MOE_LORA_DEV_* bits)
+  int32_t K;                    // reduction length of the base GEMM (H or I)
+  int32_t n_feat;               // output features (I for kGateUp, H for kDown)
+  int32_t E;
+  int32_t k;
+  int32_t P;                    // T*k, the padding sentinel
+  int32_t r_pad;                // S row length (r_max rounded up to 16)
+  int32_t ranks[MOE_LORA_MAX_ADAPTERS];
+};
+
+// Tensor maps of one grouped-GEMM launch.
+struct GemmMaps {
+  CUtensorMap w;      // base weights (W_gu 4D / W_dn 3D / A 3D)
+  CUtensorMap tok;    // token rows in sorted order (x_sorted / h_sorted) 2D
+  CUtensorMap lw;     // LoRA expand weights (Bt_gu 4D / Bt_dn 3D)
+  CUtensorMap ls;     // S run tiles 3D
+};
+
+// Launchers (defined next to their kernels).
+cudaError_t launch_route(const float* logits, int64_t T, int E, int k, int32_t* ids, float* w,
+                         cudaStream_t s);
+
+struct AlignLaunch {
+  const int32_t* topk_ids;
+  const int32_t* lora_ids;
+  int64_t P;
+  int k, E, L, BM;
+  int ch_log2;                 // log2 of the chunk size
+  int nchunks;
+  uint32_t* chunk_keys;        // [nchunks << ch_log2]
+  int32_t* counts;             // [nchunks][E*(L+1)]
+  int32_t* chunk_invalid;      // [nchunks]
+  int32_t* bucket_total;       // [E*(L+1)]
+  int32_t* bucket_base;        // [E*(L+1)]
+  int32_t* run_base;           // [E*(L+1)]
+  int32_t* expert_n;           // [E]
+  moe_lora_align_buf out;
+};
+cudaError_t launch_align(const AlignLaunch& a, cudaStream_t s);
+
+cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* sorted_p, const int32_t* totals, int64_t max_rows,
+                               int H, int k, int P, uint16_t* x_sorted, cudaStream_t s);
+cudaError_t launch_finalize(const float* acc, uint16_t* out, int64_t n, cudaStream_t s);
+cudaError_t launch_gemm(int mode, int bt, const GemmMaps& maps, const GemmParams& prm, int64_t max_blocks,
+                        int64_t max_runs, cudaStream_t s);
+
+}  // namespace moe

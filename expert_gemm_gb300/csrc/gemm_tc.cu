@@ -1,0 +1,25 @@
+// gemm_tc.cu -- instantiations of the tcgen05 grouped GEMM and the launch dispatch.
+#include "gemm_tc.cuh"
+
+namespace moe {
+
+cudaError_t launch_gemm(int mode, int bt, const GemmMaps& maps, const GemmParams& prm, int64_t max_blocks,
+                        int64_t max_runs, cudaStream_t s) {
+#define MOE_GEMM_CASE(BT_, SWAP_)                                                                       \
+  if (bt == BT_) {                                                                                      \
+    switch (mode) {                                                                                     \
+      case kShrink: return launch_gemm_t<kShrink, SWAP_, BT_>(maps, prm, max_blocks, max_runs, s);     \
+      case kGateUp: return launch_gemm_t<kGateUp, SWAP_, BT_>(maps, prm, max_blocks, max_runs, s);     \
+      case kDown: return launch_gemm_t<kDown, SWAP_, BT_>(maps, prm, max_blocks, max_runs, s);         \
+      default: return cudaErrorInvalidValue;                                                            \
+    }                                                                                                   \
+  }
+  MOE_GEMM_CASE(16, true)
+  MOE_GEMM_CASE(32, true)
+  MOE_GEMM_CASE(64, true)
+  MOE_GEMM_CASE(128, false)
+#undef MOE_GEMM_CASE
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace moe

@@ -1,0 +1,552 @@
+// moe_lora.cu -- the C ABI (include/moe_lora.h): host-side validation, workspace
+// layout, TMA tensor-map encoding and the launch sequence of the MoE-LoRA layer.
+//
+// Launch sequence of moe_lora_forward (all on the caller's stream):
+//   gather    x rows into sorted (expert, adapter, pair) order; zero padding rows
+//   shrink    S_gu per adapter run = x_block A_gu[a,e]^T          (tcgen05)
+//   gate_up   h = silu(gate) * up, gate/up = x W_gu[e]^T + S_gu Bt_gu[a,e]^T (tcgen05)
+//   shrink    S_dn per adapter run = h_block A_dn[a,e]^T          (tcgen05)
+//   down      out_acc[t] += w * (h W_dn[e]^T + S_dn Bt_dn[a,e]^T)  (tcgen05)
+//   finalize  out = bf16(out_acc)
+#include <cudaTypedefs.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "common.cuh"
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int status, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof g_err, fmt, ap);
+  va_end(ap);
+  return status;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(MOE_LORA_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define MOE_CUDA(call)                                  \
+  do {                                                  \
+    cudaError_t e_ = (call);                            \
+    if (e_ != cudaSuccess) return cuda_fail(e_, #call); \
+  } while (0)
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+int get_encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (!g_encode) return fail(MOE_LORA_ECUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  return MOE_LORA_OK;
+}
+
+// The kernels are compiled for sm_103a only.
+int check_device() {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  int maj = 0, min = 0;
+  cudaDeviceGetAttribute(&maj, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&min, cudaDevAttrComputeCapabilityMinor, dev);
+  if (maj != 10 || min != 3)
+    return fail(MOE_LORA_EUNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a", dev, maj, min);
+  return MOE_LORA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+size_t up256(size_t n) { return (n + 255) & ~size_t(255); }
+
+int validate_dims(const moe_lora_dims* d) {
+  if (!d) return fail(MOE_LORA_EINVAL, "dims is NULL");
+  if (d->T < 0) return fail(MOE_LORA_EINVAL, "T = %lld < 0", (long long)d->T);
+  if (d->H <= 0 || d->H % 64) return fail(MOE_LORA_EINVAL, "H = %d must be a positive multiple of 64", d->H);
+  if (d->I <= 0 || d->I % 64) return fail(MOE_LORA_EINVAL, "I = %d must be a positive multiple of 64", d->I);
+  if (d->E < 1 || d->E > MOE_LORA_MAX_EXPERTS) return fail(MOE_LORA_EUNSUPPORTED, "E = %d outside [1, %d]", d->E, MOE_LORA_MAX_EXPERTS);
+  if (d->k < 1 || d->k > d->E || d->k > MOE_LORA_MAX_TOPK)
+    return fail(MOE_LORA_EINVAL, "k = %d outside [1, min(E, %d)]", d->k, MOE_LORA_MAX_TOPK);
+  if (d->L < 0 || d->L > MOE_LORA_MAX_ADAPTERS) return fail(MOE_LORA_EUNSUPPORTED, "L = %d outside [0, %d]", d->L, MOE_LORA_MAX_ADAPTERS);
+  if (d->block_m != 16 && d->block_m != 32 && d->block_m != 64 && d->block_m != 128)
+    return fail(MOE_LORA_EUNSUPPORTED, "block_m = %d not in {16, 32, 64, 128}", d->block_m);
+  if (d->T * (int64_t)d->k >= (int64_t(1) << 30)) return fail(MOE_LORA_EUNSUPPORTED, "T*k too large");
+  if (d->L > 0) {
+    if (d->r_max < 8 || d->r_max > MOE_LORA_MAX_RANK || d->r_max % 8)
+      return fail(MOE_LORA_EUNSUPPORTED, "r_max = %d must be a multiple of 8 in [8, %d]", d->r_max, MOE_LORA_MAX_RANK);
+    if (!d->ranks) return fail(MOE_LORA_EINVAL, "ranks is NULL with L = %d", d->L);
+    for (int a = 0; a < d->L; ++a)
+      if (d->ranks[a] < 1 || d->ranks[a] > d->r_max)
+        return fail(MOE_LORA_EINVAL, "ranks[%d] = %d outside [1, r_max = %d]", a, d->ranks[a], d->r_max);
+  }
+  return MOE_LORA_OK;
+}
+
+struct Caps {
+  int64_t rows, blocks, runs;
+};
+Caps capacity(const moe_lora_dims* d) {
+  const int64_t P = d->T * d->k, BM = d->block_m;
+  int64_t rows = P + (P < d->E ? P : d->E) * (BM - 1);
+  rows = (rows + BM - 1) / BM * BM;
+  const int64_t blocks = rows / BM;
+  int64_t runs = blocks + (int64_t)d->E * d->L;
+  if (runs > P) runs = P;
+  if (d->L == 0) runs = 0;
+  return {rows, blocks, runs};
+}
+
+int r_pad_of(const moe_lora_dims* d) { return d->L > 0 ? (d->r_max + 15) / 16 * 16 : 16; }
+
+// ---- align scratch layout
+struct AlignLayout {
+  int ch_log2, nchunks;
+  size_t keys, counts, invalid, btotal, bbase, rbase, expn, bytes;
+};
+AlignLayout align_layout(const moe_lora_dims* d) {
+  AlignLayout l{};
+  const int64_t P = d->T * d->k;
+  int lg = 5;
+  while ((int64_t(1) << lg) < P && lg < 12) ++lg;
+  l.ch_log2 = lg;
+  l.nchunks = (int)((P + (int64_t(1) << lg) - 1) >> lg);
+  const size_t NB = (size_t)d->E * (d->L + 1);
+  size_t off = 0;
+  l.keys = off;    off += up256((size_t)l.nchunks << lg << 2);
+  l.counts = off;  off += up256((size_t)l.nchunks * NB * 4);
+  l.invalid = off; off += up256((size_t)l.nchunks * 4);
+  l.btotal = off;  off += up256(NB * 4);
+  l.bbase = off;   off += up256(NB * 4);
+  l.rbase = off;   off += up256(NB * 4);
+  l.expn = off;    off += up256((size_t)d->E * 4);
+  l.bytes = off;
+  return l;
+}
+
+// ---- forward scratch layout
+struct FwdLayout {
+  size_t xs, hs, sgu, sdn, acc, bytes;
+};
+FwdLayout fwd_layout(const moe_lora_dims* d) {
+  const Caps c = capacity(d);
+  FwdLayout l{};
+  size_t off = 0;
+  const size_t s_tile = (size_t)d->block_m * r_pad_of(d) * 2;
+  l.xs = off;  off += up256((size_t)c.rows * d->H * 2);
+  l.hs = off;  off += up256((size_t)c.rows * d->I * 2);
+  l.sgu = off; off += up256((size_t)c.runs * s_tile);
+  l.sdn = off; off += up256((size_t)c.runs * s_tile);
+  l.acc = off; off += up256((size_t)d->T * d->H * 4);
+  l.bytes = off;
+  return l;
+}
+
+// ---- tensor maps
+int encode(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims, const uint64_t* strides,
+           const uint32_t* box, CUtensorMapSwizzle sw, const char* what) {
+  cuuint64_t gd[5];
+  cuuint64_t gs[4];
+  cuuint32_t bx[5], es[5];
+  for (int i = 0; i < rank; ++i) {
+    gd[i] = dims[i];
+    bx[i] = box[i];
+    es[i] = 1;
+  }
+  for (int i = 0; i < rank - 1; ++i) gs[i] = strides[i];
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), gd, gs, bx, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MOE_LORA_ECUDA, "cuTensorMapEncodeTiled(%s) failed with %d", what, (int)r);
+  return MOE_LORA_OK;
+}
+
+#define MOE_TRY(x)                         \
+  do {                                     \
+    int st_ = (x);                         \
+    if (st_ != MOE_LORA_OK) return st_;    \
+  } while (0)
+
+int check_ptr(const void* p, const char* name, bool need16) {
+  if (!p) return fail(MOE_LORA_EINVAL, "%s is NULL", name);
+  if (need16 && !aligned16(p)) return fail(MOE_LORA_EALIGN, "%s is not 16-byte aligned", name);
+  return MOE_LORA_OK;
+}
+
+int check_align_buf(const moe_lora_align_buf* b) {
+  if (!b) return fail(MOE_LORA_EINVAL, "align buffer struct is NULL");
+  MOE_TRY(check_ptr(b->sorted_p, "sorted_p", false));
+  MOE_TRY(check_ptr(b->expert_begin, "expert_begin", false));
+  MOE_TRY(check_ptr(b->block_expert, "block_expert", false));
+  MOE_TRY(check_ptr(b->block_runs, "block_runs", false));
+  MOE_TRY(check_ptr(b->runs, "runs", false));
+  MOE_TRY(check_ptr(b->totals, "totals", false));
+  return MOE_LORA_OK;
+}
+
+int do_route(const float* logits, int64_t T, int32_t E, int32_t k, int32_t* ids, float* w, cudaStream_t s) {
+  if (T < 0 || E < 1 || E > MOE_LORA_MAX_EXPERTS || k < 1 || k > E || k > MOE_LORA_MAX_TOPK)
+    return fail(MOE_LORA_EINVAL, "route: T=%lld E=%d k=%d out of range", (long long)T, E, k);
+  if (T == 0) return MOE_LORA_OK;
+  MOE_TRY(check_ptr(logits, "logits", false));
+  MOE_TRY(check_ptr(ids, "topk_ids", false));
+  MOE_TRY(check_ptr(w, "topk_w", false));
+  MOE_TRY(check_device());
+  cudaError_t e = moe::launch_route(logits, T, E, k, ids, w, s);
+  if (e != cudaSuccess) return cuda_fail(e, "route kernel launch");
+  return MOE_LORA_OK;
+}
+
+int do_align(const moe_lora_dims* d, const int32_t* topk_ids, const int32_t* lora_ids, const moe_lora_align_buf* out,
+             void* ws, size_t ws_bytes, cudaStream_t s) {
+  MOE_TRY(validate_dims(d));
+  MOE_TRY(check_align_buf(out));
+  const AlignLayout l = align_layout(d);
+  if (d->T > 0) {
+    MOE_TRY(check_ptr(topk_ids, "topk_ids", false));
+    MOE_TRY(check_ptr(lora_ids, "lora_ids", false));
+  }
+  MOE_TRY(check_ptr(ws, "workspace", true));
+  if (ws_bytes < l.bytes) return fail(MOE_LORA_EWORKSPACE, "align workspace %zu < %zu bytes", ws_bytes, l.bytes);
+  MOE_TRY(check_device());
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  moe::AlignLaunch a{};
+  a.topk_ids = topk_ids;
+  a.lora_ids = lora_ids;
+  a.P = d->T * d->k;
+  a.k = d->k;
+  a.E = d->E;
+  a.L = d->L;
+  a.BM = d->block_m;
+  a.ch_log2 = l.ch_log2;
+  a.nchunks = l.nchunks;
+  a.chunk_keys = reinterpret_cast<uint32_t*>(base + l.keys);
+  a.counts = reinterpret_cast<int32_t*>(base + l.counts);
+  a.chunk_invalid = reinterpret_cast<int32_t*>(base + l.invalid);
+  a.bucket_total = reinterpret_cast<int32_t*>(base + l.btotal);
+  a.bucket_base = reinterpret_cast<int32_t*>(base + l.bbase);
+  a.run_base = reinterpret_cast<int32_t*>(base + l.rbase);
+  a.expert_n = reinterpret_cast<int32_t*>(base + l.expn);
+  a.out = *out;
+  cudaError_t e = moe::launch_align(a, s);
+  if (e != cudaSuccess) return cuda_fail(e, "align kernel launch");
+  return MOE_LORA_OK;
+}
+
+int do_forward(const moe_lora_dims* d, const uint16_t* x, const float* topk_w, const moe_lora_align_buf* al,
+               const uint16_t* W_gu, const uint16_t* W_dn, const uint16_t* A_gu, const uint16_t* Bt_gu,
+               const uint16_t* A_dn, const uint16_t* Bt_dn, uint16_t* out, void* ws, size_t ws_bytes,
+               int32_t* dev_status, cudaStream_t s, void* const* ev) {
+  MOE_TRY(validate_dims(d));
+  MOE_TRY(check_align_buf(al));
+  MOE_TRY(check_ptr(dev_status, "dev_status", false));
+  const FwdLayout l = fwd_layout(d);
+  const Caps cap = capacity(d);
+  if (d->T == 0) {
+    MOE_TRY(check_device());
+    MOE_CUDA(cudaMemsetAsync(dev_status, 0, sizeof(int32_t), s));
+    return MOE_LORA_OK;
+  }
+  MOE_TRY(check_ptr(x, "x", true));
+  MOE_TRY(check_ptr(topk_w, "topk_w", false));
+  MOE_TRY(check_ptr(W_gu, "W_gu", true));
+  MOE_TRY(check_ptr(W_dn, "W_dn", true));
+  MOE_TRY(check_ptr(out, "out", true));
+  MOE_TRY(check_ptr(ws, "workspace", true));
+  if (d->L > 0) {
+    MOE_TRY(check_ptr(A_gu, "A_gu", true));
+    MOE_TRY(check_ptr(Bt_gu, "Bt_gu", true));
+    MOE_TRY(check_ptr(A_dn, "A_dn", true));
+    MOE_TRY(check_ptr(Bt_dn, "Bt_dn", true));
+  }
+  if (ws_bytes < l.bytes) return fail(MOE_LORA_EWORKSPACE, "forward workspace %zu < %zu bytes", ws_bytes, l.bytes);
+  MOE_TRY(check_device());
+  MOE_TRY(get_encoder());
+
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  uint16_t* xs = reinterpret_cast<uint16_t*>(base + l.xs);
+  uint16_t* hs = reinterpret_cast<uint16_t*>(base + l.hs);
+  uint16_t* sgu = reinterpret_cast<uint16_t*>(base + l.sgu);
+  uint16_t* sdn = reinterpret_cast<uint16_t*>(base + l.sdn);
+  float* acc = reinterpret_cast<float*>(base + l.acc);
+  const int BT = d->block_m;
+  const uint64_t H = d->H, I = d->I, E = d->E, LE = (uint64_t)d->L * d->E, R = d->r_max;
+  const uint64_t rows = cap.rows, RP = r_pad_of(d);
+  const uint64_t nruns = cap.runs > 0 ? cap.runs : 1;
+
+  // tensor maps (dims innermost first; strides in bytes for dims 1..rank-1)
+  moe::GemmMaps m_sgu{}, m_gu{}, m_sdn{}, m_dn{};
+  {
+    const uint64_t dm[4] = {H, I, 2, E}, st[3] = {H * 2, I * H * 2, 2 * I * H * 2};
+    const uint32_t bx[4] = {64, 128, 1, 1};
+    MOE_TRY(encode(&m_gu.w, W_gu, 4, dm, st, bx, CU_TENSOR_MAP_SWIZZLE_128B, "W_gu"));
+  }
+  {
+    const uint64_t dm[3] = {I, H, E}, st[2] = {I * 2, H * I * 2};
+    const uint32_t bx[3] = {64, 128, 1};
+    MOE_TRY(encode(&m_dn.w, W_dn, 3, dm, st, bx, CU_TENSOR_MAP_SWIZZLE_128B, "W_dn"));
+  }
+  {
+    const uint64_t dm[2] = {H, rows}, st[1] = {H * 2};
+    const uint32_t bx[2] = {64, (uint32_t)BT};
+    MOE_TRY(encode(&m_gu.tok, xs, 2, dm, st, bx, CU_TENSOR_MAP_SWIZZLE_128B, "x_sorted"));
+  }
+  {
+    const uint64_t dm[2] = {I, rows}, st[1] = {I * 2};
+    const uint32_t bx[2] = {64, (uint32_t)BT};
+    MOE_TRY(encode(&m_dn.tok, hs, 2, dm, st, bx, CU_TENSOR_MAP_SWIZZLE_128B, "h_sorted"));
+  }
+  m_sgu.tok = m_gu.tok;
+  m_sdn.tok = m_dn.tok;
+  if (d->L > 0) {
+    {
+      const uint64_t dm[3] = {H, R, LE}, st[2] = {H * 2, R * H * 2};
+      const uint32_t bx[3] = {64, 16, 1};
+      MOE_TRY(encode(&m_sgu.w, A_gu, 3, dm, st, bx, CU_TENSOR_MAP_SWIZZLE_128B, "A_gu"));
+    }
+    {
+      const uint64_t dm[3] = {I, R, LE}, st[2] = {I * 2, R * I * 2};
+      const uint32_t bx[3] = {64, 16, 1};
+      MOE_TRY(encode(&m_sdn.w, A_dn, 3, dm, st, bx, CU_TENSOR_MAP_SWIZZLE_128B, "A_dn"));
+    }
+    {
+      const uint64_t dm[4] = {R, I, 2, LE}, st[3] = {R * 2, I * R * 2, 2 * I * R * 2};
+      const uint32_t bx[4] = {16, 128, 1, 1};
+      MOE_TRY(encode(&m_gu.lw, Bt_gu, 4, dm, st, bx, CU_TENSOR_MAP_SWIZZLE_32B, "Bt_gu"));
+    }
+    {
+      const uint64_t dm[3] = {R, H, LE}, st[2] = {R * 2, H * R * 2};
+      const uint32_t bx[3] = {16, 128, 1};
+      MOE_TRY(encode(&m_dn.lw, Bt_dn, 3, dm, st, bx, CU_TENSOR_MAP_SWIZZLE_32B, "Bt_dn"));
+    }
+    {
+      const uint64_t dm[3] = {RP, (uint64_t)BT, nruns}, st[2] = {RP * 2, (uint64_t)BT * RP * 2};
+      const uint32_t bx[3] = {16, (uint32_t)BT, 1};
+      MOE_TRY(encode(&m_gu.ls, sgu, 3, dm, st, bx, CU_TENSOR_MAP_SWIZZLE_32B, "S_gu"));
+      MOE_TRY(encode(&m_dn.ls, sdn, 3, dm, st, bx, CU_TENSOR_MAP_SWIZZLE_32B, "S_dn"));
+    }
+  } else {
+    // No adapter runs exist, so these maps are never loaded through; keep them valid.
+    m_gu.lw = m_gu.ls = m_gu.w;
+    m_dn.lw = m_dn.ls = m_dn.w;
+  }
+  m_sgu.lw = m_sgu.ls = m_sgu.w;
+  m_sdn.lw = m_sdn.ls = m_sdn.w;
+
+  moe::GemmParams p{};
+  p.block_expert = al->block_expert;
+  p.block_runs = al->block_runs;
+  p.runs = al->runs;
+  p.totals = al->totals;
+  p.sorted_p = al->sorted_p;
+  p.topk_w = topk_w;
+  p.status = dev_status;
+  p.E = d->E;
+  p.k = d->k;
+  p.P = (int32_t)(d->T * d->k);
+  p.r_pad = (int32_t)RP;
+  for (int a = 0; a < d->L; ++a) p.ranks[a] = d->ranks[a];
+
+  auto mark = [&](int i) -> cudaError_t {
+    return ev ? cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), s) : cudaSuccess;
+  };
+  MOE_CUDA(mark(0));
+  MOE_CUDA(cudaMemsetAsync(dev_status, 0, sizeof(int32_t), s));
+  MOE_CUDA(cudaMemsetAsync(acc, 0, (size_t)d->T * d->H * 4, s));
+  MOE_CUDA(moe::launch_gather_rows(x, al->sorted_p, al->totals, cap.rows, d->H, d->k, p.P, xs, s));
+  MOE_CUDA(mark(1 + MOE_LORA_STAGE_GATHER));
+
+  if (d->L > 0) {
+    moe::GemmParams q = p;
+    q.K = d->H;
+    q.s_out = sgu;
+    MOE_CUDA(moe::launch_gemm(moe::kShrink, BT, m_sgu, q, cap.blocks, cap.runs, s));
+  }
+  MOE_CUDA(mark(1 + MOE_LORA_STAGE_SHRINK_GU));
+  {
+    moe::GemmParams q = p;
+    q.K = d->H;
+    q.n_feat = d->I;
+    q.h_out = hs;
+    MOE_CUDA(moe::launch_gemm(moe::kGateUp, BT, m_gu, q, cap.blocks, cap.runs, s));
+  }
+  MOE_CUDA(mark(1 + MOE_LORA_STAGE_GATE_UP));
+  if (d->L > 0) {
+    moe::GemmParams q = p;
+    q.K = d->I;
+    q.s_out = sdn;
+    MOE_CUDA(moe::launch_gemm(moe::kShrink, BT, m_sdn, q, cap.blocks, cap.runs, s));
+  }
+  MOE_CUDA(mark(1 + MOE_LORA_STAGE_SHRINK_DN));
+  {
+    moe::GemmParams q = p;
+    q.K = d->I;
+    q.n_feat = d->H;
+    q.out_acc = acc;
+    MOE_CUDA(moe::launch_gemm(moe::kDown, BT, m_dn, q, cap.blocks, cap.runs, s));
+  }
+  MOE_CUDA(mark(1 + MOE_LORA_STAGE_DOWN));
+  MOE_CUDA(moe::launch_finalize(acc, out, d->T * d->H, s));
+  MOE_CUDA(mark(1 + MOE_LORA_STAGE_FINALIZE));
+  return MOE_LORA_OK;
+}
+
+// ---- layer_host workspace: [align | forward | inputs | route out | align arrays | out | status]
+struct LayerLayout {
+  size_t align, fwd, logits, lora, x, ids, w, sp, eb, be, br, runs, tot, out, status, bytes;
+};
+LayerLayout layer_layout(const moe_lora_dims* d) {
+  const AlignLayout a = align_layout(d);
+  const FwdLayout f = fwd_layout(d);
+  const Caps c = capacity(d);
+  LayerLayout l{};
+  size_t off = 0;
+  l.align = off;  off += up256(a.bytes);
+  l.fwd = off;    off += up256(f.bytes);
+  l.logits = off; off += up256((size_t)d->T * d->E * 4);
+  l.lora = off;   off += up256((size_t)d->T * 4);
+  l.x = off;      off += up256((size_t)d->T * d->H * 2);
+  l.ids = off;    off += up256((size_t)d->T * d->k * 4);
+  l.w = off;      off += up256((size_t)d->T * d->k * 4);
+  l.sp = off;     off += up256((size_t)c.rows * 4);
+  l.eb = off;     off += up256((size_t)(d->E + 1) * 4);
+  l.be = off;     off += up256((size_t)c.blocks * 4);
+  l.br = off;     off += up256((size_t)(c.blocks + 1) * 4);
+  l.runs = off;   off += up256((size_t)c.runs * 16);
+  l.tot = off;    off += up256(4 * 4);
+  l.out = off;    off += up256((size_t)d->T * d->H * 2);
+  l.status = off; off += up256(4);
+  l.bytes = off;
+  return l;
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_lora_version(void) { return 100; }
+
+const char* moe_lora_status_string(int status) {
+  switch (status) {
+    case MOE_LORA_OK: return "ok";
+    case MOE_LORA_EINVAL: return "invalid argument";
+    case MOE_LORA_EALIGN: return "pointer not 16-byte aligned";
+    case MOE_LORA_EWORKSPACE: return "workspace too small";
+    case MOE_LORA_EUNSUPPORTED: return "unsupported shape or device";
+    case MOE_LORA_ECUDA: return "CUDA error";
+    case MOE_LORA_EDEVICE: return "device reported an error";
+    default: return "unknown status";
+  }
+}
+
+const char* moe_lora_last_error(void) { return g_err; }
+
+int32_t moe_lora_pick_block_m(int64_t T, int32_t k, int32_t E) {
+  if (E <= 0 || k <= 0 || T <= 0) return 16;
+  const double per_expert = (double)T * k / E;
+  if (per_expert >= 96.0) return 128;
+  if (per_expert > 24.0) return 64;
+  if (per_expert > 10.0) return 32;
+  return 16;
+}
+
+int moe_lora_align_capacity(const moe_lora_dims* d, int64_t* max_rows, int64_t* max_blocks, int64_t* max_runs) {
+  MOE_TRY(validate_dims(d));
+  const Caps c = capacity(d);
+  if (max_rows) *max_rows = c.rows;
+  if (max_blocks) *max_blocks = c.blocks;
+  if (max_runs) *max_runs = c.runs;
+  return MOE_LORA_OK;
+}
+
+int moe_lora_workspace_size(const moe_lora_dims* d, size_t* align_bytes, size_t* forward_bytes) {
+  MOE_TRY(validate_dims(d));
+  if (align_bytes) *align_bytes = align_layout(d).bytes;
+  if (forward_bytes) *forward_bytes = fwd_layout(d).bytes;
+  return MOE_LORA_OK;
+}
+
+int moe_lora_layer_workspace_size(const moe_lora_dims* d, size_t* bytes) {
+  MOE_TRY(validate_dims(d));
+  if (!bytes) return fail(MOE_LORA_EINVAL, "bytes is NULL");
+  *bytes = layer_layout(d).bytes;
+  return MOE_LORA_OK;
+}
+
+int moe_lora_route(const float* logits, int64_t T, int32_t E, int32_t k, int32_t* topk_ids, float* topk_w,
+                   void* stream) {
+  return do_route(logits, T, E, k, topk_ids, topk_w, static_cast<cudaStream_t>(stream));
+}
+
+int moe_lora_align(const moe_lora_dims* d, const int32_t* topk_ids, const int32_t* lora_ids,
+                   const moe_lora_align_buf* out, void* workspace, size_t workspace_bytes, void* stream) {
+  return do_align(d, topk_ids, lora_ids, out, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+int moe_lora_forward(const moe_lora_dims* d, const uint16_t* x, const float* topk_w,
+                     const moe_lora_align_buf* aligned, const uint16_t* W_gu, const uint16_t* W_dn,
+                     const uint16_t* A_gu, const uint16_t* Bt_gu, const uint16_t* A_dn, const uint16_t* Bt_dn,
+                     uint16_t* out, void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream,
+                     void* const* stage_events) {
+  return do_forward(d, x, topk_w, aligned, W_gu, W_dn, A_gu, Bt_gu, A_dn, Bt_dn, out, workspace, workspace_bytes,
+                    dev_status, static_cast<cudaStream_t>(stream), stage_events);
+}
+
+int moe_lora_layer_host(const moe_lora_dims* d, const float* logits_host, const int32_t* lora_ids_host,
+                        const uint16_t* x_host, const uint16_t* W_gu, const uint16_t* W_dn, const uint16_t* A_gu,
+                        const uint16_t* Bt_gu, const uint16_t* A_dn, const uint16_t* Bt_dn, uint16_t* out_host,
+                        void* workspace, size_t workspace_bytes, int64_t* dropped, void* stream) {
+  MOE_TRY(validate_dims(d));
+  const LayerLayout l = layer_layout(d);
+  MOE_TRY(check_ptr(workspace, "workspace", true));
+  if (workspace_bytes < l.bytes) return fail(MOE_LORA_EWORKSPACE, "layer workspace %zu < %zu bytes", workspace_bytes, l.bytes);
+  if (d->T > 0) {
+    MOE_TRY(check_ptr(logits_host, "logits_host", false));
+    MOE_TRY(check_ptr(lora_ids_host, "lora_ids_host", false));
+    MOE_TRY(check_ptr(x_host, "x_host", false));
+    MOE_TRY(check_ptr(out_host, "out_host", false));
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* b = static_cast<uint8_t*>(workspace);
+  float* logits = reinterpret_cast<float*>(b + l.logits);
+  int32_t* lora = reinterpret_cast<int32_t*>(b + l.lora);
+  uint16_t* x = reinterpret_cast<uint16_t*>(b + l.x);
+  int32_t* ids = reinterpret_cast<int32_t*>(b + l.ids);
+  float* w = reinterpret_cast<float*>(b + l.w);
+  uint16_t* out = reinterpret_cast<uint16_t*>(b + l.out);
+  int32_t* status = reinterpret_cast<int32_t*>(b + l.status);
+  moe_lora_align_buf al{reinterpret_cast<int32_t*>(b + l.sp), reinterpret_cast<int32_t*>(b + l.eb),
+                        reinterpret_cast<int32_t*>(b + l.be), reinterpret_cast<int32_t*>(b + l.br),
+                        reinterpret_cast<int32_t*>(b + l.runs), reinterpret_cast<int32_t*>(b + l.tot)};
+  const size_t T = (size_t)d->T;
+  if (T > 0) {
+    MOE_CUDA(cudaMemcpyAsync(logits, logits_host, T * d->E * 4, cudaMemcpyHostToDevice, s));
+    MOE_CUDA(cudaMemcpyAsync(lora, lora_ids_host, T * 4, cudaMemcpyHostToDevice, s));
+    MOE_CUDA(cudaMemcpyAsync(x, x_host, T * d->H * 2, cudaMemcpyHostToDevice, s));
+    MOE_TRY(do_route(logits, d->T, d->E, d->k, ids, w, s));
+  }
+  MOE_TRY(do_align(d, ids, lora, &al, b + l.align, l.fwd - l.align, s));
+  MOE_TRY(do_forward(d, x, w, &al, W_gu, W_dn, A_gu, Bt_gu, A_dn, Bt_dn, out, b + l.fwd, l.logits - l.fwd, status, s,
+                      nullptr));
+  int32_t host_status = 0, tot[4] = {0, 0, 0, 0};
+  if (T > 0) MOE_CUDA(cudaMemcpyAsync(out_host, out, T * d->H * 2, cudaMemcpyDeviceToHost, s));
+  MOE_CUDA(cudaMemcpyAsync(&host_status, status, 4, cudaMemcpyDeviceToHost, s));
+  MOE_CUDA(cudaMemcpyAsync(tot, al.totals, 16, cudaMemcpyDeviceToHost, s));
+  MOE_CUDA(cudaStreamSynchronize(s));
+  if (dropped) *dropped = tot[3];
+  if (host_status != 0) return fail(MOE_LORA_EDEVICE, "device status 0x%x", host_status);
+  return MOE_LORA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,59 @@
+// rows.cu -- row gather into sorted order and the final fp32 -> bf16 conversion.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+// x_sorted[row] = x[sorted_p[row] / k] for real rows, zero for padding rows.
+// One warp per row, 16-byte vectors.
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ sorted_p,
+                                                          const int32_t* __restrict__ totals, int64_t max_rows, int vec_per_row,
+                                                          int k, int P, uint4* __restrict__ xs) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (row >= max_rows || row >= totals[0]) return;
+  const int p = sorted_p[row];
+  uint4* dst = xs + row * vec_per_row;
+  if (p >= P) {
+    for (int v = lane; v < vec_per_row; v += 32) dst[v] = make_uint4(0, 0, 0, 0);
+  } else {
+    const uint4* src = x + static_cast<int64_t>(p / k) * vec_per_row;
+    for (int v = lane; v < vec_per_row; v += 32) dst[v] = __ldg(src + v);
+  }
+}
+
+__global__ void __launch_bounds__(256) finalize_kernel(const float4* __restrict__ acc, uint2* __restrict__ out, int64_t n4) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const float4 v = acc[i];
+    __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y);
+    __nv_bfloat162 b = __floats2bfloat162_rn(v.z, v.w);
+    out[i] = make_uint2(*reinterpret_cast<uint32_t*>(&a), *reinterpret_cast<uint32_t*>(&b));
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* sorted_p, const int32_t* totals, int64_t max_rows,
+                               int H, int k, int P, uint16_t* x_sorted, cudaStream_t s) {
+  if (max_rows <= 0) return cudaSuccess;
+  const int rows_per_cta = 8;
+  const int64_t grid = (max_rows + rows_per_cta - 1) / rows_per_cta;
+  gather_rows_kernel<<<static_cast<unsigned>(grid), rows_per_cta * 32, 0, s>>>(
+      reinterpret_cast<const uint4*>(x), sorted_p, totals, max_rows, H / 8, k, P, reinterpret_cast<uint4*>(x_sorted));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_finalize(const float* acc, uint16_t* out, int64_t n, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  const int64_t n4 = n / 4;
+  int64_t grid = (n4 + 255) / 256;
+  if (grid > 152 * 8) grid = 152 * 8;
+  finalize_kernel<<<static_cast<unsigned>(grid), 256, 0, s>>>(reinterpret_cast<const float4*>(acc),
+                                                             reinterpret_cast<uint2*>(out), n4);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,209 @@
+/*
+ * moe_lora.h -- C ABI of the GB300 (sm_103a) fused Mixture-of-Experts layer with
+ * per-request LoRA adapters.
+ *
+ * Sources (cited by page title and section):
+ *   [AWS] AWS Machine Learning Blog, "Efficiently serve dozens of fine-tuned models
+ *         with vLLM on Amazon SageMaker AI and Amazon Bedrock".
+ *   [KO]  agentlenshq.com, "vLLM MoE 모델을 위한 Multi-LoRA 서빙".
+ *   [ZH]  setupai.cc, "vLLM 多 LoRA 提升 AWS 上 MoE 模型服務".
+ *
+ * The layer.  Each of T tokens is routed to k of E experts and carries one adapter
+ * id in [-1, L) (-1 = no adapter; adapters are swapped per request, [AWS]
+ * introduction).  Each expert is a two-stage FFN that expands the hidden state to
+ * an intermediate space (gate_up, H -> 2I) and compresses it back (down, I -> H)
+ * ([KO] "MoE 모델을 위한 Multi-LoRA 서빙").  LoRA turns XW into XW + XAB on both
+ * projections ([ZH] "增強重點摘要"), i.e. four extra ops per expert:
+ * gate_up_shrink, gate_up_expand, down_shrink, down_expand ([KO] "Amazon 전용 튜닝").
+ * For a pair (token t, expert e) with adapter a and rank r = ranks[a]:
+ *     g = W_gu[e] x_t + Bt_gu[a,e][:, :r] (A_gu[a,e][:r, :] x_t)          (2I)
+ *     h = silu(g[0:I]) * g[I:2I]                                        (I)
+ *     d = W_dn[e] h   + Bt_dn[a,e][:, :r] (A_dn[a,e][:r, :] h)            (H)
+ *     out_t = sum_j w_{t,j} d_{t,j}
+ * where the weights w are the softmax over the E router logits, kept for the k
+ * largest and renormalised; the router and the aggregation of expert outputs are
+ * [AWS] "Implementing multi-LoRA inference for MoE models in vLLM".
+ *
+ * Conventions for every entry point:
+ *   - bf16 tensors are passed as their 16-bit patterns (uint16_t).
+ *   - All tensors are dense, row-major, with the shapes stated.  Device pointers
+ *     must be 16-byte aligned (the kernels stream them with TMA).
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Device work is
+ *     enqueued asynchronously on it; nothing is synchronised unless stated.
+ *   - Ownership: the caller allocates every buffer; the library never allocates
+ *     device or pinned memory and keeps no per-call state.  Calls on different
+ *     streams with different buffers may run concurrently.
+ *   - Errors detectable on the host return a non-zero status before anything is
+ *     enqueued; moe_lora_last_error() then describes it (per thread).
+ *   - Kernels never trap.  Conditions found on the device (invalid ids, a pipeline
+ *     wait that timed out) are reported in `dev_status`, to be read by the caller
+ *     after synchronising.
+ */
+#ifndef MOE_LORA_H
+#define MOE_LORA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---------------------------------------------------------------- status -- */
+enum {
+    MOE_LORA_OK = 0,
+    MOE_LORA_EINVAL = 1,        /* null pointer, size out of range, bad rank           */
+    MOE_LORA_EALIGN = 2,        /* a device pointer is not 16-byte aligned            */
+    MOE_LORA_EWORKSPACE = 3,    /* workspace smaller than moe_lora_workspace_size()    */
+    MOE_LORA_EUNSUPPORTED = 4,  /* shape outside the compiled kernels (see limits)     */
+    MOE_LORA_ECUDA = 5,         /* a CUDA runtime call failed                          */
+    MOE_LORA_EDEVICE = 6        /* the device reported an error in dev_status          */
+};
+
+/* Bits of the forward call's device status word (dropped pairs are in totals[3]). */
+#define MOE_LORA_DEV_TIMEOUT 0x1   /* a bounded pipeline wait expired; outputs invalid */
+
+/* Stages of moe_lora_forward, in launch order (see stage_events). */
+#define MOE_LORA_STAGE_GATHER 0      /* x rows into sorted order               */
+#define MOE_LORA_STAGE_SHRINK_GU 1   /* gate_up_shrink                         */
+#define MOE_LORA_STAGE_GATE_UP 2     /* gate_up GEMM + expand + SiLU gating    */
+#define MOE_LORA_STAGE_SHRINK_DN 3   /* down_shrink                            */
+#define MOE_LORA_STAGE_DOWN 4        /* down GEMM + expand + weighted combine  */
+#define MOE_LORA_STAGE_FINALIZE 5    /* fp32 accumulation -> bf16 output       */
+#define MOE_LORA_NUM_STAGES 6
+
+/* Limits of the compiled kernels (MOE_LORA_EUNSUPPORTED beyond them). */
+#define MOE_LORA_MAX_ADAPTERS 256  /* L                                    */
+#define MOE_LORA_MAX_RANK 64       /* r_max                                */
+#define MOE_LORA_MAX_EXPERTS 1024  /* E                                    */
+#define MOE_LORA_MAX_TOPK 32       /* k                                    */
+
+/* ---------------------------------------------------------------- shapes -- */
+typedef struct moe_lora_dims {
+    int64_t T;        /* tokens, >= 0                                                   */
+    int32_t H;        /* hidden size, multiple of 64                                    */
+    int32_t I;        /* expert intermediate size, multiple of 64                       */
+    int32_t E;        /* experts, 1..MOE_LORA_MAX_EXPERTS                               */
+    int32_t k;        /* experts per token, 1..min(E, MOE_LORA_MAX_TOPK)                */
+    int32_t L;        /* adapters, 0..MOE_LORA_MAX_ADAPTERS                             */
+    int32_t r_max;    /* storage rank: rows of A, columns of Bt; multiple of 8, <= 64   */
+    int32_t block_m;  /* rows per align block: 16, 32, 64 (weight-streaming kernels)    */
+                      /* or 128 (token-tiled kernels); see moe_lora_pick_block_m        */
+    const int32_t *ranks; /* HOST array [L]: rank of adapter a, 1 <= ranks[a] <= r_max  */
+} moe_lora_dims;
+
+/*
+ * Output of moe_lora_align: the (expert, adapter) compound-sparsity layout
+ * ([AWS] "Tuning kernel configurations for Amazon SageMaker AI and Amazon
+ * Bedrock": the extra LoRA-index grid dimension and the sparsity of many
+ * adapters; [KO] "MoE 모델을 위한 Multi-LoRA 서빙").  All arrays are device int32,
+ * caller-allocated with the capacities of moe_lora_align_capacity().
+ *   Pair p = t*k + j joins expert topk_ids[p] and adapter lora_ids[t]; a pair is
+ *   valid when the expert is in [0, E) and the adapter in [-1, L).  Valid pairs are
+ *   sorted by (expert, adapter, p); each expert's rows are padded to a multiple of
+ *   block_m with the sentinel P = T*k.
+ */
+typedef struct moe_lora_align_buf {
+    int32_t *sorted_p;     /* [max_rows]   pair index of each row, P for padding        */
+    int32_t *expert_begin; /* [E+1]        first row of each expert; [E] = rows         */
+    int32_t *block_expert; /* [max_blocks] expert of each block_m-row block             */
+    int32_t *block_runs;   /* [max_blocks+1] first run of each block (CSR into runs)    */
+    int32_t *runs;         /* [max_runs][4] {block, adapter, begin_row, end_row}: maximal
+                              stretches of one adapter >= 0 inside one block, in row order */
+    int32_t *totals;       /* [4] {rows, blocks, runs, dropped pairs}                   */
+} moe_lora_align_buf;
+
+/* ----------------------------------------------------------- size queries -- */
+
+/* Capacities of the align arrays for these dims.  Returns a status. */
+int moe_lora_align_capacity(const moe_lora_dims *d, int64_t *max_rows, int64_t *max_blocks,
+                            int64_t *max_runs);
+
+/* Device scratch bytes needed by moe_lora_align and by moe_lora_forward (the two
+ * use disjoint regions, so one buffer of align_bytes + forward_bytes serves both,
+ * with forward's region at offset align_bytes).  Returns a status. */
+int moe_lora_workspace_size(const moe_lora_dims *d, size_t *align_bytes, size_t *forward_bytes);
+
+/* A block_m suited to T*k pairs over E experts (16..64 when experts see few tokens,
+ * 128 otherwise). */
+int32_t moe_lora_pick_block_m(int64_t T, int32_t k, int32_t E);
+
+/* ------------------------------------------------------------ the calls -- */
+
+/*
+ * Router top-k ([AWS] "Implementing multi-LoRA inference for MoE models in vLLM").
+ *   logits   [T][E] fp32, device, finite values
+ *   topk_ids [T][k] int32, device, out: experts in descending logit order, ties to the
+ *            lower index
+ *   topk_w   [T][k] fp32, device, out: exp(l_j - l_max) / sum over the chosen k
+ *            (= softmax over all E renormalised over the chosen k)
+ */
+int moe_lora_route(const float *logits, int64_t T, int32_t E, int32_t k,
+                   int32_t *topk_ids, float *topk_w, void *stream);
+
+/*
+ * Align-and-sort of the (expert, adapter) compound sparsity (layout above).
+ *   topk_ids [T][k], lora_ids [T]: int32, device
+ *   out:       the align arrays (bit-identical to the CPU definition)
+ *   workspace: device scratch of at least align_bytes (moe_lora_workspace_size)
+ * totals[3] counts the dropped (invalid) pairs.
+ */
+int moe_lora_align(const moe_lora_dims *d, const int32_t *topk_ids, const int32_t *lora_ids,
+                   const moe_lora_align_buf *out, void *workspace, size_t workspace_bytes,
+                   void *stream);
+
+/*
+ * The fused expert computation over an aligned pair list: gate_up GEMM with its
+ * LoRA shrink and expand, SiLU gating, down GEMM with its LoRA shrink and expand,
+ * and the weighted top-k combine.
+ *   x       [T][H]            bf16, device
+ *   topk_w  [T][k]            fp32, device (the combine weights)
+ *   aligned                   moe_lora_align output for the same dims
+ *   W_gu    [E][2I][H]        bf16; rows [0,I) gate, rows [I,2I) up
+ *   W_dn    [E][H][I]         bf16
+ *   A_gu    [L][E][r_max][H]  bf16; rows >= ranks[a] must be zero
+ *   Bt_gu   [L][E][2I][r_max] bf16 (B of gate_up, transposed); cols >= ranks[a] zero
+ *   A_dn    [L][E][r_max][I]  bf16; rows >= ranks[a] zero
+ *   Bt_dn   [L][E][H][r_max]  bf16; cols >= ranks[a] zero
+ *   out     [T][H]            bf16, device, out: fully overwritten
+ *   workspace  device scratch of at least forward_bytes
+ *   dev_status one int32, device: cleared by the call, then receives MOE_LORA_DEV_* bits
+ *   stage_events  NULL, or MOE_LORA_NUM_STAGES + 1 cudaEvent_t recorded on `stream`
+ *              before the first stage and after each stage (for timing)
+ * LoRA tensors may be NULL when L == 0.
+ */
+int moe_lora_forward(const moe_lora_dims *d, const uint16_t *x, const float *topk_w,
+                     const moe_lora_align_buf *aligned,
+                     const uint16_t *W_gu, const uint16_t *W_dn,
+                     const uint16_t *A_gu, const uint16_t *Bt_gu,
+                     const uint16_t *A_dn, const uint16_t *Bt_dn,
+                     uint16_t *out, void *workspace, size_t workspace_bytes,
+                     int32_t *dev_status, void *stream, void *const *stage_events);
+
+/*
+ * The whole layer from HOST inputs to a HOST output: copies logits [T][E] fp32,
+ * lora_ids [T] int32 and x [T][H] bf16 to the device, runs route, align and
+ * forward on `stream`, copies out [T][H] bf16 back and synchronises the stream.
+ * Weights are device pointers (resident).  Host buffers should be pinned for the
+ * copies to be asynchronous.  workspace: device scratch of at least
+ * moe_lora_layer_workspace_size().  Returns MOE_LORA_EDEVICE if the device
+ * reported a timeout.  *dropped (may be NULL) receives the dropped-pair count.
+ */
+int moe_lora_layer_workspace_size(const moe_lora_dims *d, size_t *bytes);
+int moe_lora_layer_host(const moe_lora_dims *d, const float *logits_host,
+                        const int32_t *lora_ids_host, const uint16_t *x_host,
+                        const uint16_t *W_gu, const uint16_t *W_dn,
+                        const uint16_t *A_gu, const uint16_t *Bt_gu,
+                        const uint16_t *A_dn, const uint16_t *Bt_dn,
+                        uint16_t *out_host, void *workspace, size_t workspace_bytes,
+                        int64_t *dropped, void *stream);
+
+/* ------------------------------------------------------------ diagnostics -- */
+const char *moe_lora_status_string(int status);
+const char *moe_lora_last_error(void);   /* detail of this thread's last failure */
+int moe_lora_version(void);              /* MAJOR*10000 + MINOR*100 + PATCH       */
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_LORA_H */

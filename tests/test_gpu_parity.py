@@ -1,0 +1,176 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle, on a GB300.
+
+Route ids and the align layout are compared bit for bit; route weights within 2e-6;
+the layer output element by element within max |y - ref| / max(|ref|, rms(ref)) <= 2e-2.
+"""
+import numpy as np
+import pytest
+
+from expert_gemm_gb300 import workloads as W
+from gpu_harness import (TOL, align_to_numpy, assert_align_equal, dev_weights, dims_of, inputs, parity_error,
+                         sample_tokens, to_dev)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def torch():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return torch
+
+
+@pytest.fixture(scope="module")
+def ml(torch):
+    from expert_gemm_gb300 import build, moe_lora
+    build.build()
+    moe_lora.load()
+    return moe_lora
+
+
+def run_case(ml, torch, oracle, wl, block_m=None, tokens=None, logits=None, lora=None, check_route=True):
+    logits0, lora0, x, w = inputs(wl)
+    logits = logits0 if logits is None else logits
+    lora = lora0 if lora is None else lora
+    bm = block_m or ml.pick_block_m(wl.T, wl.k, wl.E)
+    d = dims_of(wl, bm, ml)
+    layer = ml.Layer(d, dev_weights(w, torch))
+    out = layer.step(to_dev(logits, torch), to_dev(lora, torch), to_dev(x, torch))
+    torch.cuda.synchronize()
+    assert int(layer.status.item()) == 0
+    ids_o, w_o = oracle.route(logits, wl.k)
+    if check_route:
+        assert np.array_equal(layer.topk_ids.cpu().numpy(), ids_o)
+        assert np.allclose(layer.topk_w.cpu().numpy(), w_o, rtol=0, atol=2e-6)
+    al_o = oracle.align(ids_o, lora, wl.E, wl.L, bm)
+    assert_align_equal(align_to_numpy(layer.bufs), al_o)
+    ref = oracle.forward(x, ids_o, w_o.astype(np.float32), lora, w, tokens)
+    y = out.float().cpu().numpy()
+    if tokens is not None:
+        y = y[tokens]
+    elem, norm = parity_error(y, ref)
+    assert elem <= TOL, (wl.name, bm, elem, norm)
+    return elem, norm, layer
+
+
+# ----------------------------------------------------------------- configs --
+
+@pytest.mark.parametrize("name", ["tiny", "decode", "sweep_T1", "sweep_T16", "sweep_T256"])
+def test_config_full(ml, torch, oracle, name):
+    """Every output element of the smaller configurations."""
+    run_case(ml, torch, oracle, W.get(name))
+
+
+@pytest.mark.parametrize("name", ["prefill", "wide", "sweep_T4096"])
+def test_config_sampled(ml, torch, oracle, name):
+    """Full-size configurations: align checked whole, outputs on sampled tokens."""
+    wl = W.get(name)
+    run_case(ml, torch, oracle, wl, tokens=sample_tokens(wl.T, 40))
+
+
+@pytest.mark.parametrize("block_m", [16, 32, 64, 128])
+def test_every_block_size(ml, torch, oracle, block_m):
+    """Both tile orientations on one layer with several tiles and a ragged tail."""
+    wl = W.custom(name="mid", T=200, H=384, I=448, E=6, k=2, L=3, ranks=(16, 32, 8), lora_mode="uniform_with_none")
+    run_case(ml, torch, oracle, wl, block_m=block_m)
+
+
+# -------------------------------------------------------------- edge cases --
+
+def test_no_adapter_anywhere(ml, torch, oracle):
+    wl = W.get("tiny")
+    run_case(ml, torch, oracle, wl, lora=np.full(wl.T, -1, np.int32))
+
+
+def test_zero_adapters_L0(ml, torch, oracle):
+    wl = W.custom(name="l0", T=48, H=256, I=256, E=4, k=2, L=0, ranks=(), lora_mode="none")
+    run_case(ml, torch, oracle, wl, block_m=16)
+    run_case(ml, torch, oracle, wl, block_m=128)
+
+
+def test_all_tokens_one_expert(ml, torch, oracle):
+    """One expert gets every token (many blocks of one expert, several adapters per block)."""
+    wl = W.custom(name="hot", T=300, H=256, I=320, E=8, k=1, L=4, ranks=(8, 16, 32, 64), lora_mode="uniform_with_none")
+    logits, _, _, _ = inputs(wl)
+    logits = logits.copy()
+    logits[:, 5] += 100.0
+    for bm in (16, 128):
+        run_case(ml, torch, oracle, wl, block_m=bm, logits=logits)
+
+
+def test_single_token(ml, torch, oracle):
+    wl = W.custom(name="one", T=1, H=512, I=256, E=16, k=4, L=2, ranks=(16, 16), lora_mode="uniform")
+    for bm in (16, 128):
+        run_case(ml, torch, oracle, wl, block_m=bm)
+
+
+def test_invalid_ids_dropped(ml, torch, oracle):
+    """Out-of-range expert and adapter ids are dropped and counted, never trapped."""
+    wl = W.custom(name="bad", T=40, H=256, I=256, E=8, k=2, L=3, ranks=(16, 16, 16), lora_mode="uniform_with_none")
+    logits, lora, x, w = inputs(wl)
+    ids, tw = oracle.route(logits, wl.k)
+    ids[3, 0] = -1
+    ids[5, 1] = wl.E
+    lora = lora.copy()
+    lora[7] = wl.L
+    lora[9] = -5
+    d = dims_of(wl, 16, ml)
+    layer = ml.Layer(d, dev_weights(w, torch))
+    ids_d, tw_d = to_dev(ids, torch), to_dev(tw.astype(np.float32), torch)
+    ml.align(d, ids_d, to_dev(lora, torch), layer.bufs, layer.ws_align)
+    ml.forward(d, to_dev(x, torch), tw_d, layer.bufs, layer.w, layer.out, layer.ws_fwd, layer.status)
+    torch.cuda.synchronize()
+    al = align_to_numpy(layer.bufs)
+    assert_align_equal(al, oracle.align(ids, lora, wl.E, wl.L, 16))
+    assert al["num_dropped"] == 2 + 2 * 2
+    ref = oracle.forward(x, ids, tw.astype(np.float32), lora, w)
+    elem, _ = parity_error(layer.out.float().cpu().numpy(), ref)
+    assert elem <= TOL
+
+
+def test_empty_batch(ml, torch):
+    wl = W.get("tiny")
+    _, _, _, w = inputs(wl)
+    d = dims_of(wl, 16, ml, T=0)
+    layer = ml.Layer(d, dev_weights(w, torch))
+    e = torch.empty((0, wl.E), dtype=torch.float32, device="cuda")
+    layer.step(e, torch.empty(0, dtype=torch.int32, device="cuda"),
+               torch.empty((0, wl.H), dtype=torch.bfloat16, device="cuda"))
+    torch.cuda.synchronize()
+    assert layer.bufs["totals"].cpu().tolist() == [0, 0, 0, 0]
+
+
+def test_repeat_calls_reuse_buffers(ml, torch, oracle):
+    """Two different batches through one Layer: no state leaks between calls."""
+    wl = W.get("tiny")
+    e1, _, layer = run_case(ml, torch, oracle, wl)
+    logits, lora, x, w = inputs(wl, seed=0)
+    g = np.random.default_rng(5)
+    logits2 = g.standard_normal(logits.shape).astype(np.float32)
+    lora2 = g.integers(-1, wl.L, size=wl.T).astype(np.int32)
+    out = layer.step(to_dev(logits2, torch), to_dev(lora2, torch), to_dev(x, torch))
+    torch.cuda.synchronize()
+    ids, tw = oracle.route(logits2, wl.k)
+    ref = oracle.forward(x, ids, tw.astype(np.float32), lora2, w)
+    assert parity_error(out.float().cpu().numpy(), ref)[0] <= TOL
+
+
+# ------------------------------------------------------------ host buffers --
+
+@pytest.mark.parametrize("name", ["tiny", "decode"])
+def test_layer_host_entry(ml, torch, oracle, name):
+    """moe_lora_layer_host: host inputs in, host output back, same result."""
+    wl = W.get(name)
+    logits, lora, x, w = inputs(wl)
+    bm = ml.pick_block_m(wl.T, wl.k, wl.E)
+    layer = ml.Layer(dims_of(wl, bm, ml), dev_weights(w, torch))
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()   # noqa: E731
+    lg, lr, xh = pin(logits), pin(lora), pin(x.view(np.int16))
+    out_h = torch.empty((wl.T, wl.H), dtype=torch.int16).pin_memory()
+    dropped = layer.step_host(lg, lr, xh, out_h)
+    assert dropped == 0
+    y = out_h.view(torch.bfloat16).float().numpy()
+    ids, tw = oracle.route(logits, wl.k)
+    ref = oracle.forward(x, ids, tw.astype(np.float32), lora, w)
+    assert parity_error(y, ref)[0] <= TOL
