@@ -550,3 +550,49 @@ int moe_lora_layer_host(const moe_lora_dims* d, const float* logits_host, const 
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// moe_lora_align_static: align with its scratch in a static device array, for
+// callers that cannot allocate device memory when they call.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) unsigned char g_static_scratch[MOE_LORA_STATIC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mu;
+void* g_static_ptr[kMaxDevices] = {};
+
+// Device address of g_static_scratch on the current device, looked up once per
+// device.  (In host code the array's name is only a host-side stand-in.)
+int static_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(MOE_LORA_EUNSUPPORTED, "device ordinal %d >= %d", dev, kMaxDevices);
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (!g_static_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
+    g_static_ptr[dev] = p;
+  }
+  *out = g_static_ptr[dev];
+  return MOE_LORA_OK;
+}
+
+}  // namespace
+
+extern "C" int moe_lora_align_static(const moe_lora_dims* d, const int32_t* topk_ids, const int32_t* lora_ids,
+                                     const moe_lora_align_buf* out, void* stream) {
+  MOE_TRY(validate_dims(d));
+  const size_t need = align_layout(d).bytes;
+  if (need > MOE_LORA_STATIC_SCRATCH_BYTES)
+    return fail(MOE_LORA_EWORKSPACE, "align needs %zu bytes of scratch; the static scratch holds %u", need,
+                MOE_LORA_STATIC_SCRATCH_BYTES);
+  MOE_TRY(check_device());
+  void* scratch = nullptr;
+  MOE_TRY(static_scratch(&scratch));
+  return do_align(d, topk_ids, lora_ids, out, scratch, MOE_LORA_STATIC_SCRATCH_BYTES,
+                  static_cast<cudaStream_t>(stream));
+}

@@ -22,7 +22,8 @@ MAX_ADAPTERS, MAX_RANK, MAX_EXPERTS, MAX_TOPK = 256, 64, 1024, 32
 
 EXPORTS = ["moe_lora_align_capacity", "moe_lora_workspace_size", "moe_lora_pick_block_m", "moe_lora_route",
            "moe_lora_align", "moe_lora_forward", "moe_lora_layer_workspace_size", "moe_lora_layer_host",
-           "moe_lora_status_string", "moe_lora_last_error", "moe_lora_version"]
+           "moe_lora_status_string", "moe_lora_last_error", "moe_lora_version", "moe_lora_align_static"]
+STATIC_SCRATCH_BYTES = 4 << 20
 
 
 class Dims(C.Structure):
@@ -61,6 +62,7 @@ def load(path: str = LIB_PATH):
     lib.moe_lora_pick_block_m.restype = i32
     lib.moe_lora_route.argtypes = [vp, i64, i32, i32, vp, vp, vp]
     lib.moe_lora_align.argtypes = [DP, vp, vp, AP, vp, sz, vp]
+    lib.moe_lora_align_static.argtypes = [DP, vp, vp, AP, vp]
     lib.moe_lora_forward.argtypes = [DP, vp, vp, AP, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp, vp]
     lib.moe_lora_layer_host.argtypes = [DP, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, C.POINTER(i64), vp]
     lib.moe_lora_status_string.restype = C.c_char_p
@@ -68,7 +70,8 @@ def load(path: str = LIB_PATH):
     lib.moe_lora_last_error.restype = C.c_char_p
     lib.moe_lora_version.restype = C.c_int
     for name in ("moe_lora_align_capacity", "moe_lora_workspace_size", "moe_lora_layer_workspace_size",
-                 "moe_lora_route", "moe_lora_align", "moe_lora_forward", "moe_lora_layer_host"):
+                 "moe_lora_route", "moe_lora_align", "moe_lora_forward", "moe_lora_layer_host",
+                 "moe_lora_align_static"):
         getattr(lib, name).restype = C.c_int
     _lib = lib
     return lib
@@ -166,6 +169,16 @@ def alloc_align(d: LayerDims, device="cuda"):
 def align(d: LayerDims, topk_ids, lora_ids, bufs: dict, workspace, stream=None):
     _check(load().moe_lora_align(C.byref(d.c()), _ptr(topk_ids), _ptr(lora_ids), C.byref(_abuf(bufs)),
                                  _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def align_static(d: LayerDims, topk_ids, lora_ids, bufs: dict, stream=None):
+    """moe_lora_align with the library's static device scratch instead of a workspace.
+
+    For callers that cannot allocate device memory when they call.  Calls on one
+    device share that scratch: do not let them overlap on the GPU.
+    """
+    _check(load().moe_lora_align_static(C.byref(d.c()), _ptr(topk_ids), _ptr(lora_ids), C.byref(_abuf(bufs)),
+                                        _stream(stream)))
 
 
 NUM_STAGES = 6

@@ -198,6 +198,30 @@ int moe_lora_layer_host(const moe_lora_dims *d, const float *logits_host,
                         uint16_t *out_host, void *workspace, size_t workspace_bytes,
                         int64_t *dropped, void *stream);
 
+/*
+ * moe_lora_align_static: moe_lora_align without a caller-supplied workspace.
+ * The pages have no counterpart of this entry point.  It is for callers that cannot
+ * allocate device memory when they call: a serving engine that has handed almost all
+ * HBM to its own pool (weights, KV cache), so cudaMalloc has nothing left to give or
+ * would fragment that pool, and latency-bound decode loops in which a cudaMalloc --
+ * which may synchronise the device and takes unbounded time -- is not allowed.
+ * Its scratch is one static device array of MOE_LORA_STATIC_SCRATCH_BYTES, which
+ * every GPU that loads the library holds until the process exits.  Dims whose align
+ * scratch (align_bytes of moe_lora_workspace_size) is larger are rejected with
+ * MOE_LORA_EWORKSPACE before anything is enqueued.
+ *   - The first call on a device looks up the array's device address (once per
+ *     device, with that device current); make that first call before any stream
+ *     capture.
+ *   - All calls on a device share the one array: calls that overlap on the GPU
+ *     (other streams, other host threads) race on it, so serialise them.
+ *   - The array keeps the last call's contents; the align kernels write every
+ *     scratch word before reading it, so nothing needs clearing between calls.
+ * Arguments and results are those of moe_lora_align.
+ */
+#define MOE_LORA_STATIC_SCRATCH_BYTES (4u << 20)
+int moe_lora_align_static(const moe_lora_dims *d, const int32_t *topk_ids, const int32_t *lora_ids,
+                          const moe_lora_align_buf *out, void *stream);
+
 /* ------------------------------------------------------------ diagnostics -- */
 const char *moe_lora_status_string(int status);
 const char *moe_lora_last_error(void);   /* detail of this thread's last failure */
