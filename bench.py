@@ -116,6 +116,15 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+def workload_of(args) -> W.Workload:
+    wl = W.get(args.workload)
+    if getattr(args, "tokens", 0):
+        import dataclasses
+        wl = dataclasses.replace(wl, name=f"{wl.name}_T{args.tokens}", T=args.tokens,
+                                 requests=min(wl.requests, args.tokens) if wl.requests else 0)
+    return wl
+
+
 # -------------------------------------------------------------- our arm -----
 
 def run_ours(args, rank, world, local_rank):
@@ -124,7 +133,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     build.build()
     ml.load()
-    wl = W.get(args.workload)
+    wl = workload_of(args)
     seed_w, seed_b = 0, rank                      # same weights on every replica, own batch per rank
     logits, lora = W.make_routing(wl, seed_b)
     x = W.make_activations(wl, seed_b)
@@ -139,8 +148,9 @@ def run_ours(args, rank, world, local_rank):
     lg, lr, xd = dev(logits), dev(lora), dev(x)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     K, Wm = args.steps, args.warmup
+    KI = max(1, min(K, 100))                      # instrumented steps (per-stage events)
     nst = ml.NUM_STAGES + 1
-    stage_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nst)] for _ in range(K)]
+    stage_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nst)] for _ in range(KI)]
     step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     for evs in stage_ev:                          # create the CUDA events before handing them to the library
         for e in evs:
@@ -153,8 +163,9 @@ def run_ours(args, rank, world, local_rank):
         raise RuntimeError(f"device status {int(layer.status.item())}")
     ids = layer.topk_ids.cpu().numpy()
     tot = layer.bufs["totals"].cpu().numpy()
-    nchunks_launched = 3 if wl.T * wl.k > 0 else 1
-    launches_per_step = 1 + nchunks_launched + 4 + (2 if wl.L > 0 else 0)
+    P = wl.T * wl.k
+    align_launches = 1 if P <= 4096 else 3
+    launches_per_step = 1 + align_launches + 4 + (2 if wl.L > 0 else 0)
     acct = algorithmic(wl, ids, lora)
 
     clocks = ClockSampler(local_rank)
@@ -163,10 +174,15 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     clocks.start()
     t_wall0 = time.perf_counter()
+    # headline: K plain steps (events only at step boundaries)
     for i in range(K):
         step_ev[i][0].record()
-        layer.step(lg, lr, xd, stage_events=stage_ev[i])
+        layer.step(lg, lr, xd)
         step_ev[i][1].record()
+        flush.zero_()
+    # per-kernel durations: steps with an event between every two launches
+    for i in range(KI):
+        layer.step(lg, lr, xd, stage_events=stage_ev[i])
         flush.zero_()
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall0
@@ -222,11 +238,13 @@ def run_ours(args, rank, world, local_rank):
         "layer_roofline": {"alg_bytes": acct["bytes"], "alg_flops": acct["flops"], "t_roof_ms": roof_s * 1e3,
                            "frac": roof_s / layer_s, "hbm_gbs_peak": hbm, "bf16_tflops_peak": tc},
         "stage_ms": {n: float(np.mean(stage_ms[:, j])) for j, n in enumerate(ml.STAGES)},
+        "instrumented_ms_per_step": float(np.mean(np.sum(stage_ms, axis=1))),
+        "instrumented_steps": KI,
         "touched": {k_: acct[k_] for k_ in ("experts", "adapter_expert_pairs", "valid_pairs")},
         "e2e": {"value": world * wl.T / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": wl.T * (wl.E * 4 + 4 + wl.H * 2),
                 "d2h_bytes_per_step": wl.T * wl.H * 2 + 4 + 16, "ms_per_step": e2e_s * 1e3,
                 "entry": "moe_lora_layer_host (pinned host buffers)"},
-        "gpu_launches": launches_per_step * K,
+        "gpu_launches": launches_per_step * (K + KI),
         "clocks": clk,
         "wall_s_timed": t_wall,
         "align_totals": [int(v) for v in tot],
@@ -269,7 +287,7 @@ def cores_used():
 def run_reference(args):
     """The fp64 oracle as the reference arm: each step is a bounded token sample of the workload."""
     from oracle import Oracle
-    wl = W.get(args.workload)
+    wl = workload_of(args)
     o = Oracle()
     logits, lora = W.make_routing(wl, 0)
     x = W.make_activations(wl, 0)
@@ -310,6 +328,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode", choices=sorted(W.WORKLOADS))
     ap.add_argument("--block-m", type=int, default=0)
+    ap.add_argument("--tokens", type=int, default=0, help="override T of the workload (small profiling cases)")
     ap.add_argument("--cpu-baseline-s", type=float, default=12.0, help="seconds of oracle time (0 = skip)")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -331,7 +350,7 @@ def main():
     res = run_ours(args, rank, world, local_rank)
     if rank == 0:
         if world == 1 and args.cpu_baseline_s > 0:
-            wl = W.get(args.workload)
+            wl = workload_of(args)
             v, n, reps, el = oracle_sample_rate(wl, min(wl.T, 16), args.cpu_baseline_s)
             res["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": cores_used(), "kind": "oracle",
                                    "sample": f"first {n} of {wl.T} tokens, {reps} passes in {el:.1f} s "

@@ -33,11 +33,11 @@ __device__ __forceinline__ int lower_bound_u32(const uint32_t* a, int lo, int hi
   return lo;
 }
 
-__global__ void __launch_bounds__(1024) align_chunk_kernel(AlignLaunch a) {
-  extern __shared__ uint32_t keys[];
+// Phase 1 for one chunk: keys of its pairs sorted in keys[] (shared), per-bucket
+// counts of the chunk and its invalid-pair count written to global scratch.
+__device__ void chunk_phase(const AlignLaunch& a, uint32_t* keys, int chunk, bool store_keys) {
   __shared__ int32_t s_invalid;
   const int CH = 1 << a.ch_log2;
-  const int chunk = blockIdx.x;
   const int64_t p0 = static_cast<int64_t>(chunk) << a.ch_log2;
   const int LB = a.L + 1;
   const int NB = a.E * LB;
@@ -78,7 +78,7 @@ __global__ void __launch_bounds__(1024) align_chunk_kernel(AlignLaunch a) {
   __syncthreads();
   for (int i = threadIdx.x; i < CH; i += blockDim.x) {
     const uint32_t key = keys[i];
-    a.chunk_keys[p0 + i] = key;
+    if (store_keys) a.chunk_keys[p0 + i] = key;
     if (key == kInvalidKey) continue;
     const uint32_t bkt = key >> a.ch_log2;
     const bool last = (i == CH - 1) || (keys[i + 1] >> a.ch_log2) != bkt;
@@ -88,6 +88,11 @@ __global__ void __launch_bounds__(1024) align_chunk_kernel(AlignLaunch a) {
     }
   }
   if (threadIdx.x == 0) a.chunk_invalid[chunk] = s_invalid;
+}
+
+__global__ void __launch_bounds__(1024) align_chunk_kernel(AlignLaunch a) {
+  extern __shared__ uint32_t keys[];
+  chunk_phase(a, keys, blockIdx.x, true);
 }
 
 // Block-wide exclusive scan over n values produced by getv(i); put(i, prefix) receives
@@ -125,7 +130,9 @@ __device__ int block_exclusive_scan(int n, GetV getv, Put put, int32_t* s_warp) 
   return carry;
 }
 
-__global__ void __launch_bounds__(1024) align_scan_kernel(AlignLaunch a) {
+// Phase 2 (one CTA): bucket offsets, padded expert starts, runs, block experts,
+// padding sentinels, totals and block -> first-run index.
+__device__ void scan_phase(const AlignLaunch& a) {
   __shared__ int32_t s_warp[32];
   __shared__ int32_t s_rows, s_runs;
   const int LB = a.L + 1;
@@ -224,14 +231,13 @@ __global__ void __launch_bounds__(1024) align_scan_kernel(AlignLaunch a) {
   }
 }
 
-__global__ void __launch_bounds__(1024) align_scatter_kernel(AlignLaunch a) {
-  extern __shared__ uint32_t keys[];
+__global__ void __launch_bounds__(1024) align_scan_kernel(AlignLaunch a) { scan_phase(a); }
+
+// Phase 3 for one chunk whose sorted keys are in keys[] (shared): place each pair.
+__device__ void scatter_phase(const AlignLaunch& a, const uint32_t* keys, int chunk) {
   const int CH = 1 << a.ch_log2;
-  const int chunk = blockIdx.x;
   const int64_t p0 = static_cast<int64_t>(chunk) << a.ch_log2;
   const int NB = a.E * (a.L + 1);
-  for (int i = threadIdx.x; i < CH; i += blockDim.x) keys[i] = a.chunk_keys[p0 + i];
-  __syncthreads();
   for (int i = threadIdx.x; i < CH; i += blockDim.x) {
     const uint32_t key = keys[i];
     if (key == kInvalidKey) continue;
@@ -243,12 +249,36 @@ __global__ void __launch_bounds__(1024) align_scatter_kernel(AlignLaunch a) {
   }
 }
 
+__global__ void __launch_bounds__(1024) align_scatter_kernel(AlignLaunch a) {
+  extern __shared__ uint32_t keys[];
+  const int CH = 1 << a.ch_log2;
+  const int64_t p0 = static_cast<int64_t>(blockIdx.x) << a.ch_log2;
+  for (int i = threadIdx.x; i < CH; i += blockDim.x) keys[i] = a.chunk_keys[p0 + i];
+  __syncthreads();
+  scatter_phase(a, keys, blockIdx.x);
+}
+
+// All three phases in one CTA, for batches that fit one chunk: the sorted keys stay
+// in shared memory and two launches disappear from the decode path.
+__global__ void __launch_bounds__(1024) align_small_kernel(AlignLaunch a) {
+  extern __shared__ uint32_t keys[];
+  chunk_phase(a, keys, 0, false);
+  __syncthreads();
+  scan_phase(a);
+  __syncthreads();
+  scatter_phase(a, keys, 0);
+}
+
 }  // namespace
 
 cudaError_t launch_align(const AlignLaunch& a, cudaStream_t s) {
   const int CH = 1 << a.ch_log2;
   const int threads = CH < 1024 ? CH : 1024;
   const size_t smem = static_cast<size_t>(CH) * sizeof(uint32_t);
+  if (a.nchunks == 1) {
+    align_small_kernel<<<1, 1024, smem, s>>>(a);
+    return cudaGetLastError();
+  }
   if (a.nchunks > 0) {
     align_chunk_kernel<<<a.nchunks, threads, smem, s>>>(a);
     cudaError_t err = cudaGetLastError();

@@ -37,6 +37,8 @@ struct GemmParams {
   int32_t k;
   int32_t P;                    // T*k, the padding sentinel
   int32_t r_pad;                // S row length (r_max rounded up to 16)
+  int32_t ksplit;               // kDown: K splits (grid.z); partial sums meet in out_acc
+  int32_t lora_after_pdl;       // previous kernel is the shrink: wait for it only before the LoRA K-steps
   int32_t ranks[MOE_LORA_MAX_ADAPTERS];
 };
 
@@ -70,10 +72,13 @@ struct AlignLaunch {
 };
 cudaError_t launch_align(const AlignLaunch& a, cudaStream_t s);
 
+// Gathers x rows into sorted order and zeroes out_acc [n_acc floats] and *status.
 cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* sorted_p, const int32_t* totals, int64_t max_rows,
-                               int H, int k, int P, uint16_t* x_sorted, cudaStream_t s);
-cudaError_t launch_finalize(const float* acc, uint16_t* out, int64_t n, cudaStream_t s);
+                               int H, int k, int P, uint16_t* x_sorted, float* out_acc, int64_t n_acc,
+                               int32_t* status, cudaStream_t s);
+cudaError_t launch_finalize(const float* acc, uint16_t* out, int64_t n, bool pdl, cudaStream_t s);
+// pdl: launch with programmatic stream serialisation (may overlap the previous kernel).
 cudaError_t launch_gemm(int mode, int bt, const GemmMaps& maps, const GemmParams& prm, int64_t max_blocks,
-                        int64_t max_runs, cudaStream_t s);
+                        int64_t max_runs, bool pdl, cudaStream_t s);
 
 }  // namespace moe

@@ -4,13 +4,13 @@
 namespace moe {
 
 cudaError_t launch_gemm(int mode, int bt, const GemmMaps& maps, const GemmParams& prm, int64_t max_blocks,
-                        int64_t max_runs, cudaStream_t s) {
+                        int64_t max_runs, bool pdl, cudaStream_t s) {
 #define MOE_GEMM_CASE(BT_, SWAP_)                                                                       \
   if (bt == BT_) {                                                                                      \
     switch (mode) {                                                                                     \
-      case kShrink: return launch_gemm_t<kShrink, SWAP_, BT_>(maps, prm, max_blocks, max_runs, s);     \
-      case kGateUp: return launch_gemm_t<kGateUp, SWAP_, BT_>(maps, prm, max_blocks, max_runs, s);     \
-      case kDown: return launch_gemm_t<kDown, SWAP_, BT_>(maps, prm, max_blocks, max_runs, s);         \
+      case kShrink: return launch_gemm_t<kShrink, SWAP_, BT_>(maps, prm, max_blocks, max_runs, pdl, s);     \
+      case kGateUp: return launch_gemm_t<kGateUp, SWAP_, BT_>(maps, prm, max_blocks, max_runs, pdl, s);     \
+      case kDown: return launch_gemm_t<kDown, SWAP_, BT_>(maps, prm, max_blocks, max_runs, pdl, s);         \
       default: return cudaErrorInvalidValue;                                                            \
     }                                                                                                   \
   }

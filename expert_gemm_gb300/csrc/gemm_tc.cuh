@@ -81,22 +81,35 @@ __global__ void __launch_bounds__(192, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // ---- work unit (uniform across the CTA; CTAs past the device-side count leave now)
+  // ---- work unit (uniform across the CTA; CTAs past the device-side count leave now).
+  // The routing metadata comes from align, which finished before the previous kernel
+  // started, so it may be read before waiting on that kernel.
   int b, f0 = 0, run0 = 0, nruns = 0, shrink_run = -1;
+  int kb0 = 0, nk = prm.K / kKTile;
   if constexpr (MODE == kShrink) {
     shrink_run = blockIdx.x;
     if (shrink_run >= prm.totals[2]) return;
     b = prm.runs[4 * shrink_run + 0];
+    // S tiles feed the next kernel's LoRA K-steps; it may launch once every shrink
+    // CTA has passed this point, which is after the inputs of this kernel are ready.
+    pdl_wait();
+    pdl_trigger();
   } else {
     b = blockIdx.y;
     if (b >= prm.totals[1]) return;
     f0 = blockIdx.x * (MODE == kGateUp ? 128 : 256);
-    run0 = prm.block_runs[b];
-    nruns = prm.block_runs[b + 1] - run0;
+    if (blockIdx.z == 0) {
+      run0 = prm.block_runs[b];
+      nruns = prm.block_runs[b + 1] - run0;
+    }
+    const int nk_all = nk;
+    kb0 = static_cast<int>(blockIdx.z) * nk_all / prm.ksplit;
+    nk = (static_cast<int>(blockIdx.z) + 1) * nk_all / prm.ksplit - kb0;
+    if (!prm.lora_after_pdl) pdl_wait();   // the previous kernel produced the token rows
+    pdl_trigger();
   }
   const int e = prm.block_expert[b];
   const int row0 = b * BT;
-  const int nk = prm.K / kKTile;
   const int n_it = nk + nruns;
   int shrink_a = 0, shrink_nch = 0;
   if constexpr (MODE == kShrink) {
@@ -148,7 +161,7 @@ __global__ void __launch_bounds__(192, 1)
         uint8_t* tdst = wdst + C::W_BYTES;
         uint64_t* fb = &bars->full[s];
         if (it < nk) {
-          const int k0 = it * kKTile;
+          const int k0 = (kb0 + it) * kKTile;
           if constexpr (MODE == kGateUp) {
             mbar_arrive_expect_tx(fb, C::W_BYTES + C::T_BYTES);
             tma_load_4d(wdst, &maps.w, fb, k0, f0, 0, e);               // gate rows f0..f0+127
@@ -165,6 +178,7 @@ __global__ void __launch_bounds__(192, 1)
           }
           tma_load_2d(tdst, &maps.tok, fb, k0, row0);
         } else if constexpr (C::kLora) {
+          if (it == nk && prm.lora_after_pdl) pdl_wait();   // S tiles come from the previous kernel
           const int run = run0 + (it - nk);
           const int a = prm.runs[4 * run + 1];
           const int nch = (prm.ranks[a] + kRankChunk - 1) / kRankChunk;
@@ -384,7 +398,7 @@ __global__ void __launch_bounds__(192, 1)
 
 template <int MODE, bool SWAP, int BT>
 cudaError_t launch_gemm_t(const GemmMaps& maps, const GemmParams& prm, int64_t max_blocks, int64_t max_runs,
-                          cudaStream_t s) {
+                          bool pdl, cudaStream_t s) {
   using C = GemmCfg<MODE, SWAP, BT>;
   auto kern = moe_gemm_kernel<MODE, SWAP, BT>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
@@ -396,10 +410,20 @@ cudaError_t launch_gemm_t(const GemmMaps& maps, const GemmParams& prm, int64_t m
   } else {
     if (max_blocks <= 0) return cudaSuccess;
     const int tile = MODE == kGateUp ? 128 : 256;
-    grid = dim3(static_cast<unsigned>((prm.n_feat + tile - 1) / tile), static_cast<unsigned>(max_blocks), 1);
+    grid = dim3(static_cast<unsigned>((prm.n_feat + tile - 1) / tile), static_cast<unsigned>(max_blocks),
+                static_cast<unsigned>(prm.ksplit));
   }
-  kern<<<grid, 192, C::SMEM_BYTES, s>>>(maps, prm);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(192, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, maps, prm);
 }
 
 }  // namespace moe

@@ -195,6 +195,34 @@ int check_align_buf(const moe_lora_align_buf* b) {
   return MOE_LORA_OK;
 }
 
+int sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess && cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+      n = v;
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
+
+// K splits of the weight-streaming down GEMM: only when the tiles cannot fill one wave
+// (each extra CTA pays its own prologue, which costs more than a partial last wave);
+// each split keeps at least 8 K-tiles.  The token-tiled (compute-bound) shape keeps one.
+int down_ksplit(const moe_lora_dims* d, const Caps& cap) {
+  if (d->block_m >= 128) return 1;
+  const int64_t P = d->T * d->k;
+  int64_t est_blocks = cap.blocks;
+  if (est_blocks > d->E) est_blocks = d->E;
+  if (est_blocks > P) est_blocks = P;
+  const int64_t tiles = (int64_t)((d->H + 255) / 256) * (est_blocks > 0 ? est_blocks : 1);
+  int64_t ks = ((int64_t)sm_count() + tiles - 1) / tiles;
+  const int64_t nk = d->I / 64;
+  const int64_t ks_max = nk / 8 < 4 ? (nk / 8 > 1 ? nk / 8 : 1) : 4;
+  if (ks > ks_max) ks = ks_max;
+  return ks < 1 ? 1 : (int)ks;
+}
+
 int do_route(const float* logits, int64_t T, int32_t E, int32_t k, int32_t* ids, float* w, cudaStream_t s) {
   if (T < 0 || E < 1 || E > MOE_LORA_MAX_EXPERTS || k < 1 || k > E || k > MOE_LORA_MAX_TOPK)
     return fail(MOE_LORA_EINVAL, "route: T=%lld E=%d k=%d out of range", (long long)T, E, k);
@@ -356,22 +384,28 @@ int do_forward(const moe_lora_dims* d, const uint16_t* x, const float* topk_w, c
   p.k = d->k;
   p.P = (int32_t)(d->T * d->k);
   p.r_pad = (int32_t)RP;
+  p.ksplit = 1;
+  p.lora_after_pdl = 0;
   for (int a = 0; a < d->L; ++a) p.ranks[a] = d->ranks[a];
 
   auto mark = [&](int i) -> cudaError_t {
     return ev ? cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), s) : cudaSuccess;
   };
+  // Each kernel after the gather is launched as a programmatic dependent of the one
+  // before it: it may start (prologue, weight streaming) while its predecessor
+  // finishes, and waits on the device exactly where it reads that predecessor's
+  // output.  Stage events, when given, sit between launches.
+  const bool lora = d->L > 0;
   MOE_CUDA(mark(0));
-  MOE_CUDA(cudaMemsetAsync(dev_status, 0, sizeof(int32_t), s));
-  MOE_CUDA(cudaMemsetAsync(acc, 0, (size_t)d->T * d->H * 4, s));
-  MOE_CUDA(moe::launch_gather_rows(x, al->sorted_p, al->totals, cap.rows, d->H, d->k, p.P, xs, s));
+  MOE_CUDA(moe::launch_gather_rows(x, al->sorted_p, al->totals, cap.rows, d->H, d->k, p.P, xs, acc,
+                                   d->T * (int64_t)d->H, dev_status, s));
   MOE_CUDA(mark(1 + MOE_LORA_STAGE_GATHER));
 
-  if (d->L > 0) {
+  if (lora) {
     moe::GemmParams q = p;
     q.K = d->H;
     q.s_out = sgu;
-    MOE_CUDA(moe::launch_gemm(moe::kShrink, BT, m_sgu, q, cap.blocks, cap.runs, s));
+    MOE_CUDA(moe::launch_gemm(moe::kShrink, BT, m_sgu, q, cap.blocks, cap.runs, true, s));
   }
   MOE_CUDA(mark(1 + MOE_LORA_STAGE_SHRINK_GU));
   {
@@ -379,14 +413,15 @@ int do_forward(const moe_lora_dims* d, const uint16_t* x, const float* topk_w, c
     q.K = d->H;
     q.n_feat = d->I;
     q.h_out = hs;
-    MOE_CUDA(moe::launch_gemm(moe::kGateUp, BT, m_gu, q, cap.blocks, cap.runs, s));
+    q.lora_after_pdl = lora;
+    MOE_CUDA(moe::launch_gemm(moe::kGateUp, BT, m_gu, q, cap.blocks, cap.runs, true, s));
   }
   MOE_CUDA(mark(1 + MOE_LORA_STAGE_GATE_UP));
-  if (d->L > 0) {
+  if (lora) {
     moe::GemmParams q = p;
     q.K = d->I;
     q.s_out = sdn;
-    MOE_CUDA(moe::launch_gemm(moe::kShrink, BT, m_sdn, q, cap.blocks, cap.runs, s));
+    MOE_CUDA(moe::launch_gemm(moe::kShrink, BT, m_sdn, q, cap.blocks, cap.runs, true, s));
   }
   MOE_CUDA(mark(1 + MOE_LORA_STAGE_SHRINK_DN));
   {
@@ -394,10 +429,12 @@ int do_forward(const moe_lora_dims* d, const uint16_t* x, const float* topk_w, c
     q.K = d->I;
     q.n_feat = d->H;
     q.out_acc = acc;
-    MOE_CUDA(moe::launch_gemm(moe::kDown, BT, m_dn, q, cap.blocks, cap.runs, s));
+    q.lora_after_pdl = lora;
+    q.ksplit = down_ksplit(d, cap);
+    MOE_CUDA(moe::launch_gemm(moe::kDown, BT, m_dn, q, cap.blocks, cap.runs, true, s));
   }
   MOE_CUDA(mark(1 + MOE_LORA_STAGE_DOWN));
-  MOE_CUDA(moe::launch_finalize(acc, out, d->T * d->H, s));
+  MOE_CUDA(moe::launch_finalize(acc, out, d->T * d->H, true, s));
   MOE_CUDA(mark(1 + MOE_LORA_STAGE_FINALIZE));
   return MOE_LORA_OK;
 }

@@ -102,6 +102,15 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* m, uin
       : "memory");
 }
 
+// ------------------------------------------- programmatic dependent launch
+// A kernel launched with programmatic stream serialisation may start before the
+// previous kernel in the stream has finished.  pdl_wait() blocks the calling thread
+// until that previous grid has completed and its memory is visible; pdl_trigger()
+// lets the next kernel in the stream start launching.  Both are no-ops for kernels
+// launched without the attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ------------------------------------------------------------------ tcgen05
 
 // TMEM allocation: executed by one full warp; writes the TMEM base address to *dst.

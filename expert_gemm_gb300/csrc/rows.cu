@@ -2,15 +2,23 @@
 #include <cuda_bf16.h>
 
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace moe {
 namespace {
 
-// x_sorted[row] = x[sorted_p[row] / k] for real rows, zero for padding rows.
-// One warp per row, 16-byte vectors.
+// x_sorted[row] = x[sorted_p[row] / k] for real rows, zero for padding rows; one warp
+// per row, 16-byte vectors.  The same launch zeroes the fp32 combine accumulator and
+// the call's device status word, so the forward needs no memset nodes.
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ sorted_p,
                                                           const int32_t* __restrict__ totals, int64_t max_rows, int vec_per_row,
-                                                          int k, int P, uint4* __restrict__ xs) {
+                                                          int k, int P, uint4* __restrict__ xs, float4* __restrict__ acc,
+                                                          int64_t n_acc4, int32_t* __restrict__ status) {
+  pdl_trigger();   // the next kernel waits for this grid before reading what it writes
+  const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t nthr = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = tid; i < n_acc4; i += nthr) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (tid == 0) *status = 0;
   const int lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (row >= max_rows || row >= totals[0]) return;
@@ -25,6 +33,7 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
 }
 
 __global__ void __launch_bounds__(256) finalize_kernel(const float4* __restrict__ acc, uint2* __restrict__ out, int64_t n4) {
+  pdl_wait();   // out_acc is complete once the down GEMM has finished
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const float4 v = acc[i];
@@ -37,23 +46,33 @@ __global__ void __launch_bounds__(256) finalize_kernel(const float4* __restrict_
 }  // namespace
 
 cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* sorted_p, const int32_t* totals, int64_t max_rows,
-                               int H, int k, int P, uint16_t* x_sorted, cudaStream_t s) {
-  if (max_rows <= 0) return cudaSuccess;
+                               int H, int k, int P, uint16_t* x_sorted, float* out_acc, int64_t n_acc,
+                               int32_t* status, cudaStream_t s) {
   const int rows_per_cta = 8;
-  const int64_t grid = (max_rows + rows_per_cta - 1) / rows_per_cta;
+  int64_t grid = (max_rows + rows_per_cta - 1) / rows_per_cta;
+  if (grid < 1) grid = 1;
   gather_rows_kernel<<<static_cast<unsigned>(grid), rows_per_cta * 32, 0, s>>>(
-      reinterpret_cast<const uint4*>(x), sorted_p, totals, max_rows, H / 8, k, P, reinterpret_cast<uint4*>(x_sorted));
+      reinterpret_cast<const uint4*>(x), sorted_p, totals, max_rows, H / 8, k, P, reinterpret_cast<uint4*>(x_sorted),
+      reinterpret_cast<float4*>(out_acc), n_acc / 4, status);
   return cudaGetLastError();
 }
 
-cudaError_t launch_finalize(const float* acc, uint16_t* out, int64_t n, cudaStream_t s) {
+cudaError_t launch_finalize(const float* acc, uint16_t* out, int64_t n, bool pdl, cudaStream_t s) {
   if (n <= 0) return cudaSuccess;
   const int64_t n4 = n / 4;
   int64_t grid = (n4 + 255) / 256;
   if (grid > 152 * 8) grid = 152 * 8;
-  finalize_kernel<<<static_cast<unsigned>(grid), 256, 0, s>>>(reinterpret_cast<const float4*>(acc),
-                                                             reinterpret_cast<uint2*>(out), n4);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, finalize_kernel, reinterpret_cast<const float4*>(acc),
+                            reinterpret_cast<uint2*>(out), n4);
 }
 
 }  // namespace moe

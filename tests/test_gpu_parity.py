@@ -76,6 +76,14 @@ def test_every_block_size(ml, torch, oracle, block_m):
     run_case(ml, torch, oracle, wl, block_m=block_m)
 
 
+@pytest.mark.parametrize("block_m", [16, 32])
+def test_down_split_k(ml, torch, oracle, block_m):
+    """Few tokens over a long I: the weight-streaming down GEMM runs with K split 4 ways,
+    partial sums meeting in the fp32 accumulator."""
+    wl = W.custom(name="splitk", T=8, H=256, I=2048, E=4, k=2, L=2, ranks=(16, 32), lora_mode="uniform_with_none")
+    run_case(ml, torch, oracle, wl, block_m=block_m)
+
+
 # -------------------------------------------------------------- edge cases --
 
 def test_no_adapter_anywhere(ml, torch, oracle):
