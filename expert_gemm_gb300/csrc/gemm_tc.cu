@@ -18,6 +18,7 @@ cudaError_t launch_gemm(int mode, int bt, const GemmMaps& maps, const GemmParams
   MOE_GEMM_CASE(32, true)
   MOE_GEMM_CASE(64, true)
   MOE_GEMM_CASE(128, false)
+  MOE_GEMM_CASE(256, false)
 #undef MOE_GEMM_CASE
   return cudaErrorInvalidValue;
 }

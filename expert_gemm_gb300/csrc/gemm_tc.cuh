@@ -15,8 +15,11 @@
 // taken one step further: base GEMM, expand and epilogue share one accumulator.
 //
 // Two tile orientations (template SWAP):
-//   SWAP = false (token blocks of 128 rows): MMA M = 128 tokens, N = 256 weight rows
-//          (gate_up: 128 gate + 128 up rows of the same features; down: 256 features).
+//   SWAP = false (token blocks of 128 or 256 rows): MMA M = 128 tokens per accumulator
+//          (one or two accumulators, MT = BT/128), N = 256 weight rows (gate_up: 128 gate
+//          + 128 up rows of the same features; down: 256 features).  A 256-token block
+//          uses each staged weight tile twice, which halves the L2 traffic per flop of
+//          the weight side.
 //   SWAP = true  (token blocks of 16/32/64 rows, few tokens per expert): MMA M = 128
 //          weight rows, N = BT tokens; two accumulators (gate/up, or two feature halves).
 //          Weights stream through the tensor core at full tile height however few
@@ -41,14 +44,18 @@ struct GemmCfg {
   static constexpr int W_BYTES = WROWS * 128;
   static constexpr int T_BYTES = BT * 128;
   static constexpr int STAGE_BYTES = W_BYTES + T_BYTES;
-  static constexpr int STAGES = MODE == kShrink ? 4 : (SWAP ? (BT <= 16 ? 6 : 5) : 4);
-  // accumulators: non-swapped one M=128 x N tile; swapped NH tiles of 128 x BT
+  static constexpr int STAGES = MODE == kShrink ? 4 : (SWAP ? (BT <= 16 ? 6 : 5) : (BT == 256 ? 3 : 4));
+  // accumulators: non-swapped MT tiles of M=128 tokens x N; swapped NH tiles of 128 x BT
   static constexpr int NH = MODE == kShrink ? 1 : 2;
-  static constexpr int ACC_COLS = SWAP ? NH * BT : (MODE == kShrink ? 64 : 256);
-  static constexpr int TMEM_COLS = ACC_COLS <= 32 ? 32 : ACC_COLS <= 64 ? 64 : ACC_COLS <= 128 ? 128 : 256;
+  static constexpr int MT = SWAP ? 1 : BT / 128;
+  static constexpr int NACC = MODE == kShrink ? 64 : 256;   // columns of one non-swapped accumulator
+  static constexpr int ACC_COLS = SWAP ? NH * BT : MT * NACC;
+  static constexpr int TMEM_COLS =
+      ACC_COLS <= 32 ? 32 : ACC_COLS <= 64 ? 64 : ACC_COLS <= 128 ? 128 : ACC_COLS <= 256 ? 256 : 512;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align slack*/ + 256 /*barriers*/;
   static_assert(!SWAP || (BT == 16 || BT == 32 || BT == 64), "swapped tiles take 16/32/64 tokens");
-  static_assert(SWAP || BT == 128, "token-tiled blocks are 128 rows");
+  static_assert(SWAP || BT == 128 || BT == 256, "token-tiled blocks are 128 or 256 rows");
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
   static_assert(W_BYTES % 1024 == 0 && T_BYTES % 1024 == 0, "stage regions keep 1024-byte alignment");
 };
 
@@ -224,9 +231,12 @@ __global__ void __launch_bounds__(192, 1)
           for (int kk = 0; kk < kKTile / 16; ++kk) {
             if constexpr (!SWAP) {
               const uint32_t n_mma = MODE == kShrink ? shrink_nch * kRankChunk : 256;
-              const uint64_t ad = smem_desc(tbase + kk * 32, 1024, kSw128);
               const uint64_t bd = smem_desc(wbase + kk * 32, 1024, kSw128);
-              tc_mma(tmem, ad, bd, idesc_bf16_f32(128, n_mma), acc);
+#pragma unroll
+              for (int mt = 0; mt < C::MT; ++mt) {
+                const uint64_t ad = smem_desc(tbase + mt * 128 * 128 + kk * 32, 1024, kSw128);
+                tc_mma(tmem + mt * C::NACC, ad, bd, idesc_bf16_f32(128, n_mma), acc);
+              }
             } else {
               const uint64_t bd = smem_desc(tbase + kk * 32, 1024, kSw128);
 #pragma unroll
@@ -244,7 +254,10 @@ __global__ void __launch_bounds__(192, 1)
             const uint32_t wc = wbase + c * (C::WROWS * 32);
             const uint32_t tc = tbase + c * (BT * 32);
             if constexpr (!SWAP) {
-              tc_mma(tmem, smem_desc(tc, 256, kSw32), smem_desc(wc, 256, kSw32), idesc_bf16_f32(128, 256), 1);
+              const uint64_t bd = smem_desc(wc, 256, kSw32);
+#pragma unroll
+              for (int mt = 0; mt < C::MT; ++mt)
+                tc_mma(tmem + mt * C::NACC, smem_desc(tc + mt * 128 * 32, 256, kSw32), bd, idesc_bf16_f32(128, 256), 1);
             } else {
               const uint64_t bd = smem_desc(tc, 256, kSw32);
 #pragma unroll
@@ -274,11 +287,13 @@ __global__ void __launch_bounds__(192, 1)
         const int r_a = prm.ranks[shrink_a];
         uint16_t* srun = prm.s_out + static_cast<size_t>(shrink_run) * BT * prm.r_pad;
         if constexpr (!SWAP) {
-          // row m of the token block; columns are ranks
-          const bool in_run = m >= beg && m < end;
+          // row mt*128 + m of the token block; columns are ranks
+          for (int mt = 0; mt < C::MT; ++mt) {
+          const int row = mt * 128 + m;
+          const bool in_run = row >= beg && row < end;
           for (int c = 0; c < prm.r_pad; c += 16) {
             if (c < shrink_nch * kRankChunk) {
-              tmem_ld16(tq + c, v);
+              tmem_ld16(tq + mt * C::NACC + c, v);
               tmem_ld_wait();
             } else {
 #pragma unroll
@@ -292,9 +307,10 @@ __global__ void __launch_bounds__(192, 1)
               const float a1 = (in_run && c0 + 1 < r_a) ? __uint_as_float(v[2 * i + 1]) : 0.f;
               pk[i] = pack_bf16x2(a0, a1);
             }
-            uint4* dst = reinterpret_cast<uint4*>(srun + static_cast<size_t>(m) * prm.r_pad + c);
+            uint4* dst = reinterpret_cast<uint4*>(srun + static_cast<size_t>(row) * prm.r_pad + c);
             dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
             dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+          }
           }
         } else {
           // row m is rank index m; columns are the BT tokens of the block
@@ -315,11 +331,13 @@ __global__ void __launch_bounds__(192, 1)
       } else if constexpr (MODE == kGateUp) {
         const int I = prm.n_feat;
         if constexpr (!SWAP) {
-          uint16_t* hrow = prm.h_out + static_cast<size_t>(row0 + m) * I + f0;
+          for (int mt = 0; mt < C::MT; ++mt) {
+          uint16_t* hrow = prm.h_out + static_cast<size_t>(row0 + mt * 128 + m) * I + f0;
+          const uint32_t ta = tq + mt * C::NACC;
           for (int c = 0; c < 128; c += 16) {
             if (f0 + c >= I) break;
-            tmem_ld16(tq + c, v);          // gate features f0+c ..
-            tmem_ld16(tq + 128 + c, u);    // up features   f0+c ..
+            tmem_ld16(ta + c, v);          // gate features f0+c ..
+            tmem_ld16(ta + 128 + c, u);    // up features   f0+c ..
             tmem_ld_wait();
             uint32_t pk[8];
 #pragma unroll
@@ -329,6 +347,7 @@ __global__ void __launch_bounds__(192, 1)
             uint4* dst = reinterpret_cast<uint4*>(hrow + c);
             dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
             dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+          }
           }
         } else {
           const int f = f0 + m;           // feature of this thread; columns are tokens
@@ -348,13 +367,14 @@ __global__ void __launch_bounds__(192, 1)
       } else {  // kDown
         const int H = prm.n_feat;
         if constexpr (!SWAP) {
-          const int p = prm.sorted_p[row0 + m];
+          for (int mt = 0; mt < C::MT; ++mt) {
+          const int p = prm.sorted_p[row0 + mt * 128 + m];
           const bool valid = p < prm.P;
           const float w = valid ? prm.topk_w[p] : 0.f;
           float* orow = prm.out_acc + static_cast<size_t>(valid ? p / prm.k : 0) * H + f0;
           for (int c = 0; c < 256; c += 16) {
             if (f0 + c >= H) break;
-            tmem_ld16(tq + c, v);
+            tmem_ld16(tq + mt * C::NACC + c, v);
             tmem_ld_wait();
             if (valid) {
 #pragma unroll
@@ -363,6 +383,7 @@ __global__ void __launch_bounds__(192, 1)
                           make_float4(w * __uint_as_float(v[4 * i]), w * __uint_as_float(v[4 * i + 1]),
                                       w * __uint_as_float(v[4 * i + 2]), w * __uint_as_float(v[4 * i + 3])));
             }
+          }
           }
         } else {
 #pragma unroll

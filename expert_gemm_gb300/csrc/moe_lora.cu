@@ -80,8 +80,8 @@ int validate_dims(const moe_lora_dims* d) {
   if (d->k < 1 || d->k > d->E || d->k > MOE_LORA_MAX_TOPK)
     return fail(MOE_LORA_EINVAL, "k = %d outside [1, min(E, %d)]", d->k, MOE_LORA_MAX_TOPK);
   if (d->L < 0 || d->L > MOE_LORA_MAX_ADAPTERS) return fail(MOE_LORA_EUNSUPPORTED, "L = %d outside [0, %d]", d->L, MOE_LORA_MAX_ADAPTERS);
-  if (d->block_m != 16 && d->block_m != 32 && d->block_m != 64 && d->block_m != 128)
-    return fail(MOE_LORA_EUNSUPPORTED, "block_m = %d not in {16, 32, 64, 128}", d->block_m);
+  if (d->block_m != 16 && d->block_m != 32 && d->block_m != 64 && d->block_m != 128 && d->block_m != 256)
+    return fail(MOE_LORA_EUNSUPPORTED, "block_m = %d not in {16, 32, 64, 128, 256}", d->block_m);
   if (d->T * (int64_t)d->k >= (int64_t(1) << 30)) return fail(MOE_LORA_EUNSUPPORTED, "T*k too large");
   if (d->L > 0) {
     if (d->r_max < 8 || d->r_max > MOE_LORA_MAX_RANK || d->r_max % 8)
@@ -492,6 +492,7 @@ const char* moe_lora_last_error(void) { return g_err; }
 int32_t moe_lora_pick_block_m(int64_t T, int32_t k, int32_t E) {
   if (E <= 0 || k <= 0 || T <= 0) return 16;
   const double per_expert = (double)T * k / E;
+  if (per_expert >= 1024.0) return 256;
   if (per_expert >= 96.0) return 128;
   if (per_expert > 24.0) return 64;
   if (per_expert > 10.0) return 32;

@@ -88,7 +88,7 @@ typedef struct moe_lora_dims {
     int32_t L;        /* adapters, 0..MOE_LORA_MAX_ADAPTERS                             */
     int32_t r_max;    /* storage rank: rows of A, columns of Bt; multiple of 8, <= 64   */
     int32_t block_m;  /* rows per align block: 16, 32, 64 (weight-streaming kernels)    */
-                      /* or 128 (token-tiled kernels); see moe_lora_pick_block_m        */
+                      /* or 128, 256 (token-tiled kernels); see moe_lora_pick_block_m   */
     const int32_t *ranks; /* HOST array [L]: rank of adapter a, 1 <= ranks[a] <= r_max  */
 } moe_lora_dims;
 
@@ -125,7 +125,7 @@ int moe_lora_align_capacity(const moe_lora_dims *d, int64_t *max_rows, int64_t *
 int moe_lora_workspace_size(const moe_lora_dims *d, size_t *align_bytes, size_t *forward_bytes);
 
 /* A block_m suited to T*k pairs over E experts (16..64 when experts see few tokens,
- * 128 otherwise). */
+ * 128 or 256 when they see many). */
 int32_t moe_lora_pick_block_m(int64_t T, int32_t k, int32_t E);
 
 /* ------------------------------------------------------------ the calls -- */

@@ -69,7 +69,7 @@ def test_config_sampled(ml, torch, oracle, name):
     run_case(ml, torch, oracle, wl, tokens=sample_tokens(wl.T, 40))
 
 
-@pytest.mark.parametrize("block_m", [16, 32, 64, 128])
+@pytest.mark.parametrize("block_m", [16, 32, 64, 128, 256])
 def test_every_block_size(ml, torch, oracle, block_m):
     """Both tile orientations on one layer with several tiles and a ragged tail."""
     wl = W.custom(name="mid", T=200, H=384, I=448, E=6, k=2, L=3, ranks=(16, 32, 8), lora_mode="uniform_with_none")
@@ -103,7 +103,7 @@ def test_all_tokens_one_expert(ml, torch, oracle):
     logits, _, _, _ = inputs(wl)
     logits = logits.copy()
     logits[:, 5] += 100.0
-    for bm in (16, 128):
+    for bm in (16, 128, 256):
         run_case(ml, torch, oracle, wl, block_m=bm, logits=logits)
 
 
