@@ -17,6 +17,17 @@ enum GemmMode : int {
 };
 
 constexpr int kKTile = 64;      // K elements per pipeline stage (one 128-byte swizzle row of bf16)
+
+// K elements per pipeline stage of a GEMM launch; host tensor maps use the same value.
+// Token-tiled gate_up/down may be compiled with 32 (64-byte rows, 64-byte swizzle,
+// twice the stages in the same shared memory); measured on GB300 the 64-wide stages
+// of the persistent kernel are faster, so 64 is the default everywhere.
+#ifndef MOE_TOKEN_TILED_BK
+#define MOE_TOKEN_TILED_BK 64
+#endif
+constexpr int gemm_bk(int mode, int block_m) {
+  return (block_m >= 128 && mode != kShrink) ? MOE_TOKEN_TILED_BK : kKTile;
+}
 constexpr int kRankChunk = 16;  // LoRA rank elements per MMA K-step
 
 // Parameters of one grouped-GEMM launch (passed by value, read-only on the device).
@@ -37,7 +48,9 @@ struct GemmParams {
   int32_t k;
   int32_t P;                    // T*k, the padding sentinel
   int32_t r_pad;                // S row length (r_max rounded up to 16)
-  int32_t ksplit;               // kDown: K splits (grid.z); partial sums meet in out_acc
+  int32_t* tile_ctr;            // tile counter of this launch (zero at launch; persistent CTAs take tiles)
+  int32_t n_ft;                 // feature tiles per token block (kGateUp, kDown)
+  int32_t ksplit;               // kDown: K splits; partial sums meet in out_acc
   int32_t lora_after_pdl;       // previous kernel is the shrink: wait for it only before the LoRA K-steps
   int32_t ranks[MOE_LORA_MAX_ADAPTERS];
 };
@@ -72,10 +85,11 @@ struct AlignLaunch {
 };
 cudaError_t launch_align(const AlignLaunch& a, cudaStream_t s);
 
-// Gathers x rows into sorted order and zeroes out_acc [n_acc floats] and *status.
+// Gathers x rows into sorted order and zeroes out_acc [n_acc floats], *status and the
+// n_ctr tile counters of the forward's GEMM launches.
 cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* sorted_p, const int32_t* totals, int64_t max_rows,
                                int H, int k, int P, uint16_t* x_sorted, float* out_acc, int64_t n_acc,
-                               int32_t* status, cudaStream_t s);
+                               int32_t* status, int32_t* ctr, int n_ctr, cudaStream_t s);
 cudaError_t launch_finalize(const float* acc, uint16_t* out, int64_t n, bool pdl, cudaStream_t s);
 // pdl: launch with programmatic stream serialisation (may overlap the previous kernel).
 cudaError_t launch_gemm(int mode, int bt, const GemmMaps& maps, const GemmParams& prm, int64_t max_blocks,

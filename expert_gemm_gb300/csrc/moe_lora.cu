@@ -137,8 +137,9 @@ AlignLayout align_layout(const moe_lora_dims* d) {
 
 // ---- forward scratch layout
 struct FwdLayout {
-  size_t xs, hs, sgu, sdn, acc, bytes;
+  size_t xs, hs, sgu, sdn, acc, ctr, bytes;
 };
+constexpr int kNumGemmCounters = 4;   // shrink_gu, gate_up, shrink_dn, down
 FwdLayout fwd_layout(const moe_lora_dims* d) {
   const Caps c = capacity(d);
   FwdLayout l{};
@@ -149,6 +150,7 @@ FwdLayout fwd_layout(const moe_lora_dims* d) {
   l.sgu = off; off += up256((size_t)c.runs * s_tile);
   l.sdn = off; off += up256((size_t)c.runs * s_tile);
   l.acc = off; off += up256((size_t)d->T * d->H * 4);
+  l.ctr = off; off += up256(kNumGemmCounters * 4);
   l.bytes = off;
   return l;
 }
@@ -206,9 +208,9 @@ int sm_count() {
   return n;
 }
 
-// K splits of the weight-streaming down GEMM: only when the tiles cannot fill one wave
-// (each extra CTA pays its own prologue, which costs more than a partial last wave);
-// each split keeps at least 8 K-tiles.  The token-tiled (compute-bound) shape keeps one.
+// K splits of the weight-streaming down GEMM: enough tiles for about six per
+// persistent CTA, so the CTAs finish together; each split keeps at least 8 K-tiles.
+// The token-tiled (compute-bound) shape keeps one.
 int down_ksplit(const moe_lora_dims* d, const Caps& cap) {
   if (d->block_m >= 128) return 1;
   const int64_t P = d->T * d->k;
@@ -216,7 +218,7 @@ int down_ksplit(const moe_lora_dims* d, const Caps& cap) {
   if (est_blocks > d->E) est_blocks = d->E;
   if (est_blocks > P) est_blocks = P;
   const int64_t tiles = (int64_t)((d->H + 255) / 256) * (est_blocks > 0 ? est_blocks : 1);
-  int64_t ks = ((int64_t)sm_count() + tiles - 1) / tiles;
+  int64_t ks = (6 * (int64_t)sm_count() + tiles - 1) / tiles;
   const int64_t nk = d->I / 64;
   const int64_t ks_max = nk / 8 < 4 ? (nk / 8 > 1 ? nk / 8 : 1) : 4;
   if (ks > ks_max) ks = ks_max;
@@ -308,6 +310,7 @@ int do_forward(const moe_lora_dims* d, const uint16_t* x, const float* topk_w, c
   uint16_t* sgu = reinterpret_cast<uint16_t*>(base + l.sgu);
   uint16_t* sdn = reinterpret_cast<uint16_t*>(base + l.sdn);
   float* acc = reinterpret_cast<float*>(base + l.acc);
+  int32_t* ctr = reinterpret_cast<int32_t*>(base + l.ctr);
   const int BT = d->block_m;
   const uint64_t H = d->H, I = d->I, E = d->E, LE = (uint64_t)d->L * d->E, R = d->r_max;
   const uint64_t rows = cap.rows, RP = r_pad_of(d);
@@ -315,28 +318,34 @@ int do_forward(const moe_lora_dims* d, const uint16_t* x, const float* topk_w, c
 
   // tensor maps (dims innermost first; strides in bytes for dims 1..rank-1)
   moe::GemmMaps m_sgu{}, m_gu{}, m_sdn{}, m_dn{};
+  // K width of each launch's stages and the matching swizzle (64 -> 128-byte, 32 -> 64-byte)
+  const uint32_t bk_gu = (uint32_t)moe::gemm_bk(moe::kGateUp, BT), bk_dn = (uint32_t)moe::gemm_bk(moe::kDown, BT);
+  const uint32_t bk_sh = (uint32_t)moe::gemm_bk(moe::kShrink, BT);
+  auto swz = [](uint32_t bk) { return bk == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B; };
   {
     const uint64_t dm[4] = {H, I, 2, E}, st[3] = {H * 2, I * H * 2, 2 * I * H * 2};
-    const uint32_t bx[4] = {64, 128, 1, 1};
-    MOE_TRY(encode(&m_gu.w, W_gu, 4, dm, st, bx, CU_TENSOR_MAP_SWIZZLE_128B, "W_gu"));
+    const uint32_t bx[4] = {bk_gu, 128, 1, 1};
+    MOE_TRY(encode(&m_gu.w, W_gu, 4, dm, st, bx, swz(bk_gu), "W_gu"));
   }
   {
     const uint64_t dm[3] = {I, H, E}, st[2] = {I * 2, H * I * 2};
-    const uint32_t bx[3] = {64, 128, 1};
-    MOE_TRY(encode(&m_dn.w, W_dn, 3, dm, st, bx, CU_TENSOR_MAP_SWIZZLE_128B, "W_dn"));
+    const uint32_t bx[3] = {bk_dn, 128, 1};
+    MOE_TRY(encode(&m_dn.w, W_dn, 3, dm, st, bx, swz(bk_dn), "W_dn"));
   }
   {
     const uint64_t dm[2] = {H, rows}, st[1] = {H * 2};
-    const uint32_t bx[2] = {64, (uint32_t)BT};
-    MOE_TRY(encode(&m_gu.tok, xs, 2, dm, st, bx, CU_TENSOR_MAP_SWIZZLE_128B, "x_sorted"));
+    const uint32_t bx[2] = {bk_gu, (uint32_t)BT};
+    MOE_TRY(encode(&m_gu.tok, xs, 2, dm, st, bx, swz(bk_gu), "x_sorted"));
+    const uint32_t bxs[2] = {bk_sh, (uint32_t)BT};
+    MOE_TRY(encode(&m_sgu.tok, xs, 2, dm, st, bxs, swz(bk_sh), "x_sorted"));
   }
   {
     const uint64_t dm[2] = {I, rows}, st[1] = {I * 2};
-    const uint32_t bx[2] = {64, (uint32_t)BT};
-    MOE_TRY(encode(&m_dn.tok, hs, 2, dm, st, bx, CU_TENSOR_MAP_SWIZZLE_128B, "h_sorted"));
+    const uint32_t bx[2] = {bk_dn, (uint32_t)BT};
+    MOE_TRY(encode(&m_dn.tok, hs, 2, dm, st, bx, swz(bk_dn), "h_sorted"));
+    const uint32_t bxs[2] = {bk_sh, (uint32_t)BT};
+    MOE_TRY(encode(&m_sdn.tok, hs, 2, dm, st, bxs, swz(bk_sh), "h_sorted"));
   }
-  m_sgu.tok = m_gu.tok;
-  m_sdn.tok = m_dn.tok;
   if (d->L > 0) {
     {
       const uint64_t dm[3] = {H, R, LE}, st[2] = {H * 2, R * H * 2};
@@ -398,13 +407,14 @@ int do_forward(const moe_lora_dims* d, const uint16_t* x, const float* topk_w, c
   const bool lora = d->L > 0;
   MOE_CUDA(mark(0));
   MOE_CUDA(moe::launch_gather_rows(x, al->sorted_p, al->totals, cap.rows, d->H, d->k, p.P, xs, acc,
-                                   d->T * (int64_t)d->H, dev_status, s));
+                                   d->T * (int64_t)d->H, dev_status, ctr, kNumGemmCounters, s));
   MOE_CUDA(mark(1 + MOE_LORA_STAGE_GATHER));
 
   if (lora) {
     moe::GemmParams q = p;
     q.K = d->H;
     q.s_out = sgu;
+    q.tile_ctr = ctr + 0;
     MOE_CUDA(moe::launch_gemm(moe::kShrink, BT, m_sgu, q, cap.blocks, cap.runs, true, s));
   }
   MOE_CUDA(mark(1 + MOE_LORA_STAGE_SHRINK_GU));
@@ -414,6 +424,8 @@ int do_forward(const moe_lora_dims* d, const uint16_t* x, const float* topk_w, c
     q.n_feat = d->I;
     q.h_out = hs;
     q.lora_after_pdl = lora;
+    q.tile_ctr = ctr + 1;
+    q.n_ft = (d->I + 127) / 128;
     MOE_CUDA(moe::launch_gemm(moe::kGateUp, BT, m_gu, q, cap.blocks, cap.runs, true, s));
   }
   MOE_CUDA(mark(1 + MOE_LORA_STAGE_GATE_UP));
@@ -421,6 +433,7 @@ int do_forward(const moe_lora_dims* d, const uint16_t* x, const float* topk_w, c
     moe::GemmParams q = p;
     q.K = d->I;
     q.s_out = sdn;
+    q.tile_ctr = ctr + 2;
     MOE_CUDA(moe::launch_gemm(moe::kShrink, BT, m_sdn, q, cap.blocks, cap.runs, true, s));
   }
   MOE_CUDA(mark(1 + MOE_LORA_STAGE_SHRINK_DN));
@@ -431,6 +444,8 @@ int do_forward(const moe_lora_dims* d, const uint16_t* x, const float* topk_w, c
     q.out_acc = acc;
     q.lora_after_pdl = lora;
     q.ksplit = down_ksplit(d, cap);
+    q.tile_ctr = ctr + 3;
+    q.n_ft = (d->H + 255) / 256;
     MOE_CUDA(moe::launch_gemm(moe::kDown, BT, m_dn, q, cap.blocks, cap.runs, true, s));
   }
   MOE_CUDA(mark(1 + MOE_LORA_STAGE_DOWN));
@@ -492,8 +507,7 @@ const char* moe_lora_last_error(void) { return g_err; }
 int32_t moe_lora_pick_block_m(int64_t T, int32_t k, int32_t E) {
   if (E <= 0 || k <= 0 || T <= 0) return 16;
   const double per_expert = (double)T * k / E;
-  if (per_expert >= 1024.0) return 256;
-  if (per_expert >= 96.0) return 128;
+  if (per_expert >= 96.0) return 128;   // 256 is accepted but measured slower with double-buffered TMEM
   if (per_expert > 24.0) return 64;
   if (per_expert > 10.0) return 32;
   return 16;

@@ -13,12 +13,14 @@ namespace {
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ sorted_p,
                                                           const int32_t* __restrict__ totals, int64_t max_rows, int vec_per_row,
                                                           int k, int P, uint4* __restrict__ xs, float4* __restrict__ acc,
-                                                          int64_t n_acc4, int32_t* __restrict__ status) {
+                                                          int64_t n_acc4, int32_t* __restrict__ status,
+                                                          int32_t* __restrict__ ctr, int n_ctr) {
   pdl_trigger();   // the next kernel waits for this grid before reading what it writes
   const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t nthr = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t i = tid; i < n_acc4; i += nthr) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   if (tid == 0) *status = 0;
+  if (tid < n_ctr) ctr[tid] = 0;
   const int lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (row >= max_rows || row >= totals[0]) return;
@@ -47,13 +49,13 @@ __global__ void __launch_bounds__(256) finalize_kernel(const float4* __restrict_
 
 cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* sorted_p, const int32_t* totals, int64_t max_rows,
                                int H, int k, int P, uint16_t* x_sorted, float* out_acc, int64_t n_acc,
-                               int32_t* status, cudaStream_t s) {
+                               int32_t* status, int32_t* ctr, int n_ctr, cudaStream_t s) {
   const int rows_per_cta = 8;
   int64_t grid = (max_rows + rows_per_cta - 1) / rows_per_cta;
   if (grid < 1) grid = 1;
   gather_rows_kernel<<<static_cast<unsigned>(grid), rows_per_cta * 32, 0, s>>>(
       reinterpret_cast<const uint4*>(x), sorted_p, totals, max_rows, H / 8, k, P, reinterpret_cast<uint4*>(x_sorted),
-      reinterpret_cast<float4*>(out_acc), n_acc / 4, status);
+      reinterpret_cast<float4*>(out_acc), n_acc / 4, status, ctr, n_ctr);
   return cudaGetLastError();
 }
 

@@ -125,7 +125,7 @@ int moe_lora_align_capacity(const moe_lora_dims *d, int64_t *max_rows, int64_t *
 int moe_lora_workspace_size(const moe_lora_dims *d, size_t *align_bytes, size_t *forward_bytes);
 
 /* A block_m suited to T*k pairs over E experts (16..64 when experts see few tokens,
- * 128 or 256 when they see many). */
+ * 128 when they see many). */
 int32_t moe_lora_pick_block_m(int64_t T, int32_t k, int32_t E);
 
 /* ------------------------------------------------------------ the calls -- */
