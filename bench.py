@@ -127,27 +127,61 @@ def workload_of(args) -> W.Workload:
 
 # -------------------------------------------------------------- our arm -----
 
-def run_ours(args, rank, world, local_rank):
+KERNEL_SOURCES = ("gemm_tc.cuh", "ptx.cuh", "common.cuh", "gemm_tc.cu")
+
+
+def kernel_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "expert_gemm_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch from a committed ncu capture, if it was taken of the current kernel source."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            doc = json.load(f)
+    except Exception:
+        return None
+    e = doc.get(workload, {}).get(kernel)
+    if not e or e.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    """The largest value over all ranks (every rank gets it); the value itself when alone."""
+    if world <= 1:
+        return value
     import torch
-    from expert_gemm_gb300 import build, moe_lora as ml
-    torch.cuda.set_device(local_rank)
-    build.build()
-    ml.load()
-    wl = workload_of(args)
-    seed_w, seed_b = 0, rank                      # same weights on every replica, own batch per rank
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(tokens_per_rank: int, world: int, ms_per_step: float) -> float:
+    """Whole-job tokens/s: every rank's tokens over the slowest rank's step time."""
+    return world * tokens_per_rank / (ms_per_step * 1e-3)
+
+
+def _dev(torch, a):
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).cuda().view(torch.bfloat16)
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def measure(torch, ml, wl, wd, seed_b, K, Wm, bm, world, flush, graph=False, e2e=True, clocks=None):
+    """Times K steps of one workload on resident inputs; returns a dict of measurements."""
     logits, lora = W.make_routing(wl, seed_b)
     x = W.make_activations(wl, seed_b)
-    w = W.make_weights(wl, seed_w)
-    bm = args.block_m or ml.pick_block_m(wl.T, wl.k, wl.E)
     d = ml.LayerDims(T=wl.T, H=wl.H, I=wl.I, E=wl.E, k=wl.k, L=wl.L, r_max=wl.r_max, block_m=bm, ranks=wl.ranks)
-    dev = lambda a: (torch.from_numpy(a.view(np.int16)).cuda().view(torch.bfloat16) if a.dtype == np.uint16  # noqa
-                     else torch.from_numpy(np.ascontiguousarray(a)).cuda())
-    wd = {n: dev(w[n]) for n in ("W_gu", "W_dn", "A_gu", "Bt_gu", "A_dn", "Bt_dn")}
-    del w
     layer = ml.Layer(d, wd)
-    lg, lr, xd = dev(logits), dev(lora), dev(x)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
-    K, Wm = args.steps, args.warmup
+    lg, lr, xd = _dev(torch, logits), _dev(torch, lora), _dev(torch, x)
     KI = max(1, min(K, 100))                      # instrumented steps (per-stage events)
     nst = ml.NUM_STAGES + 1
     stage_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nst)] for _ in range(KI)]
@@ -164,15 +198,14 @@ def run_ours(args, rank, world, local_rank):
     ids = layer.topk_ids.cpu().numpy()
     tot = layer.bufs["totals"].cpu().numpy()
     P = wl.T * wl.k
-    align_launches = 1 if P <= 4096 else 3
-    launches_per_step = 1 + align_launches + 4 + (2 if wl.L > 0 else 0)
+    launches_per_step = 1 + (1 if P <= 4096 else 3) + 4 + (2 if wl.L > 0 else 0)
     acct = algorithmic(wl, ids, lora)
 
-    clocks = ClockSampler(local_rank)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    clocks.start()
+    if clocks is not None:
+        clocks.start()
     t_wall0 = time.perf_counter()
     # headline: K plain steps (events only at step boundaries)
     for i in range(K):
@@ -188,67 +221,149 @@ def run_ours(args, rank, world, local_rank):
     t_wall = time.perf_counter() - t_wall0
     if world > 1:
         torch.distributed.barrier()
-    clk = clocks.stop()
+    clk = clocks.stop() if clocks is not None else None
     step_ms = [a.elapsed_time(b) for a, b in step_ev]
     stage_ms = np.array([[evs[j].elapsed_time(evs[j + 1]) for j in range(nst - 1)] for evs in stage_ev])
-    ms = float(np.sum(step_ms)) / K
-    if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64, device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(float(np.sum(step_ms)) / K, world)
     if int(layer.status.item()) != 0:
         raise RuntimeError(f"device status {int(layer.status.item())}")
+    out = {"wl": wl, "bm": bm, "ms": ms, "K": K, "KI": KI, "stage_ms": stage_ms, "acct": acct, "clocks": clk,
+           "t_wall": t_wall, "totals": [int(v) for v in tot], "launches": launches_per_step * (K + KI)}
 
-    # end to end through the host-buffer entry point (pinned host memory)
-    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
-    lg_h, lr_h, x_h = pin(logits), pin(lora), pin(x.view(np.int16))
-    out_h = torch.empty((wl.T, wl.H), dtype=torch.int16).pin_memory()
-    for _ in range(max(2, min(Wm, 10))):
-        layer.step_host(lg_h, lr_h, x_h, out_h)
-    ke = max(1, min(K, 500))
-    if world > 1:
-        torch.distributed.barrier()
-    t0 = time.perf_counter()
-    for _ in range(ke):
-        layer.step_host(lg_h, lr_h, x_h, out_h)
-    e2e_s = (time.perf_counter() - t0) / ke
-    if world > 1:
-        t = torch.tensor([e2e_s], dtype=torch.float64, device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    if graph:
+        try:
+            out["graph_ms"] = _graph_ms(torch, layer, lg, lr, xd, flush, K)
+        except Exception as exc:   # report, keep the rest of the measurement
+            out["graph_error"] = f"{type(exc).__name__}: {exc}"[:300]
+    if e2e:
+        # end to end through the host-buffer entry point (pinned host memory)
+        pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
+        lg_h, lr_h, x_h = pin(logits), pin(lora), pin(x.view(np.int16))
+        out_h = torch.empty((wl.T, wl.H), dtype=torch.int16).pin_memory()
+        for _ in range(max(2, min(Wm, 10))):
+            layer.step_host(lg_h, lr_h, x_h, out_h)
+        ke = max(1, min(K, 500))
+        if world > 1:
+            torch.distributed.barrier()
+        t0 = time.perf_counter()
+        for _ in range(ke):
+            layer.step_host(lg_h, lr_h, x_h, out_h)
+        out["e2e_s"] = max_over_ranks((time.perf_counter() - t0) / ke, world)
+    del layer
+    return out
 
+
+def _graph_ms(torch, layer, lg, lr, xd, flush, K):
+    """The same step captured once into a CUDA graph and replayed (launch overhead off the host)."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        layer.step(lg, lr, xd, stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        layer.step(lg, lr, xd)
+    for _ in range(3):
+        g.replay()
+        flush.zero_()
+    gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    torch.cuda.synchronize()
+    for i in range(K):
+        gev[i][0].record()
+        g.replay()
+        gev[i][1].record()
+        flush.zero_()
+    torch.cuda.synchronize()
+    if int(layer.status.item()) != 0:
+        raise RuntimeError(f"device status {int(layer.status.item())} after graph replay")
+    return float(np.mean([a.elapsed_time(b) for a, b in gev]))
+
+
+def roofline_of(m, ml):
+    """Dominant-kernel roofline (gate_up) and the whole-layer roofline of one measurement."""
     hbm, tc, tc_sus, src = peaks()
-    gu_ms = float(np.mean(stage_ms[:, 2]))
-    gu_gbs = acct["gate_up_bytes"] / (gu_ms * 1e-3) / 1e9
-    layer_s = ms * 1e-3
-    roof_s = max(acct["bytes"] / (hbm * 1e9), acct["flops"] / (tc * 1e12))
+    acct, wl = m["acct"], m["wl"]
+    gu_ms = float(np.mean(m["stage_ms"][:, ml.STAGES.index("gate_up")]))
+    intensity = acct["gate_up_flops"] / max(acct["gate_up_bytes"], 1)
+    ridge = tc * 1e12 / (hbm * 1e9)
+    kname = "gate_up (tcgen05 grouped GEMM + LoRA expand + SiLU)"
+    if intensity < ridge:
+        ach = acct["gate_up_bytes"] / (gu_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "kernel": kname, "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
+                "peak_source": f"{src} (HBM copy)", "algorithmic_bytes_per_launch": acct["gate_up_bytes"]}
+    else:
+        ach = acct["gate_up_flops"] / (gu_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "kernel": kname, "achieved": ach, "peak": tc, "unit": "TFLOP/s",
+                "frac": ach / tc, "peak_source": f"{src} (cuBLAS bf16 burst)",
+                "algorithmic_flops_per_launch": acct["gate_up_flops"]}
+    roof["launch_ms"] = gu_ms
+    roof["traffic"] = committed_traffic(wl.name, "gate_up")
+    layer_s = m["ms"] * 1e-3
+    t_bw, t_tc = acct["bytes"] / (hbm * 1e9), acct["flops"] / (tc * 1e12)
+    layer = {"alg_bytes": acct["bytes"], "alg_flops": acct["flops"], "t_roof_ms": max(t_bw, t_tc) * 1e3,
+             "bound": "hbm" if t_bw >= t_tc else "tensor", "frac": max(t_bw, t_tc) / layer_s,
+             "hbm_gbs_peak": hbm, "bf16_tflops_peak": tc}
+    return roof, layer
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    from expert_gemm_gb300 import build, moe_lora as ml
+    torch.cuda.set_device(local_rank)
+    build.build()
+    ml.load()
+    wl = workload_of(args)
+    w = W.make_weights(wl, 0)                     # same weights on every replica, own batch per rank
+    wd = {n: _dev(torch, w[n]) for n in ("W_gu", "W_dn", "A_gu", "Bt_gu", "A_dn", "Bt_dn")}
+    del w
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    bm = args.block_m or ml.pick_block_m(wl.T, wl.k, wl.E)
+    m = measure(torch, ml, wl, wd, rank, args.steps, args.warmup, bm, world, flush,
+                graph=not args.no_graph, clocks=ClockSampler(local_rank))
+    roof, layer = roofline_of(m, ml)
+    stage_ms = m["stage_ms"]
     res = {
-        "metric": METRIC, "value": world * wl.T / layer_s, "unit": "tokens/s", "n_gpus": world, "steps": K,
-        "warmup": Wm, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16", "data": "synthetic (seeded normals, bf16)",
+        "metric": METRIC, "value": job_throughput(wl.T, world, m["ms"]), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": m["ms"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded normals, bf16)",
         "config": {"workload": f"{wl.name}: T={wl.T} H={wl.H} I={wl.I} E={wl.E} top-{wl.k} L={wl.L} "
                                f"ranks={sorted(set(wl.ranks))}", "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E,
                    "k": wl.k, "L": wl.L, "block_m": bm, "global_batch": world * wl.T,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "flushed between timed steps (256 MiB write)"},
-        "roofline": {"bound": "hbm", "kernel": "gate_up (tcgen05 grouped GEMM + LoRA expand + SiLU)",
-                     "achieved": gu_gbs, "peak": hbm, "unit": "GB/s", "frac": gu_gbs / hbm,
-                     "peak_source": src, "traffic": None, "launch_ms": gu_ms,
-                     "algorithmic_bytes_per_launch": acct["gate_up_bytes"]},
-        "layer_roofline": {"alg_bytes": acct["bytes"], "alg_flops": acct["flops"], "t_roof_ms": roof_s * 1e3,
-                           "frac": roof_s / layer_s, "hbm_gbs_peak": hbm, "bf16_tflops_peak": tc},
+        "roofline": roof,
+        "layer_roofline": layer,
         "stage_ms": {n: float(np.mean(stage_ms[:, j])) for j, n in enumerate(ml.STAGES)},
         "instrumented_ms_per_step": float(np.mean(np.sum(stage_ms, axis=1))),
-        "instrumented_steps": KI,
-        "touched": {k_: acct[k_] for k_ in ("experts", "adapter_expert_pairs", "valid_pairs")},
-        "e2e": {"value": world * wl.T / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": wl.T * (wl.E * 4 + 4 + wl.H * 2),
-                "d2h_bytes_per_step": wl.T * wl.H * 2 + 4 + 16, "ms_per_step": e2e_s * 1e3,
+        "instrumented_steps": m["KI"],
+        "touched": {k_: m["acct"][k_] for k_ in ("experts", "adapter_expert_pairs", "valid_pairs")},
+        "e2e": {"value": job_throughput(wl.T, world, m["e2e_s"] * 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": wl.T * (wl.E * 4 + 4 + wl.H * 2),
+                "d2h_bytes_per_step": wl.T * wl.H * 2 + 4 + 16, "ms_per_step": m["e2e_s"] * 1e3,
                 "entry": "moe_lora_layer_host (pinned host buffers)"},
-        "gpu_launches": launches_per_step * (K + KI),
-        "clocks": clk,
-        "wall_s_timed": t_wall,
-        "align_totals": [int(v) for v in tot],
+        "gpu_launches": m["launches"],
+        "clocks": m["clocks"],
+        "wall_s_timed": m["t_wall"],
+        "align_totals": m["totals"],
     }
+    if "graph_ms" in m:
+        res["cuda_graph"] = {"ms_per_step": m["graph_ms"], "value": world * wl.T / (m["graph_ms"] * 1e-3),
+                             "unit": "tokens/s", "note": "the same step captured once and replayed"}
+    elif "graph_error" in m:
+        res["cuda_graph"] = {"error": m["graph_error"]}
+    # the prefill layer has the decode layer's shapes and weights: measure it too
+    if args.secondary and wl.name == "decode":
+        pw = W.get("prefill")
+        pk = max(3, min(args.steps, 20))
+        pm = measure(torch, ml, pw, wd, rank, pk, 3, ml.pick_block_m(pw.T, pw.k, pw.E), world, flush,
+                     graph=False, e2e=False)
+        proof, player = roofline_of(pm, ml)
+        res["prefill"] = {"workload": f"prefill: T={pw.T} (16 requests x 1600 tokens), decode-layer shapes",
+                          "value": world * pw.T / (pm["ms"] * 1e-3), "unit": "tokens/s", "ms_per_step": pm["ms"],
+                          "steps": pk, "block_m": pm["bm"], "roofline": proof, "layer_roofline": player,
+                          "stage_ms": {n: float(np.mean(pm["stage_ms"][:, j])) for j, n in enumerate(ml.STAGES)}}
+        res["gpu_launches"] += pm["launches"]
     return res
 
 
@@ -329,6 +444,9 @@ def main():
     ap.add_argument("--workload", default="decode", choices=sorted(W.WORKLOADS))
     ap.add_argument("--block-m", type=int, default=0)
     ap.add_argument("--tokens", type=int, default=0, help="override T of the workload (small profiling cases)")
+    ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay timing")
+    ap.add_argument("--no-secondary", dest="secondary", action="store_false",
+                    help="skip the prefill measurement that accompanies the decode workload")
     ap.add_argument("--cpu-baseline-s", type=float, default=12.0, help="seconds of oracle time (0 = skip)")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -574,21 +574,26 @@ cudaError_t launch_gemm_t(const GemmMaps& maps, const GemmParams& prm, int64_t m
                           bool pdl, cudaStream_t s) {
   using C = GemmCfg<MODE, SWAP, BT>;
   auto kern = moe_gemm_kernel<MODE, SWAP, BT>;
-  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-  if (err != cudaSuccess) return err;
   int64_t cap_tiles;
   if constexpr (MODE == kShrink) cap_tiles = max_runs;
   else cap_tiles = max_blocks * prm.n_ft * prm.ksplit;
   if (cap_tiles <= 0) return cudaSuccess;
-  // persistent grid: as many CTAs as fit on the device at once, no more than tiles
-  int dev = 0, sms = 0, per_sm = 0;
-  if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
-  if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return err;
-  if ((err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 192, C::SMEM_BYTES)) != cudaSuccess)
-    return err;
-  if (per_sm < 1) per_sm = 1;
-  // co-resident CTAs share TMEM: keep their accumulators within its 512 columns
-  while (per_sm > 1 && per_sm * C::TMEM_COLS > 512) --per_sm;
+  // Persistent grid: as many CTAs as fit on the device at once, no more than tiles.
+  // The attribute and the occupancy are settled on the first launch of this kernel
+  // (per process: one device model), so later launches make no such calls.
+  static int per_sm = 0, sms = 0;
+  if (per_sm == 0) {
+    int dev = 0, occ = 0;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (err == cudaSuccess) err = cudaGetDevice(&dev);
+    if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (err == cudaSuccess) err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, 192, C::SMEM_BYTES);
+    if (err != cudaSuccess) return err;
+    if (occ < 1) occ = 1;
+    // co-resident CTAs share TMEM: keep their accumulators within its 512 columns
+    while (occ > 1 && occ * C::TMEM_COLS > 512) --occ;
+    per_sm = occ;
+  }
   int64_t grid = static_cast<int64_t>(sms) * per_sm;
   if (grid > cap_tiles) grid = cap_tiles;
 
