@@ -40,6 +40,10 @@ struct GemmParams {
   const float* topk_w;          // [T*k]
   uint16_t* h_out;              // kGateUp: h rows in sorted order [rows][I] (bf16)
   float* out_acc;               // kDown:   [T][H] fp32 accumulation
+  float* g_acc;                 // kGateUp with K splits: [rows][2I] fp32 pre-activations
+  float* s_part;                // kShrink with K splits: [ksplit][max_runs][BT][r_pad] fp32 partials
+  int32_t* s_cnt;               // kShrink with K splits: [max_runs] splits finished per run (zero at launch)
+  int32_t max_runs;
   uint16_t* s_out;              // kShrink: [runs][BT][r_pad] (bf16), rows outside the run zero
   int32_t* status;              // device status word (MOE_LORA_DEV_* bits)
   int32_t K;                    // reduction length of the base GEMM (H or I)
@@ -85,12 +89,16 @@ struct AlignLaunch {
 };
 cudaError_t launch_align(const AlignLaunch& a, cudaStream_t s);
 
-// Gathers x rows into sorted order and zeroes out_acc [n_acc floats], *status and the
-// n_ctr tile counters of the forward's GEMM launches.
+// Gathers x rows into sorted order and zeroes out_acc [n_acc floats], *status, the
+// n_ctr tile counters of the forward's GEMM launches and, when g_acc is given, the
+// g_cols fp32 pre-activations of every live sorted row.
 cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* sorted_p, const int32_t* totals, int64_t max_rows,
                                int H, int k, int P, uint16_t* x_sorted, float* out_acc, int64_t n_acc,
-                               int32_t* status, int32_t* ctr, int n_ctr, cudaStream_t s);
+                               int32_t* status, int32_t* ctr, int n_ctr, float* g_acc, int g_cols, cudaStream_t s);
 cudaError_t launch_finalize(const float* acc, uint16_t* out, int64_t n, bool pdl, cudaStream_t s);
+// h = bf16(silu(g[:, :I]) * g[:, I:]) for the live sorted rows, after a K-split gate_up.
+cudaError_t launch_silu_rows(const float* g_acc, const int32_t* totals, int64_t max_rows, int I, uint16_t* h,
+                             bool pdl, cudaStream_t s);
 // pdl: launch with programmatic stream serialisation (may overlap the previous kernel).
 cudaError_t launch_gemm(int mode, int bt, const GemmMaps& maps, const GemmParams& prm, int64_t max_blocks,
                         int64_t max_runs, bool pdl, cudaStream_t s);

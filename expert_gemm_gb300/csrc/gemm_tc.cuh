@@ -104,18 +104,20 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
 
 // One unit of work.  kShrink: one adapter run.  kGateUp / kDown: one (K split, token
-// block, feature tile), feature tile fastest.
+// block, feature tile), feature tile fastest.  Only weight-streaming (swapped) gate_up
+// splits K; its partial pre-activations then meet in fp32 and SiLU runs afterwards.
 struct Tile {
   int b, e, row0, f0;
   int run0, nruns;        // adapter runs of the block (first K split only)
   int kb0, nk;            // base K-tiles of this split
   int n_it;               // pipeline stages of this tile
   int srun, sa, snch;     // kShrink: run, adapter, rank chunks
+  int ks;                 // K split of this tile
 };
 
 template <int MODE>
 __device__ __forceinline__ int live_tiles(const GemmParams& prm) {
-  if constexpr (MODE == kShrink) return prm.totals[2];
+  if constexpr (MODE == kShrink) return prm.totals[2] * prm.ksplit;
   else return prm.totals[1] * prm.n_ft * prm.ksplit;
 }
 
@@ -129,19 +131,22 @@ __device__ __forceinline__ Tile decode_tile(int tau, const GemmParams& prm) {
   t.f0 = 0;
   t.srun = t.sa = t.snch = 0;
   if constexpr (MODE == kShrink) {
-    t.srun = tau;
-    t.b = prm.runs[4 * tau + 0];
-    t.sa = prm.runs[4 * tau + 1];
+    // the K splits of one run are consecutive tiles
+    t.srun = tau / prm.ksplit;
+    t.ks = tau % prm.ksplit;
+    t.b = prm.runs[4 * t.srun + 0];
+    t.sa = prm.runs[4 * t.srun + 1];
     t.snch = (prm.ranks[t.sa] + kRankChunk - 1) / kRankChunk;
-    t.kb0 = 0;
-    t.nk = nk_all;
-    t.n_it = nk_all;
+    t.kb0 = t.ks * nk_all / prm.ksplit;
+    t.nk = (t.ks + 1) * nk_all / prm.ksplit - t.kb0;
+    t.n_it = t.nk;
   } else {
     const int nb = prm.totals[1];
     const int ft = tau % prm.n_ft;
     const int rest = tau / prm.n_ft;
     t.b = rest % nb;
     const int ks = rest / nb;
+    t.ks = ks;
     t.f0 = ft * (MODE == kGateUp ? 128 : 256);
     if (ks == 0) {
       t.run0 = prm.block_runs[t.b];
@@ -457,7 +462,7 @@ __global__ void __launch_bounds__(192, 1)
                 dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
               }
             }
-          } else {
+          } else if (prm.ksplit == 1) {
             // row m is rank index m; columns are the BT tokens of the block
             for (int n0 = 0; n0 < BT; n0 += 16) {
               tmem_ld16(tq + n0, v);
@@ -469,6 +474,43 @@ __global__ void __launch_bounds__(192, 1)
                   const float val = (n >= beg && n < end && m < r_a) ? __uint_as_float(v[j]) : 0.f;
                   __nv_bfloat16 hv = __float2bfloat16_rn(val);
                   srun[static_cast<size_t>(n) * prm.r_pad + m] = *reinterpret_cast<uint16_t*>(&hv);
+                }
+              }
+            }
+          } else {
+            // K split: each epilogue warp owns 32 rank rows.  It stores this split's
+            // fp32 partial S for them, then counts itself in on a per-(run, warp)
+            // arrival counter; the warp that completes the count (no waiting) sums
+            // all splits' partials and writes those rows of the bf16 S tile.
+            // Partials: [split][run][BT][r_pad]; counters: [run][4].
+            if (q * 32 < prm.r_pad) {
+              const size_t part = (static_cast<size_t>(t.ks) * prm.max_runs + t.srun) * BT * prm.r_pad;
+              for (int n0 = 0; n0 < BT; n0 += 16) {
+                tmem_ld16(tq + n0, v);
+                tmem_ld_wait();
+                if (m < prm.r_pad) {
+#pragma unroll
+                  for (int j = 0; j < 16; ++j)
+                    prm.s_part[part + static_cast<size_t>(n0 + j) * prm.r_pad + m] = __uint_as_float(v[j]);
+                }
+              }
+              __threadfence();
+              __syncwarp();
+              int last = 0;
+              if (lane == 0) last = atomicAdd(prm.s_cnt + 4 * t.srun + q, 1) == prm.ksplit - 1;
+              last = __shfl_sync(0xffffffffu, last, 0);
+              if (last) {
+                __threadfence();
+                if (m < prm.r_pad) {
+                  for (int n = 0; n < BT; ++n) {
+                    float sum = 0.f;
+                    for (int sp = 0; sp < prm.ksplit; ++sp)
+                      sum += __ldcg(prm.s_part + (static_cast<size_t>(sp) * prm.max_runs + t.srun) * BT * prm.r_pad +
+                                    static_cast<size_t>(n) * prm.r_pad + m);
+                    const float val = (n >= beg && n < end && m < r_a) ? sum : 0.f;
+                    __nv_bfloat16 hv = __float2bfloat16_rn(val);
+                    srun[static_cast<size_t>(n) * prm.r_pad + m] = *reinterpret_cast<uint16_t*>(&hv);
+                  }
                 }
               }
             }
@@ -501,10 +543,20 @@ __global__ void __launch_bounds__(192, 1)
               tmem_ld16(tq + BT + n0, u);
               tmem_ld_wait();
               if (f < I) {
+                if (prm.ksplit > 1) {
+                  // K split: partial gate/up pre-activations meet in fp32; SiLU follows later
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                  __nv_bfloat16 hv = __float2bfloat16_rn(silu_f(__uint_as_float(v[j])) * __uint_as_float(u[j]));
-                  prm.h_out[static_cast<size_t>(row0 + n0 + j) * I + f] = *reinterpret_cast<uint16_t*>(&hv);
+                  for (int j = 0; j < 16; ++j) {
+                    float* g = prm.g_acc + static_cast<size_t>(row0 + n0 + j) * (2 * I);
+                    atomicAdd(g + f, __uint_as_float(v[j]));
+                    atomicAdd(g + I + f, __uint_as_float(u[j]));
+                  }
+                } else {
+#pragma unroll
+                  for (int j = 0; j < 16; ++j) {
+                    __nv_bfloat16 hv = __float2bfloat16_rn(silu_f(__uint_as_float(v[j])) * __uint_as_float(u[j]));
+                    prm.h_out[static_cast<size_t>(row0 + n0 + j) * I + f] = *reinterpret_cast<uint16_t*>(&hv);
+                  }
                 }
               }
             }
@@ -575,7 +627,7 @@ cudaError_t launch_gemm_t(const GemmMaps& maps, const GemmParams& prm, int64_t m
   using C = GemmCfg<MODE, SWAP, BT>;
   auto kern = moe_gemm_kernel<MODE, SWAP, BT>;
   int64_t cap_tiles;
-  if constexpr (MODE == kShrink) cap_tiles = max_runs;
+  if constexpr (MODE == kShrink) cap_tiles = max_runs * prm.ksplit;
   else cap_tiles = max_blocks * prm.n_ft * prm.ksplit;
   if (cap_tiles <= 0) return cudaSuccess;
   // Persistent grid: as many CTAs as fit on the device at once, no more than tiles.

@@ -137,9 +137,12 @@ AlignLayout align_layout(const moe_lora_dims* d) {
 
 // ---- forward scratch layout
 struct FwdLayout {
-  size_t xs, hs, sgu, sdn, acc, ctr, bytes;
+  size_t xs, hs, sgu, sdn, acc, ctr, gacc, pgu, pdn, bytes;
+  int n_ctr;
 };
-constexpr int kNumGemmCounters = 4;   // shrink_gu, gate_up, shrink_dn, down
+constexpr int kNumGemmCounters = 4;   // tile counters: shrink_gu, gate_up, shrink_dn, down
+constexpr int kPlanSMs = 152;         // SM count the K-split heuristics plan for (GB300)
+int shrink_ksplit(const moe_lora_dims* d, const Caps& cap, int K);
 FwdLayout fwd_layout(const moe_lora_dims* d) {
   const Caps c = capacity(d);
   FwdLayout l{};
@@ -150,7 +153,14 @@ FwdLayout fwd_layout(const moe_lora_dims* d) {
   l.sgu = off; off += up256((size_t)c.runs * s_tile);
   l.sdn = off; off += up256((size_t)c.runs * s_tile);
   l.acc = off; off += up256((size_t)d->T * d->H * 4);
-  l.ctr = off; off += up256(kNumGemmCounters * 4);
+  l.ctr = off; off += up256((size_t)(kNumGemmCounters + 2 * 4 * c.runs) * 4);
+  // fp32 gate/up pre-activations for a K-split (weight-streaming) gate_up
+  l.gacc = off; off += d->block_m < 128 ? up256((size_t)c.rows * 2 * d->I * 4) : 0;
+  // fp32 partial S of K-split shrinks, and their per-(run, warp) arrival counters
+  const size_t s_part = (size_t)c.runs * d->block_m * r_pad_of(d) * 4;
+  l.pgu = off; off += up256((size_t)shrink_ksplit(d, c, d->H) * s_part);
+  l.pdn = off; off += up256((size_t)shrink_ksplit(d, c, d->I) * s_part);
+  l.n_ctr = kNumGemmCounters + 2 * 4 * (int)c.runs;
   l.bytes = off;
   return l;
 }
@@ -208,19 +218,40 @@ int sm_count() {
   return n;
 }
 
-// K splits of the weight-streaming down GEMM: enough tiles for about six per
-// persistent CTA, so the CTAs finish together; each split keeps at least 8 K-tiles.
-// The token-tiled (compute-bound) shape keeps one.
-int down_ksplit(const moe_lora_dims* d, const Caps& cap) {
+// K splits of a weight-streaming GEMM (n_ft feature tiles per block, reduction K):
+// enough tiles for about `per_cta` per persistent CTA, so the CTAs finish together;
+// each split keeps at least 8 K-tiles, at most 4 splits.  Token-tiled (compute-bound)
+// shapes keep one.
+int weight_stream_ksplit(const moe_lora_dims* d, const Caps& cap, int n_ft, int K, int per_cta) {
   if (d->block_m >= 128) return 1;
   const int64_t P = d->T * d->k;
   int64_t est_blocks = cap.blocks;
   if (est_blocks > d->E) est_blocks = d->E;
   if (est_blocks > P) est_blocks = P;
-  const int64_t tiles = (int64_t)((d->H + 255) / 256) * (est_blocks > 0 ? est_blocks : 1);
-  int64_t ks = (6 * (int64_t)sm_count() + tiles - 1) / tiles;
-  const int64_t nk = d->I / 64;
+  const int64_t tiles = (int64_t)n_ft * (est_blocks > 0 ? est_blocks : 1);
+  int64_t ks = ((int64_t)per_cta * kPlanSMs + tiles - 1) / tiles;
+  const int64_t nk = K / 64;
   const int64_t ks_max = nk / 8 < 4 ? (nk / 8 > 1 ? nk / 8 : 1) : 4;
+  if (ks > ks_max) ks = ks_max;
+  return ks < 1 ? 1 : (int)ks;
+}
+int down_ksplit(const moe_lora_dims* d, const Caps& cap) {
+  return weight_stream_ksplit(d, cap, (d->H + 255) / 256, d->I, 6);
+}
+// gate_up splits only when its tiles are too few to spread over the SMs: a split adds
+// an fp32 round trip of the pre-activations and a SiLU pass.
+int gate_up_ksplit(const moe_lora_dims* d, const Caps& cap) {
+  return weight_stream_ksplit(d, cap, (d->I + 127) / 128, d->H, 2);
+}
+// The weight-streaming shrink splits K only for long reductions (>= 64 K-tiles) whose
+// runs cannot fill the SMs -- a run's tile otherwise walks all of K alone.  Measured:
+// splitting short reductions only adds per-tile overhead and keeps the SMs from the
+// next kernel.  About one tile per SM, each split at least 16 K-tiles, at most 8.
+int shrink_ksplit(const moe_lora_dims* d, const Caps& cap, int K) {
+  const int64_t nk = K / 64;
+  if (d->block_m >= 128 || d->L == 0 || cap.runs <= 0 || nk < 64 || cap.runs >= kPlanSMs) return 1;
+  int64_t ks = ((int64_t)kPlanSMs + cap.runs - 1) / cap.runs;
+  const int64_t ks_max = nk / 16 < 8 ? nk / 16 : 8;
   if (ks > ks_max) ks = ks_max;
   return ks < 1 ? 1 : (int)ks;
 }
@@ -311,6 +342,8 @@ int do_forward(const moe_lora_dims* d, const uint16_t* x, const float* topk_w, c
   uint16_t* sdn = reinterpret_cast<uint16_t*>(base + l.sdn);
   float* acc = reinterpret_cast<float*>(base + l.acc);
   int32_t* ctr = reinterpret_cast<int32_t*>(base + l.ctr);
+  const int ks_gu = gate_up_ksplit(d, cap);
+  float* gacc = ks_gu > 1 ? reinterpret_cast<float*>(base + l.gacc) : nullptr;
   const int BT = d->block_m;
   const uint64_t H = d->H, I = d->I, E = d->E, LE = (uint64_t)d->L * d->E, R = d->r_max;
   const uint64_t rows = cap.rows, RP = r_pad_of(d);
@@ -395,6 +428,7 @@ int do_forward(const moe_lora_dims* d, const uint16_t* x, const float* topk_w, c
   p.r_pad = (int32_t)RP;
   p.ksplit = 1;
   p.lora_after_pdl = 0;
+  p.max_runs = (int32_t)cap.runs;
   for (int a = 0; a < d->L; ++a) p.ranks[a] = d->ranks[a];
 
   auto mark = [&](int i) -> cudaError_t {
@@ -407,7 +441,7 @@ int do_forward(const moe_lora_dims* d, const uint16_t* x, const float* topk_w, c
   const bool lora = d->L > 0;
   MOE_CUDA(mark(0));
   MOE_CUDA(moe::launch_gather_rows(x, al->sorted_p, al->totals, cap.rows, d->H, d->k, p.P, xs, acc,
-                                   d->T * (int64_t)d->H, dev_status, ctr, kNumGemmCounters, s));
+                                   d->T * (int64_t)d->H, dev_status, ctr, l.n_ctr, gacc, 2 * d->I, s));
   MOE_CUDA(mark(1 + MOE_LORA_STAGE_GATHER));
 
   if (lora) {
@@ -415,6 +449,9 @@ int do_forward(const moe_lora_dims* d, const uint16_t* x, const float* topk_w, c
     q.K = d->H;
     q.s_out = sgu;
     q.tile_ctr = ctr + 0;
+    q.ksplit = shrink_ksplit(d, cap, d->H);
+    q.s_part = reinterpret_cast<float*>(base + l.pgu);
+    q.s_cnt = ctr + kNumGemmCounters;
     MOE_CUDA(moe::launch_gemm(moe::kShrink, BT, m_sgu, q, cap.blocks, cap.runs, true, s));
   }
   MOE_CUDA(mark(1 + MOE_LORA_STAGE_SHRINK_GU));
@@ -426,7 +463,10 @@ int do_forward(const moe_lora_dims* d, const uint16_t* x, const float* topk_w, c
     q.lora_after_pdl = lora;
     q.tile_ctr = ctr + 1;
     q.n_ft = (d->I + 127) / 128;
+    q.ksplit = ks_gu;
+    q.g_acc = gacc;
     MOE_CUDA(moe::launch_gemm(moe::kGateUp, BT, m_gu, q, cap.blocks, cap.runs, true, s));
+    if (ks_gu > 1) MOE_CUDA(moe::launch_silu_rows(gacc, al->totals, cap.rows, d->I, hs, true, s));
   }
   MOE_CUDA(mark(1 + MOE_LORA_STAGE_GATE_UP));
   if (lora) {
@@ -434,6 +474,9 @@ int do_forward(const moe_lora_dims* d, const uint16_t* x, const float* topk_w, c
     q.K = d->I;
     q.s_out = sdn;
     q.tile_ctr = ctr + 2;
+    q.ksplit = shrink_ksplit(d, cap, d->I);
+    q.s_part = reinterpret_cast<float*>(base + l.pdn);
+    q.s_cnt = ctr + kNumGemmCounters + 4 * cap.runs;
     MOE_CUDA(moe::launch_gemm(moe::kShrink, BT, m_sdn, q, cap.blocks, cap.runs, true, s));
   }
   MOE_CUDA(mark(1 + MOE_LORA_STAGE_SHRINK_DN));

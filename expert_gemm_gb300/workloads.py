@@ -20,6 +20,10 @@ vLLM" and Figure 3 -- is stood in for by synthetic tensors of those shapes):
   sweep_T{1,16,256,4096}
               T       H=2048 I=768   E=128 k=8  L=64 r{16,64} ids Zipf(1.1) with 10% -1,
                                                               logit bias N(0,0.5)
+  dense_decode T=16   H=5120 I=25600 E=1   k=1  L=8  r=32     ids uniform {0..7}
+              (multi-LoRA on a dense SwiGLU MLP of a 32B-class model: the single
+              "expert" is the MLP; the pages report the same optimisations helping
+              dense models, section "Results & Conclusion")
 
 Value recipe: x ~ N(0,1); router logits ~ N(0,1) (fp32, plus the per-expert
 bias where the workload has one, added in fp32); W, A, B ~ N(0, 0.02).  Every
@@ -92,6 +96,7 @@ WORKLOADS = {
                         "per_request", requests=16),
     "wide": Workload("wide", 4096, 4096, 11008, 8, 2, 32, (32,) * 32, "zipf",
                      bias_std=1.0),
+    "dense_decode": Workload("dense_decode", 16, 5120, 25600, 1, 1, 8, (32,) * 8, "uniform"),
     "sweep_T1": _sweep(1),
     "sweep_T16": _sweep(16),
     "sweep_T256": _sweep(256),

@@ -84,6 +84,32 @@ def test_down_split_k(ml, torch, oracle, block_m):
     run_case(ml, torch, oracle, wl, block_m=block_m)
 
 
+def test_shrink_split_k(ml, torch, oracle):
+    """A long reduction (I = 8192) over few adapter runs: the weight-streaming down shrink
+    splits K; the last split of each run sums the fp32 partials."""
+    wl = W.custom(name="shsplit", T=6, H=256, I=8192, E=2, k=1, L=3, ranks=(16, 64, 32), lora_mode="uniform")
+    run_case(ml, torch, oracle, wl, block_m=16)
+
+
+def test_gate_up_split_k(ml, torch, oracle):
+    """Few feature tiles: the weight-streaming gate_up splits K, its fp32 partials meet
+    before SiLU; the down GEMM splits too."""
+    wl = W.custom(name="gusplit", T=8, H=1024, I=512, E=2, k=1, L=2, ranks=(16, 32), lora_mode="uniform_with_none")
+    run_case(ml, torch, oracle, wl, block_m=16)
+
+
+@pytest.mark.parametrize("block_m", [16, 128])
+def test_dense_multi_lora(ml, torch, oracle, block_m):
+    """E=1, k=1: multi-LoRA on one dense SwiGLU MLP (every token, weight 1)."""
+    wl = W.custom(name="dense", T=40, H=1024, I=2048, E=1, k=1, L=4, ranks=(16, 32, 16, 32), lora_mode="uniform")
+    run_case(ml, torch, oracle, wl, block_m=block_m)
+
+
+def test_dense_decode_config(ml, torch, oracle):
+    """The dense 32B-class MLP at decode size (H=5120, I=25600), every output element."""
+    run_case(ml, torch, oracle, W.get("dense_decode"))
+
+
 # -------------------------------------------------------------- edge cases --
 
 def test_no_adapter_anywhere(ml, torch, oracle):
