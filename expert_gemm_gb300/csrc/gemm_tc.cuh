@@ -67,12 +67,32 @@ struct GemmCfg {
   static constexpr int TMEM_COLS =
       TMEM_NEED <= 32 ? 32 : TMEM_NEED <= 64 ? 64 : TMEM_NEED <= 128 ? 128 : TMEM_NEED <= 256 ? 256 : 512;
   static constexpr int SD = 4;                              // tile-id ring depth
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align slack*/ + 512 /*barriers*/;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align slack*/ + 2048 /*barriers, tile ring*/;
   static_assert(!SWAP || (BT == 16 || BT == 32 || BT == 64), "swapped tiles take 16/32/64 tokens");
   static_assert(SWAP || BT == 128 || BT == 256, "token-tiled blocks are 128 or 256 rows");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
   static_assert(W_BYTES % 1024 == 0 && T_BYTES % 1024 == 0, "stage regions keep 1024-byte alignment");
   static_assert(STAGES >= 2 && STAGES <= 8, "pipeline depth");
+};
+
+// One unit of work.  kShrink: one adapter run.  kGateUp / kDown: one (K split, token
+// block, feature tile), feature tile fastest.  Only weight-streaming (swapped) gate_up
+// splits K; its partial pre-activations then meet in fp32 and SiLU runs afterwards.
+// The producer decodes each tile once and publishes it in the shared ring, so the
+// MMA and epilogue warps never wait on the global routing metadata.
+constexpr int kMaxBlockRuns = 256;   // runs of one block <= its rows <= 256
+struct TileHdr {
+  int tau;                // tile id; >= the live count ends the CTA's loop
+  int b, e, row0, f0;
+  int run0, nruns;        // adapter runs of the block (first K split only)
+  int kb0, nk;            // base K-tiles of this split
+  int n_it;               // pipeline stages of this tile
+  int srun, sa, snch;     // kShrink: run, adapter, rank chunks
+  int ks;                 // K split of this tile
+};
+struct Tile {
+  TileHdr h;                    // copied to registers by every reader
+  uint8_t nch[kMaxBlockRuns];   // rank chunks of each adapter run of the block
 };
 
 struct GemmBars {
@@ -83,11 +103,12 @@ struct GemmBars {
   uint64_t sched_full[4];    // tile id published (producer)
   uint64_t sched_empty[4];   // tile id read (MMA thread + one arrive per epilogue warp)
   uint64_t drain;            // all MMAs of this CTA finished (teardown)
-  int32_t sched[4];
   uint32_t tmem_base;
   int32_t abort;
+  Tile tiles[4];             // the tile ring (published with sched_full)
 };
-static_assert(sizeof(GemmBars) <= 512, "barrier block");
+constexpr int kBarBytes = 2048;
+static_assert(sizeof(GemmBars) <= kBarBytes, "barrier block");
 
 __device__ __forceinline__ void record_timeout(GemmBars* bars, int32_t* status) {
   atomicOr(status, MOE_LORA_DEV_TIMEOUT);
@@ -103,18 +124,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
 }
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
 
-// One unit of work.  kShrink: one adapter run.  kGateUp / kDown: one (K split, token
-// block, feature tile), feature tile fastest.  Only weight-streaming (swapped) gate_up
-// splits K; its partial pre-activations then meet in fp32 and SiLU runs afterwards.
-struct Tile {
-  int b, e, row0, f0;
-  int run0, nruns;        // adapter runs of the block (first K split only)
-  int kb0, nk;            // base K-tiles of this split
-  int n_it;               // pipeline stages of this tile
-  int srun, sa, snch;     // kShrink: run, adapter, rank chunks
-  int ks;                 // K split of this tile
-};
-
 template <int MODE>
 __device__ __forceinline__ int live_tiles(const GemmParams& prm) {
   if constexpr (MODE == kShrink) return prm.totals[2] * prm.ksplit;
@@ -122,9 +131,10 @@ __device__ __forceinline__ int live_tiles(const GemmParams& prm) {
 }
 
 template <int MODE, bool SWAP, int BT>
-__device__ __forceinline__ Tile decode_tile(int tau, const GemmParams& prm) {
+__device__ __forceinline__ TileHdr decode_tile(int tau, const GemmParams& prm, uint8_t* nch_out) {
   using C = GemmCfg<MODE, SWAP, BT>;
-  Tile t;
+  TileHdr t;
+  t.tau = tau;
   const int nk_all = prm.K / C::BK;
   t.run0 = 0;
   t.nruns = 0;
@@ -157,6 +167,7 @@ __device__ __forceinline__ Tile decode_tile(int tau, const GemmParams& prm) {
     t.n_it = t.nk;
     for (int r = 0; r < t.nruns; ++r) {
       const int nch = (prm.ranks[prm.runs[4 * (t.run0 + r) + 1]] + kRankChunk - 1) / kRankChunk;
+      nch_out[r] = static_cast<uint8_t>(nch);
       t.n_it += (nch + C::CPS - 1) / C::CPS;
     }
   }
@@ -165,14 +176,14 @@ __device__ __forceinline__ Tile decode_tile(int tau, const GemmParams& prm) {
   return t;
 }
 
-// Tile id of ring slot i; -1 if the wait gave up.
-__device__ __forceinline__ int sched_read(GemmBars* bars, int i, int32_t* status) {
+// Tile of ring slot i (stays valid until the slot is released); null if the wait gave up.
+__device__ __forceinline__ const Tile* sched_read(GemmBars* bars, int i, int32_t* status) {
   const int slot = i & 3;
   if (!mbar_wait(&bars->sched_full[slot], (i >> 2) & 1)) {
     record_timeout(bars, status);
-    return -1;
+    return nullptr;
   }
-  return *reinterpret_cast<volatile int32_t*>(&bars->sched[slot]);
+  return &bars->tiles[slot];
 }
 
 template <int MODE, bool SWAP, int BT>
@@ -246,11 +257,12 @@ __global__ void __launch_bounds__(192, 1)
           record_timeout(bars, prm.status);
           break;
         }
-        bars->sched[slot] = tau < n_live ? tau : n_live;
-        mbar_arrive(&bars->sched_full[slot]);
+        TileHdr t;
+        t.tau = n_live;
+        if (tau < n_live) t = decode_tile<MODE, SWAP, BT>(tau, prm, bars->tiles[slot].nch);
+        bars->tiles[slot].h = t;
+        mbar_arrive(&bars->sched_full[slot]);   // release: the tile fields are visible to the readers
         if (tau >= n_live) break;
-
-        const Tile t = decode_tile<MODE, SWAP, BT>(tau, prm);
         int lr = 0, lc = 0;   // LoRA run and first rank chunk of the next LoRA stage
         bool ok = true;
         for (int it = 0; it < t.n_it; ++it, ++gs) {
@@ -328,10 +340,13 @@ __global__ void __launch_bounds__(192, 1)
     if (lane == 0) {
       int gs = 0;
       for (int i = 0;; ++i) {
-        const int tau = sched_read(bars, i, prm.status);
-        if (tau >= 0) mbar_arrive(&bars->sched_empty[i & 3]);
-        if (tau < 0 || tau >= n_live || aborted(bars)) break;
-        const Tile t = decode_tile<MODE, SWAP, BT>(tau, prm);
+        const Tile* tp = sched_read(bars, i, prm.status);
+        if (!tp) break;
+        const TileHdr t = tp->h;   // registers; the slot (run chunk counts) is released after the tile
+        if (t.tau >= n_live || aborted(bars)) {
+          mbar_arrive(&bars->sched_empty[i & 3]);
+          break;
+        }
         const int ab = i % C::NBUF;
         if (!mbar_wait(&bars->acc_empty[ab], ((i / C::NBUF) & 1) ^ 1)) {
           record_timeout(bars, prm.status);
@@ -379,8 +394,7 @@ __global__ void __launch_bounds__(192, 1)
               acc = 1;
             }
           } else if constexpr (C::kLora) {
-            const int run = t.run0 + lr;
-            const int nch = (prm.ranks[prm.runs[4 * run + 1]] + kRankChunk - 1) / kRankChunk;
+            const int nch = tp->nch[lr];
             const int nc = nch - lc < C::CPS ? nch - lc : C::CPS;
             lc += nc;
             if (lc >= nch) {
@@ -408,6 +422,7 @@ __global__ void __launch_bounds__(192, 1)
           tc_commit(&bars->empty[s]);
         }
         tc_commit(&bars->acc_full[ab]);   // also after an abort, so the epilogue is released
+        mbar_arrive(&bars->sched_empty[i & 3]);
         if (!ok) break;
       }
       tc_commit(&bars->drain);   // arrives once every MMA issued above has completed
@@ -417,11 +432,14 @@ __global__ void __launch_bounds__(192, 1)
     const int q = warp & 3;          // TMEM lane quarter this warp may access
     const int m = q * 32 + lane;     // accumulator row (TMEM lane) of this thread
     for (int i = 0;; ++i) {
-      const int tau = sched_read(bars, i, prm.status);
-      __syncwarp();
-      if (lane == 0 && tau >= 0) mbar_arrive(&bars->sched_empty[i & 3]);
-      if (tau < 0 || tau >= n_live) break;
-      const Tile t = decode_tile<MODE, SWAP, BT>(tau, prm);
+      const Tile* tp = sched_read(bars, i, prm.status);
+      if (!tp) break;
+      const TileHdr t = tp->h;   // registers; the slot is released after this tile's epilogue
+      if (t.tau >= n_live) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->sched_empty[i & 3]);
+        break;
+      }
       const int ab = i % C::NBUF;
       const bool got = mbar_wait(&bars->acc_full[ab], (i / C::NBUF) & 1);
       if (!got) record_timeout(bars, prm.status);
@@ -601,10 +619,13 @@ __global__ void __launch_bounds__(192, 1)
           }
         }
       }
-      // release the accumulator buffer to the MMA warp
+      // release the accumulator buffer to the MMA warp and the tile slot to the producer
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->acc_empty[ab]);
+      if (lane == 0) {
+        mbar_arrive(&bars->acc_empty[ab]);
+        mbar_arrive(&bars->sched_empty[i & 3]);
+      }
       if (!ok) break;
     }
   }
