@@ -18,6 +18,7 @@
 //               of the bucket in the sorted chunk, so equal keys keep pair order.
 // Integer work only; the result is bit-identical to the sequential definition.
 #include "common.cuh"
+#include "route.cuh"
 
 namespace moe {
 namespace {
@@ -34,8 +35,9 @@ __device__ __forceinline__ int lower_bound_u32(const uint32_t* a, int lo, int hi
 }
 
 // Phase 1 for one chunk: keys of its pairs sorted in keys[] (shared), per-bucket
-// counts of the chunk and its invalid-pair count written to global scratch.
-__device__ void chunk_phase(const AlignLaunch& a, uint32_t* keys, int chunk, bool store_keys) {
+// counts of the chunk and its invalid-pair count written to global scratch.  ids: the
+// expert ids [P] (global, or shared when the same CTA has just routed them).
+__device__ void chunk_phase(const AlignLaunch& a, const int32_t* ids, uint32_t* keys, int chunk, bool store_keys) {
   __shared__ int32_t s_invalid;
   const int CH = 1 << a.ch_log2;
   const int64_t p0 = static_cast<int64_t>(chunk) << a.ch_log2;
@@ -49,7 +51,7 @@ __device__ void chunk_phase(const AlignLaunch& a, uint32_t* keys, int chunk, boo
     const int64_t p = p0 + i;
     uint32_t key = kInvalidKey;
     if (p < a.P) {
-      const int e = a.topk_ids[p];
+      const int e = ids[p];
       const int ad = a.lora_ids[p / a.k];
       if (e >= 0 && e < a.E && ad >= -1 && ad < a.L)
         key = (static_cast<uint32_t>(e * LB + ad + 1) << a.ch_log2) | static_cast<uint32_t>(i);
@@ -92,7 +94,7 @@ __device__ void chunk_phase(const AlignLaunch& a, uint32_t* keys, int chunk, boo
 
 __global__ void __launch_bounds__(1024) align_chunk_kernel(AlignLaunch a) {
   extern __shared__ uint32_t keys[];
-  chunk_phase(a, keys, blockIdx.x, true);
+  chunk_phase(a, a.topk_ids, keys, blockIdx.x, true);
 }
 
 // Block-wide exclusive scan over n values produced by getv(i); put(i, prefix) receives
@@ -262,7 +264,28 @@ __global__ void __launch_bounds__(1024) align_scatter_kernel(AlignLaunch a) {
 // in shared memory and two launches disappear from the decode path.
 __global__ void __launch_bounds__(1024) align_small_kernel(AlignLaunch a) {
   extern __shared__ uint32_t keys[];
-  chunk_phase(a, keys, 0, false);
+  chunk_phase(a, a.topk_ids, keys, 0, false);
+  __syncthreads();
+  scan_phase(a);
+  __syncthreads();
+  scatter_phase(a, keys, 0);
+}
+
+// Route and align in one CTA (one chunk): each warp routes tokens into shared memory,
+// the expert ids are copied out to topk_ids, and the align phases read them from
+// shared memory.  One launch for the whole routing front of a decode step.
+__global__ void __launch_bounds__(1024) route_align_small_kernel(AlignLaunch a, const float* __restrict__ logits,
+                                                                 float* __restrict__ topk_w,
+                                                                 int32_t* __restrict__ topk_ids) {
+  extern __shared__ uint32_t keys[];
+  int32_t* s_ids = reinterpret_cast<int32_t*>(keys + (1 << a.ch_log2));
+  const int T = static_cast<int>(a.P / a.k);
+  const int lane = threadIdx.x & 31;
+  for (int t = threadIdx.x >> 5; t < T; t += blockDim.x >> 5)
+    route_token(logits + static_cast<int64_t>(t) * a.E, a.E, a.k, lane, s_ids + t * a.k, topk_w + t * a.k);
+  __syncthreads();
+  for (int p = threadIdx.x; p < a.P; p += blockDim.x) topk_ids[p] = s_ids[p];
+  chunk_phase(a, s_ids, keys, 0, false);
   __syncthreads();
   scan_phase(a);
   __syncthreads();
@@ -292,6 +315,13 @@ cudaError_t launch_align(const AlignLaunch& a, cudaStream_t s) {
     err = cudaGetLastError();
   }
   return err;
+}
+
+cudaError_t launch_route_align_small(const AlignLaunch& a, const float* logits, float* topk_w, int32_t* topk_ids,
+                                     cudaStream_t s) {
+  const size_t smem = (static_cast<size_t>(1) << a.ch_log2) * sizeof(uint32_t) + static_cast<size_t>(a.P) * 4;
+  route_align_small_kernel<<<1, 1024, smem, s>>>(a, logits, topk_w, topk_ids);
+  return cudaGetLastError();
 }
 
 }  // namespace moe

@@ -13,7 +13,7 @@ namespace moe {
 enum GemmMode : int {
   kShrink = 0,   // S_run = X_block * A[a,e]^T       (gate_up_shrink / down_shrink)
   kGateUp = 1,   // h = silu(gate) * up, gate/up = X W_gu[e]^T + S_run Bt_gu[a,e]^T (gate_up + expand)
-  kDown = 2,     // out_acc[t] += w * (h W_dn[e]^T + S_run Bt_dn[a,e]^T)            (down + expand)
+  kDown = 2,     // y[row] = h W_dn[e]^T + S_run Bt_dn[a,e]^T                      (down + expand)
 };
 
 constexpr int kKTile = 64;      // K elements per pipeline stage (one 128-byte swizzle row of bf16)
@@ -37,10 +37,11 @@ struct GemmParams {
   const int32_t* runs;          // [runs][4] {block, adapter, begin, end}
   const int32_t* totals;        // {rows, blocks, runs, dropped}
   const int32_t* sorted_p;      // [rows]
-  const float* topk_w;          // [T*k]
   uint16_t* h_out;              // kGateUp: h rows in sorted order [rows][I] (bf16)
-  float* out_acc;               // kDown:   [T][H] fp32 accumulation
-  float* g_acc;                 // kGateUp with K splits: [rows][2I] fp32 pre-activations
+  void* y_out;                  // kDown: expert outputs of the real rows in sorted order,
+                                //   [rows][H] bf16 (ksplit 1) or [ksplit][part_rows][H] fp32 partials
+  float* g_part;                // kGateUp with K splits: [ksplit][part_rows][2I] fp32 partial pre-activations
+  int64_t part_rows;            // row stride between the K splits' partial buffers
   float* s_part;                // kShrink with K splits: [ksplit][max_runs][BT][r_pad] fp32 partials
   int32_t* s_cnt;               // kShrink with K splits: [max_runs] splits finished per run (zero at launch)
   int32_t max_runs;
@@ -54,7 +55,7 @@ struct GemmParams {
   int32_t r_pad;                // S row length (r_max rounded up to 16)
   int32_t* tile_ctr;            // tile counter of this launch (zero at launch; persistent CTAs take tiles)
   int32_t n_ft;                 // feature tiles per token block (kGateUp, kDown)
-  int32_t ksplit;               // kDown: K splits; partial sums meet in out_acc
+  int32_t ksplit;               // K splits; each split stores its own partial sums
   int32_t lora_after_pdl;       // previous kernel is the shrink: wait for it only before the LoRA K-steps
   int32_t ranks[MOE_LORA_MAX_ADAPTERS];
 };
@@ -88,19 +89,31 @@ struct AlignLaunch {
   moe_lora_align_buf out;
 };
 cudaError_t launch_align(const AlignLaunch& a, cudaStream_t s);
+// Route + align in one single-CTA launch; only for a.nchunks == 1 (T*k <= 4096).
+// a.topk_ids is ignored: the routed ids are written to topk_ids.
+cudaError_t launch_route_align_small(const AlignLaunch& a, const float* logits, float* topk_w, int32_t* topk_ids,
+                                     cudaStream_t s);
 
-// Gathers x rows into sorted order and zeroes out_acc [n_acc floats], *status, the
-// n_ctr tile counters of the forward's GEMM launches and, when g_acc is given, the
-// g_cols fp32 pre-activations of every live sorted row.
+// Gathers x rows into sorted order, records the sorted row of every placed pair in
+// pair_row [T*k], and zeroes *status and the n_ctr tile counters of the forward's
+// GEMM launches.
 cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* sorted_p, const int32_t* totals, int64_t max_rows,
-                               int H, int k, int P, uint16_t* x_sorted, float* out_acc, int64_t n_acc,
-                               int32_t* status, int32_t* ctr, int n_ctr, float* g_acc, int g_cols, cudaStream_t s);
-cudaError_t launch_finalize(const float* acc, uint16_t* out, int64_t n, bool pdl, cudaStream_t s);
-// h = bf16(silu(g[:, :I]) * g[:, I:]) for the live sorted rows, after a K-split gate_up.
-cudaError_t launch_silu_rows(const float* g_acc, const int32_t* totals, int64_t max_rows, int I, uint16_t* h,
-                             bool pdl, cudaStream_t s);
+                               int H, int k, int P, uint16_t* x_sorted, int32_t* pair_row, int32_t* status,
+                               int32_t* ctr, int n_ctr, cudaStream_t s);
+// out[t] = bf16(sum_j topk_w[t,j] * y(row of pair t*k+j)) in a fixed order; y is bf16
+// [rows][H] when ksplit == 1, else fp32 partials [ksplit][part_rows][H] summed in order.
+cudaError_t launch_combine(const void* y, int ksplit, int64_t part_rows, const int32_t* pair_row,
+                           const int32_t* sorted_p, const int32_t* totals, const float* topk_w, int64_t T, int k,
+                           int H, uint16_t* out, bool pdl, cudaStream_t s);
+// h = bf16(silu(g[:, :I]) * g[:, I:]) for the live sorted rows after a K-split gate_up,
+// g being the sum of the ksplit partial buffers [ksplit][part_rows][2I] in split order.
+cudaError_t launch_silu_rows(const float* g_part, int ksplit, int64_t part_rows, const int32_t* totals,
+                             int64_t max_rows, int I, uint16_t* h, bool pdl, cudaStream_t s);
 // pdl: launch with programmatic stream serialisation (may overlap the previous kernel).
 cudaError_t launch_gemm(int mode, int bt, const GemmMaps& maps, const GemmParams& prm, int64_t max_blocks,
                         int64_t max_runs, bool pdl, cudaStream_t s);
+// K elements per pipeline stage and stage count of the compiled GEMM for (mode, bt);
+// false if no kernel is compiled for it.  Host only, no device calls.
+bool gemm_stage_shape(int mode, int bt, int* k_tile, int* stages);
 
 }  // namespace moe

@@ -23,4 +23,23 @@ cudaError_t launch_gemm(int mode, int bt, const GemmMaps& maps, const GemmParams
   return cudaErrorInvalidValue;
 }
 
+bool gemm_stage_shape(int mode, int bt, int* k_tile, int* stages) {
+#define MOE_SHAPE_CASE(BT_, SWAP_)                                                       \
+  if (bt == BT_) {                                                                       \
+    switch (mode) {                                                                      \
+      case kShrink: *k_tile = GemmCfg<kShrink, SWAP_, BT_>::BK; *stages = GemmCfg<kShrink, SWAP_, BT_>::STAGES; return true; \
+      case kGateUp: *k_tile = GemmCfg<kGateUp, SWAP_, BT_>::BK; *stages = GemmCfg<kGateUp, SWAP_, BT_>::STAGES; return true; \
+      case kDown: *k_tile = GemmCfg<kDown, SWAP_, BT_>::BK; *stages = GemmCfg<kDown, SWAP_, BT_>::STAGES; return true;       \
+      default: return false;                                                             \
+    }                                                                                    \
+  }
+  MOE_SHAPE_CASE(16, true)
+  MOE_SHAPE_CASE(32, true)
+  MOE_SHAPE_CASE(64, true)
+  MOE_SHAPE_CASE(128, false)
+  MOE_SHAPE_CASE(256, false)
+#undef MOE_SHAPE_CASE
+  return false;
+}
+
 }  // namespace moe

@@ -3,13 +3,15 @@
 //
 //   kShrink : S_run = X_block * A[a,e]^T           LoRA shrink of gate_up or down
 //   kGateUp : g = X W_gu[e]^T (+ S_run Bt_gu[a,e]^T per adapter run), h = silu(g_gate) * g_up
-//   kDown   : d = H W_dn[e]^T (+ S_run Bt_dn[a,e]^T per adapter run), out[t] += w * d
+//   kDown   : d = H W_dn[e]^T (+ S_run Bt_dn[a,e]^T per adapter run), stored per sorted row
 //
 // The LoRA expand is not a separate kernel: every adapter run of a token block adds
 // ceil(rank/16) extra K-steps (packed BK/16 per pipeline stage) to the same TMEM
 // accumulator, with the run's S tile (rows outside the run are zero) as the
-// token-side operand and Bt[a,e] as the weight-side operand.  SiLU gating and the
-// weighted top-k combine happen in the epilogue that drains TMEM.  This is the pages'
+// token-side operand and Bt[a,e] as the weight-side operand.  SiLU gating happens in
+// the epilogue that drains TMEM; the down epilogue stores each real row's output with
+// plain stores and a separate pass combines a token's k rows in a fixed order (no
+// atomics anywhere, so repeated calls give identical bytes).  This is the pages'
 // fusion of the LoRA add into the expand kernel (AWS ML Blog "Efficiently serve
 // dozens of fine-tuned models with vLLM on Amazon SageMaker AI and Amazon Bedrock",
 // section "Kernel optimizations") taken one step further: base GEMM, expand and
@@ -562,12 +564,13 @@ __global__ void __launch_bounds__(192, 1)
               tmem_ld_wait();
               if (f < I) {
                 if (prm.ksplit > 1) {
-                  // K split: partial gate/up pre-activations meet in fp32; SiLU follows later
+                  // K split: this split's fp32 pre-activations go to its own buffer; the
+                  // SiLU pass adds the splits in order
+                  float* gs = prm.g_part + (static_cast<size_t>(t.ks) * prm.part_rows + row0 + n0) * (2 * I);
 #pragma unroll
                   for (int j = 0; j < 16; ++j) {
-                    float* g = prm.g_acc + static_cast<size_t>(row0 + n0 + j) * (2 * I);
-                    atomicAdd(g + f, __uint_as_float(v[j]));
-                    atomicAdd(g + I + f, __uint_as_float(u[j]));
+                    gs[static_cast<size_t>(j) * (2 * I) + f] = __uint_as_float(v[j]);
+                    gs[static_cast<size_t>(j) * (2 * I) + I + f] = __uint_as_float(u[j]);
                   }
                 } else {
 #pragma unroll
@@ -579,24 +582,32 @@ __global__ void __launch_bounds__(192, 1)
               }
             }
           }
-        } else {  // kDown
+        } else {  // kDown: each real row's output to its own row of y (no combine here)
           const int H = prm.n_feat;
+          uint16_t* y16 = static_cast<uint16_t*>(prm.y_out);
+          float* y32 = static_cast<float*>(prm.y_out) + static_cast<size_t>(t.ks) * prm.part_rows * H;
           if constexpr (!SWAP) {
             for (int mt = 0; mt < C::MT; ++mt) {
-              const int p = prm.sorted_p[row0 + mt * 128 + m];
-              const bool valid = p < prm.P;
-              const float w = valid ? prm.topk_w[p] : 0.f;
-              float* orow = prm.out_acc + static_cast<size_t>(valid ? p / prm.k : 0) * H + f0;
+              const int row = row0 + mt * 128 + m;
+              const bool valid = prm.sorted_p[row] < prm.P;
               for (int c = 0; c < 256; c += 16) {
                 if (f0 + c >= H) break;
                 tmem_ld16(tq + mt * C::NACC + c, v);
                 tmem_ld_wait();
-                if (valid) {
+                if (!valid) continue;
+                if (prm.ksplit == 1) {
+                  uint32_t pk[8];
+#pragma unroll
+                  for (int j = 0; j < 8; ++j) pk[j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+                  uint4* dst = reinterpret_cast<uint4*>(y16 + static_cast<size_t>(row) * H + f0 + c);
+                  dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                  dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                } else {
+                  float4* dst = reinterpret_cast<float4*>(y32 + static_cast<size_t>(row) * H + f0 + c);
 #pragma unroll
                   for (int j = 0; j < 4; ++j)
-                    atomicAdd(reinterpret_cast<float4*>(orow + c + 4 * j),
-                              make_float4(w * __uint_as_float(v[4 * j]), w * __uint_as_float(v[4 * j + 1]),
-                                          w * __uint_as_float(v[4 * j + 2]), w * __uint_as_float(v[4 * j + 3])));
+                    dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                         __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
                 }
               }
             }
@@ -607,12 +618,17 @@ __global__ void __launch_bounds__(192, 1)
               for (int n0 = 0; n0 < BT; n0 += 16) {
                 tmem_ld16(tq + h * BT + n0, v);
                 tmem_ld_wait();
+                if (f >= H) continue;
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
-                  const int p = prm.sorted_p[row0 + n0 + j];
-                  if (p < prm.P && f < H)
-                    atomicAdd(prm.out_acc + static_cast<size_t>(p / prm.k) * H + f,
-                              prm.topk_w[p] * __uint_as_float(v[j]));
+                  const int row = row0 + n0 + j;
+                  if (prm.sorted_p[row] >= prm.P) continue;
+                  if (prm.ksplit == 1) {
+                    __nv_bfloat16 hv = __float2bfloat16_rn(__uint_as_float(v[j]));
+                    y16[static_cast<size_t>(row) * H + f] = *reinterpret_cast<uint16_t*>(&hv);
+                  } else {
+                    y32[static_cast<size_t>(row) * H + f] = __uint_as_float(v[j]);
+                  }
                 }
               }
             }

@@ -6,8 +6,8 @@
 //   shrink    S_gu per adapter run = x_block A_gu[a,e]^T          (tcgen05)
 //   gate_up   h = silu(gate) * up, gate/up = x W_gu[e]^T + S_gu Bt_gu[a,e]^T (tcgen05)
 //   shrink    S_dn per adapter run = h_block A_dn[a,e]^T          (tcgen05)
-//   down      out_acc[t] += w * (h W_dn[e]^T + S_dn Bt_dn[a,e]^T)  (tcgen05)
-//   finalize  out = bf16(out_acc)
+//   down      y[row] = h W_dn[e]^T + S_dn Bt_dn[a,e]^T              (tcgen05)
+//   combine   out[t] = bf16(sum_j w[t,j] y[row of (t,j)]), fixed order
 #include <cudaTypedefs.h>
 
 #include <cstdarg>
@@ -94,6 +94,67 @@ int validate_dims(const moe_lora_dims* d) {
   return MOE_LORA_OK;
 }
 
+// ---- compiled-in tile table
+// The pages tune the fused MoE-LoRA kernels per shape, with tables of tile sizes
+// picked by problem size (AWS ML Blog "Efficiently serve dozens of fine-tuned models
+// with vLLM on Amazon SageMaker AI and Amazon Bedrock", section "Tuning kernel
+// configurations for Amazon SageMaker AI and Amazon Bedrock"; agentlenshq.com "vLLM
+// MoE 모델을 위한 Multi-LoRA 서빙", section "Amazon 전용 튜닝").  Here the table is
+// compiled in.  A shape's class is its pairs per expert T*k/E -- how many token rows
+// each streamed weight tile serves -- and the class fixes the token tile (= align
+// block) and, for the weight-streaming kernels, the targets of the K-split rules,
+// which then weigh the tile counts against H, I and the SM count.  Rows were set from
+// GB300 sweeps over the workloads' shapes (256-row blocks are accepted but were
+// slower than 128 with double-buffered TMEM, so no class picks them).
+struct TileClass {
+  double ppe_above;       // the class holds shapes whose T*k/E exceeds this
+  int block_m;            // token tile: < 128 weight-streaming, >= 128 token-tiled
+  int gu_tiles_per_cta;   // weight-streaming gate_up: split K until about this many tiles per CTA
+  int dn_tiles_per_cta;   // weight-streaming down: the same
+  int shrink_min_ktiles;  // weight-streaming shrink: split K only from this many 64-wide K-tiles
+  int shrink_max_splits;
+};
+constexpr TileClass kTileTable[] = {
+    {-1.0, 16, 2, 6, 64, 8},    // up to 10 pairs per expert (decode batches)
+    {10.0, 32, 2, 6, 64, 8},    // 10 .. 24
+    {24.0, 64, 2, 6, 64, 8},    // 24 .. 95
+    {95.0, 128, 1, 1, 0, 1},    // more than 95: token-tiled, compute-bound, no K split
+};
+constexpr int kTableRows = sizeof(kTileTable) / sizeof(kTileTable[0]);
+
+// Row of the shape class of (T, k, E).
+int class_row(int64_t T, int32_t k, int32_t E) {
+  if (E <= 0 || k <= 0 || T <= 0) return 0;
+  const double ppe = (double)T * k / E;
+  int row = 0;
+  for (int i = 0; i < kTableRows; ++i)
+    if (ppe > kTileTable[i].ppe_above) row = i;
+  return row;
+}
+
+// Row whose constants a launch with this token tile uses (256 takes the 128 row).
+int block_row(int block_m) {
+  int row = 0;
+  for (int i = 0; i < kTableRows; ++i)
+    if (kTileTable[i].block_m <= block_m) row = i;
+  return row;
+}
+
+// block_m == 0 asks for the table's choice; every entry point works on a resolved copy.
+int resolve(const moe_lora_dims* in, moe_lora_dims* out) {
+  if (!in) return fail(MOE_LORA_EINVAL, "dims is NULL");
+  *out = *in;
+  if (out->block_m == 0) out->block_m = kTileTable[class_row(out->T, out->k, out->E)].block_m;
+  return MOE_LORA_OK;
+}
+#define MOE_RESOLVE(d)                           \
+  moe_lora_dims d##_resolved;                    \
+  do {                                           \
+    int st_ = resolve(d, &d##_resolved);         \
+    if (st_ != MOE_LORA_OK) return st_;          \
+  } while (0);                                   \
+  d = &d##_resolved
+
 struct Caps {
   int64_t rows, blocks, runs;
 };
@@ -137,25 +198,31 @@ AlignLayout align_layout(const moe_lora_dims* d) {
 
 // ---- forward scratch layout
 struct FwdLayout {
-  size_t xs, hs, sgu, sdn, acc, ctr, gacc, pgu, pdn, bytes;
-  int n_ctr;
+  size_t xs, hs, sgu, sdn, y, prow, ctr, gpart, pgu, pdn, bytes;
+  int n_ctr, ks_gu, ks_dn;
 };
 constexpr int kNumGemmCounters = 4;   // tile counters: shrink_gu, gate_up, shrink_dn, down
 constexpr int kPlanSMs = 152;         // SM count the K-split heuristics plan for (GB300)
 int shrink_ksplit(const moe_lora_dims* d, const Caps& cap, int K);
+int gate_up_ksplit(const moe_lora_dims* d, const Caps& cap);
+int down_ksplit(const moe_lora_dims* d, const Caps& cap);
 FwdLayout fwd_layout(const moe_lora_dims* d) {
   const Caps c = capacity(d);
   FwdLayout l{};
+  l.ks_gu = gate_up_ksplit(d, c);
+  l.ks_dn = down_ksplit(d, c);
   size_t off = 0;
   const size_t s_tile = (size_t)d->block_m * r_pad_of(d) * 2;
   l.xs = off;  off += up256((size_t)c.rows * d->H * 2);
   l.hs = off;  off += up256((size_t)c.rows * d->I * 2);
   l.sgu = off; off += up256((size_t)c.runs * s_tile);
   l.sdn = off; off += up256((size_t)c.runs * s_tile);
-  l.acc = off; off += up256((size_t)d->T * d->H * 4);
+  // down outputs per sorted row: bf16, or fp32 partials per K split
+  l.y = off;   off += up256(l.ks_dn > 1 ? (size_t)l.ks_dn * c.rows * d->H * 4 : (size_t)c.rows * d->H * 2);
+  l.prow = off; off += up256((size_t)d->T * d->k * 4);
   l.ctr = off; off += up256((size_t)(kNumGemmCounters + 2 * 4 * c.runs) * 4);
-  // fp32 gate/up pre-activations for a K-split (weight-streaming) gate_up
-  l.gacc = off; off += d->block_m < 128 ? up256((size_t)c.rows * 2 * d->I * 4) : 0;
+  // fp32 partial gate/up pre-activations of a K-split (weight-streaming) gate_up
+  l.gpart = off; off += l.ks_gu > 1 ? up256((size_t)l.ks_gu * c.rows * 2 * d->I * 4) : 0;
   // fp32 partial S of K-split shrinks, and their per-(run, warp) arrival counters
   const size_t s_part = (size_t)c.runs * d->block_m * r_pad_of(d) * 4;
   l.pgu = off; off += up256((size_t)shrink_ksplit(d, c, d->H) * s_part);
@@ -207,23 +274,12 @@ int check_align_buf(const moe_lora_align_buf* b) {
   return MOE_LORA_OK;
 }
 
-int sm_count() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0, v = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess && cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
-      n = v;
-    if (n <= 0) n = 148;
-  }
-  return n;
-}
-
 // K splits of a weight-streaming GEMM (n_ft feature tiles per block, reduction K):
 // enough tiles for about `per_cta` per persistent CTA, so the CTAs finish together;
 // each split keeps at least 8 K-tiles, at most 4 splits.  Token-tiled (compute-bound)
 // shapes keep one.
 int weight_stream_ksplit(const moe_lora_dims* d, const Caps& cap, int n_ft, int K, int per_cta) {
-  if (d->block_m >= 128) return 1;
+  if (d->block_m >= 128 || per_cta <= 1) return 1;
   const int64_t P = d->T * d->k;
   int64_t est_blocks = cap.blocks;
   if (est_blocks > d->E) est_blocks = d->E;
@@ -236,22 +292,25 @@ int weight_stream_ksplit(const moe_lora_dims* d, const Caps& cap, int n_ft, int 
   return ks < 1 ? 1 : (int)ks;
 }
 int down_ksplit(const moe_lora_dims* d, const Caps& cap) {
-  return weight_stream_ksplit(d, cap, (d->H + 255) / 256, d->I, 6);
+  return weight_stream_ksplit(d, cap, (d->H + 255) / 256, d->I, kTileTable[block_row(d->block_m)].dn_tiles_per_cta);
 }
 // gate_up splits only when its tiles are too few to spread over the SMs: a split adds
 // an fp32 round trip of the pre-activations and a SiLU pass.
 int gate_up_ksplit(const moe_lora_dims* d, const Caps& cap) {
-  return weight_stream_ksplit(d, cap, (d->I + 127) / 128, d->H, 2);
+  return weight_stream_ksplit(d, cap, (d->I + 127) / 128, d->H, kTileTable[block_row(d->block_m)].gu_tiles_per_cta);
 }
-// The weight-streaming shrink splits K only for long reductions (>= 64 K-tiles) whose
-// runs cannot fill the SMs -- a run's tile otherwise walks all of K alone.  Measured:
-// splitting short reductions only adds per-tile overhead and keeps the SMs from the
-// next kernel.  About one tile per SM, each split at least 16 K-tiles, at most 8.
+// The weight-streaming shrink splits K only for long reductions whose runs cannot fill
+// the SMs -- a run's tile otherwise walks all of K alone.  Measured: splitting short
+// reductions only adds per-tile overhead and keeps the SMs from the next kernel.
+// About one tile per SM, each split at least 16 K-tiles.
 int shrink_ksplit(const moe_lora_dims* d, const Caps& cap, int K) {
+  const TileClass& tc = kTileTable[block_row(d->block_m)];
   const int64_t nk = K / 64;
-  if (d->block_m >= 128 || d->L == 0 || cap.runs <= 0 || nk < 64 || cap.runs >= kPlanSMs) return 1;
+  if (d->block_m >= 128 || d->L == 0 || cap.runs <= 0 || tc.shrink_min_ktiles <= 0 || nk < tc.shrink_min_ktiles ||
+      cap.runs >= kPlanSMs)
+    return 1;
   int64_t ks = ((int64_t)kPlanSMs + cap.runs - 1) / cap.runs;
-  const int64_t ks_max = nk / 16 < 8 ? nk / 16 : 8;
+  const int64_t ks_max = nk / 16 < tc.shrink_max_splits ? nk / 16 : tc.shrink_max_splits;
   if (ks > ks_max) ks = ks_max;
   return ks < 1 ? 1 : (int)ks;
 }
@@ -269,18 +328,8 @@ int do_route(const float* logits, int64_t T, int32_t E, int32_t k, int32_t* ids,
   return MOE_LORA_OK;
 }
 
-int do_align(const moe_lora_dims* d, const int32_t* topk_ids, const int32_t* lora_ids, const moe_lora_align_buf* out,
-             void* ws, size_t ws_bytes, cudaStream_t s) {
-  MOE_TRY(validate_dims(d));
-  MOE_TRY(check_align_buf(out));
-  const AlignLayout l = align_layout(d);
-  if (d->T > 0) {
-    MOE_TRY(check_ptr(topk_ids, "topk_ids", false));
-    MOE_TRY(check_ptr(lora_ids, "lora_ids", false));
-  }
-  MOE_TRY(check_ptr(ws, "workspace", true));
-  if (ws_bytes < l.bytes) return fail(MOE_LORA_EWORKSPACE, "align workspace %zu < %zu bytes", ws_bytes, l.bytes);
-  MOE_TRY(check_device());
+moe::AlignLaunch align_launch(const moe_lora_dims* d, const AlignLayout& l, const int32_t* topk_ids,
+                              const int32_t* lora_ids, const moe_lora_align_buf* out, void* ws) {
   uint8_t* base = static_cast<uint8_t*>(ws);
   moe::AlignLaunch a{};
   a.topk_ids = topk_ids;
@@ -300,8 +349,49 @@ int do_align(const moe_lora_dims* d, const int32_t* topk_ids, const int32_t* lor
   a.run_base = reinterpret_cast<int32_t*>(base + l.rbase);
   a.expert_n = reinterpret_cast<int32_t*>(base + l.expn);
   a.out = *out;
-  cudaError_t e = moe::launch_align(a, s);
+  return a;
+}
+
+int do_align(const moe_lora_dims* d, const int32_t* topk_ids, const int32_t* lora_ids, const moe_lora_align_buf* out,
+             void* ws, size_t ws_bytes, cudaStream_t s) {
+  MOE_RESOLVE(d);
+  MOE_TRY(validate_dims(d));
+  MOE_TRY(check_align_buf(out));
+  const AlignLayout l = align_layout(d);
+  if (d->T > 0) {
+    MOE_TRY(check_ptr(topk_ids, "topk_ids", false));
+    MOE_TRY(check_ptr(lora_ids, "lora_ids", false));
+  }
+  MOE_TRY(check_ptr(ws, "workspace", true));
+  if (ws_bytes < l.bytes) return fail(MOE_LORA_EWORKSPACE, "align workspace %zu < %zu bytes", ws_bytes, l.bytes);
+  MOE_TRY(check_device());
+  cudaError_t e = moe::launch_align(align_launch(d, l, topk_ids, lora_ids, out, ws), s);
   if (e != cudaSuccess) return cuda_fail(e, "align kernel launch");
+  return MOE_LORA_OK;
+}
+
+// Route then align.  Batches of one align chunk (T*k <= 4096) take a single launch;
+// larger ones the route kernel and the align kernels.
+int do_route_align(const moe_lora_dims* d, const float* logits, const int32_t* lora_ids, int32_t* topk_ids,
+                   float* topk_w, const moe_lora_align_buf* out, void* ws, size_t ws_bytes, cudaStream_t s) {
+  MOE_RESOLVE(d);
+  MOE_TRY(validate_dims(d));
+  const AlignLayout l = align_layout(d);
+  if (l.nchunks != 1) {
+    MOE_TRY(do_route(logits, d->T, d->E, d->k, topk_ids, topk_w, s));
+    return do_align(d, topk_ids, lora_ids, out, ws, ws_bytes, s);
+  }
+  MOE_TRY(check_align_buf(out));
+  MOE_TRY(check_ptr(logits, "logits", false));
+  MOE_TRY(check_ptr(lora_ids, "lora_ids", false));
+  MOE_TRY(check_ptr(topk_ids, "topk_ids", false));
+  MOE_TRY(check_ptr(topk_w, "topk_w", false));
+  MOE_TRY(check_ptr(ws, "workspace", true));
+  if (ws_bytes < l.bytes) return fail(MOE_LORA_EWORKSPACE, "align workspace %zu < %zu bytes", ws_bytes, l.bytes);
+  MOE_TRY(check_device());
+  cudaError_t e = moe::launch_route_align_small(align_launch(d, l, topk_ids, lora_ids, out, ws), logits, topk_w,
+                                                topk_ids, s);
+  if (e != cudaSuccess) return cuda_fail(e, "route_align kernel launch");
   return MOE_LORA_OK;
 }
 
@@ -309,6 +399,7 @@ int do_forward(const moe_lora_dims* d, const uint16_t* x, const float* topk_w, c
                const uint16_t* W_gu, const uint16_t* W_dn, const uint16_t* A_gu, const uint16_t* Bt_gu,
                const uint16_t* A_dn, const uint16_t* Bt_dn, uint16_t* out, void* ws, size_t ws_bytes,
                int32_t* dev_status, cudaStream_t s, void* const* ev) {
+  MOE_RESOLVE(d);
   MOE_TRY(validate_dims(d));
   MOE_TRY(check_align_buf(al));
   MOE_TRY(check_ptr(dev_status, "dev_status", false));
@@ -340,10 +431,11 @@ int do_forward(const moe_lora_dims* d, const uint16_t* x, const float* topk_w, c
   uint16_t* hs = reinterpret_cast<uint16_t*>(base + l.hs);
   uint16_t* sgu = reinterpret_cast<uint16_t*>(base + l.sgu);
   uint16_t* sdn = reinterpret_cast<uint16_t*>(base + l.sdn);
-  float* acc = reinterpret_cast<float*>(base + l.acc);
+  void* y = base + l.y;
+  int32_t* prow = reinterpret_cast<int32_t*>(base + l.prow);
   int32_t* ctr = reinterpret_cast<int32_t*>(base + l.ctr);
-  const int ks_gu = gate_up_ksplit(d, cap);
-  float* gacc = ks_gu > 1 ? reinterpret_cast<float*>(base + l.gacc) : nullptr;
+  const int ks_gu = l.ks_gu;
+  float* gpart = ks_gu > 1 ? reinterpret_cast<float*>(base + l.gpart) : nullptr;
   const int BT = d->block_m;
   const uint64_t H = d->H, I = d->I, E = d->E, LE = (uint64_t)d->L * d->E, R = d->r_max;
   const uint64_t rows = cap.rows, RP = r_pad_of(d);
@@ -420,7 +512,7 @@ int do_forward(const moe_lora_dims* d, const uint16_t* x, const float* topk_w, c
   p.runs = al->runs;
   p.totals = al->totals;
   p.sorted_p = al->sorted_p;
-  p.topk_w = topk_w;
+  p.part_rows = cap.rows;
   p.status = dev_status;
   p.E = d->E;
   p.k = d->k;
@@ -440,8 +532,8 @@ int do_forward(const moe_lora_dims* d, const uint16_t* x, const float* topk_w, c
   // output.  Stage events, when given, sit between launches.
   const bool lora = d->L > 0;
   MOE_CUDA(mark(0));
-  MOE_CUDA(moe::launch_gather_rows(x, al->sorted_p, al->totals, cap.rows, d->H, d->k, p.P, xs, acc,
-                                   d->T * (int64_t)d->H, dev_status, ctr, l.n_ctr, gacc, 2 * d->I, s));
+  MOE_CUDA(moe::launch_gather_rows(x, al->sorted_p, al->totals, cap.rows, d->H, d->k, p.P, xs, prow, dev_status, ctr,
+                                   l.n_ctr, s));
   MOE_CUDA(mark(1 + MOE_LORA_STAGE_GATHER));
 
   if (lora) {
@@ -464,9 +556,9 @@ int do_forward(const moe_lora_dims* d, const uint16_t* x, const float* topk_w, c
     q.tile_ctr = ctr + 1;
     q.n_ft = (d->I + 127) / 128;
     q.ksplit = ks_gu;
-    q.g_acc = gacc;
+    q.g_part = gpart;
     MOE_CUDA(moe::launch_gemm(moe::kGateUp, BT, m_gu, q, cap.blocks, cap.runs, true, s));
-    if (ks_gu > 1) MOE_CUDA(moe::launch_silu_rows(gacc, al->totals, cap.rows, d->I, hs, true, s));
+    if (ks_gu > 1) MOE_CUDA(moe::launch_silu_rows(gpart, ks_gu, cap.rows, al->totals, cap.rows, d->I, hs, true, s));
   }
   MOE_CUDA(mark(1 + MOE_LORA_STAGE_GATE_UP));
   if (lora) {
@@ -484,16 +576,17 @@ int do_forward(const moe_lora_dims* d, const uint16_t* x, const float* topk_w, c
     moe::GemmParams q = p;
     q.K = d->I;
     q.n_feat = d->H;
-    q.out_acc = acc;
+    q.y_out = y;
     q.lora_after_pdl = lora;
-    q.ksplit = down_ksplit(d, cap);
+    q.ksplit = l.ks_dn;
     q.tile_ctr = ctr + 3;
     q.n_ft = (d->H + 255) / 256;
     MOE_CUDA(moe::launch_gemm(moe::kDown, BT, m_dn, q, cap.blocks, cap.runs, true, s));
   }
   MOE_CUDA(mark(1 + MOE_LORA_STAGE_DOWN));
-  MOE_CUDA(moe::launch_finalize(acc, out, d->T * d->H, true, s));
-  MOE_CUDA(mark(1 + MOE_LORA_STAGE_FINALIZE));
+  MOE_CUDA(moe::launch_combine(y, l.ks_dn, cap.rows, prow, al->sorted_p, al->totals, topk_w, d->T, d->k, d->H, out,
+                               true, s));
+  MOE_CUDA(mark(1 + MOE_LORA_STAGE_COMBINE));
   return MOE_LORA_OK;
 }
 
@@ -530,7 +623,7 @@ LayerLayout layer_layout(const moe_lora_dims* d) {
 
 extern "C" {
 
-int moe_lora_version(void) { return 100; }
+int moe_lora_version(void) { return 200; }
 
 const char* moe_lora_status_string(int status) {
   switch (status) {
@@ -548,15 +641,37 @@ const char* moe_lora_status_string(int status) {
 const char* moe_lora_last_error(void) { return g_err; }
 
 int32_t moe_lora_pick_block_m(int64_t T, int32_t k, int32_t E) {
-  if (E <= 0 || k <= 0 || T <= 0) return 16;
-  const double per_expert = (double)T * k / E;
-  if (per_expert >= 96.0) return 128;   // 256 is accepted but measured slower with double-buffered TMEM
-  if (per_expert > 24.0) return 64;
-  if (per_expert > 10.0) return 32;
-  return 16;
+  return kTileTable[class_row(T, k, E)].block_m;
+}
+
+int moe_lora_plan_query(const moe_lora_dims* d, moe_lora_plan* out) {
+  MOE_RESOLVE(d);
+  MOE_TRY(validate_dims(d));
+  if (!out) return fail(MOE_LORA_EINVAL, "plan is NULL");
+  const Caps cap = capacity(d);
+  const FwdLayout l = fwd_layout(d);
+  moe_lora_plan p{};
+  p.block_m = d->block_m;
+  p.table_row = block_row(d->block_m);
+  p.weight_streaming = d->block_m < 128;
+  const bool lora = d->L > 0;
+  p.ksplit[0] = lora ? shrink_ksplit(d, cap, d->H) : 0;
+  p.ksplit[1] = l.ks_gu;
+  p.ksplit[2] = lora ? shrink_ksplit(d, cap, d->I) : 0;
+  p.ksplit[3] = l.ks_dn;
+  const int modes[4] = {moe::kShrink, moe::kGateUp, moe::kShrink, moe::kDown};
+  for (int g = 0; g < 4; ++g)
+    if (!moe::gemm_stage_shape(modes[g], d->block_m, &p.k_tile[g], &p.stages[g]))
+      return fail(MOE_LORA_EUNSUPPORTED, "no GEMM compiled for block_m = %d", d->block_m);
+  const int64_t P = d->T * d->k;
+  p.launches_route_align = (P > 0 && P <= 4096) ? 1 : (P == 0 ? 1 : 4);
+  p.launches_forward = d->T == 0 ? 0 : 4 + (lora ? 2 : 0) + (l.ks_gu > 1 ? 1 : 0);
+  *out = p;
+  return MOE_LORA_OK;
 }
 
 int moe_lora_align_capacity(const moe_lora_dims* d, int64_t* max_rows, int64_t* max_blocks, int64_t* max_runs) {
+  MOE_RESOLVE(d);
   MOE_TRY(validate_dims(d));
   const Caps c = capacity(d);
   if (max_rows) *max_rows = c.rows;
@@ -566,6 +681,7 @@ int moe_lora_align_capacity(const moe_lora_dims* d, int64_t* max_rows, int64_t* 
 }
 
 int moe_lora_workspace_size(const moe_lora_dims* d, size_t* align_bytes, size_t* forward_bytes) {
+  MOE_RESOLVE(d);
   MOE_TRY(validate_dims(d));
   if (align_bytes) *align_bytes = align_layout(d).bytes;
   if (forward_bytes) *forward_bytes = fwd_layout(d).bytes;
@@ -573,6 +689,7 @@ int moe_lora_workspace_size(const moe_lora_dims* d, size_t* align_bytes, size_t*
 }
 
 int moe_lora_layer_workspace_size(const moe_lora_dims* d, size_t* bytes) {
+  MOE_RESOLVE(d);
   MOE_TRY(validate_dims(d));
   if (!bytes) return fail(MOE_LORA_EINVAL, "bytes is NULL");
   *bytes = layer_layout(d).bytes;
@@ -589,6 +706,13 @@ int moe_lora_align(const moe_lora_dims* d, const int32_t* topk_ids, const int32_
   return do_align(d, topk_ids, lora_ids, out, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
 }
 
+int moe_lora_route_align(const moe_lora_dims* d, const float* logits, const int32_t* lora_ids, int32_t* topk_ids,
+                         float* topk_w, const moe_lora_align_buf* out, void* workspace, size_t workspace_bytes,
+                         void* stream) {
+  return do_route_align(d, logits, lora_ids, topk_ids, topk_w, out, workspace, workspace_bytes,
+                        static_cast<cudaStream_t>(stream));
+}
+
 int moe_lora_forward(const moe_lora_dims* d, const uint16_t* x, const float* topk_w,
                      const moe_lora_align_buf* aligned, const uint16_t* W_gu, const uint16_t* W_dn,
                      const uint16_t* A_gu, const uint16_t* Bt_gu, const uint16_t* A_dn, const uint16_t* Bt_dn,
@@ -602,6 +726,7 @@ int moe_lora_layer_host(const moe_lora_dims* d, const float* logits_host, const 
                         const uint16_t* x_host, const uint16_t* W_gu, const uint16_t* W_dn, const uint16_t* A_gu,
                         const uint16_t* Bt_gu, const uint16_t* A_dn, const uint16_t* Bt_dn, uint16_t* out_host,
                         void* workspace, size_t workspace_bytes, int64_t* dropped, void* stream) {
+  MOE_RESOLVE(d);
   MOE_TRY(validate_dims(d));
   const LayerLayout l = layer_layout(d);
   MOE_TRY(check_ptr(workspace, "workspace", true));
@@ -629,9 +754,10 @@ int moe_lora_layer_host(const moe_lora_dims* d, const float* logits_host, const 
     MOE_CUDA(cudaMemcpyAsync(logits, logits_host, T * d->E * 4, cudaMemcpyHostToDevice, s));
     MOE_CUDA(cudaMemcpyAsync(lora, lora_ids_host, T * 4, cudaMemcpyHostToDevice, s));
     MOE_CUDA(cudaMemcpyAsync(x, x_host, T * d->H * 2, cudaMemcpyHostToDevice, s));
-    MOE_TRY(do_route(logits, d->T, d->E, d->k, ids, w, s));
+    MOE_TRY(do_route_align(d, logits, lora, ids, w, &al, b + l.align, l.fwd - l.align, s));
+  } else {
+    MOE_TRY(do_align(d, ids, lora, &al, b + l.align, l.fwd - l.align, s));
   }
-  MOE_TRY(do_align(d, ids, lora, &al, b + l.align, l.fwd - l.align, s));
   MOE_TRY(do_forward(d, x, w, &al, W_gu, W_dn, A_gu, Bt_gu, A_dn, Bt_dn, out, b + l.fwd, l.logits - l.fwd, status, s,
                       nullptr));
   int32_t host_status = 0, tot[4] = {0, 0, 0, 0};
@@ -680,6 +806,7 @@ int static_scratch(void** out) {
 
 extern "C" int moe_lora_align_static(const moe_lora_dims* d, const int32_t* topk_ids, const int32_t* lora_ids,
                                      const moe_lora_align_buf* out, void* stream) {
+  MOE_RESOLVE(d);
   MOE_TRY(validate_dims(d));
   const size_t need = align_layout(d).bytes;
   if (need > MOE_LORA_STATIC_SCRATCH_BYTES)

@@ -1,4 +1,5 @@
-// rows.cu -- row gather into sorted order and the final fp32 -> bf16 conversion.
+// rows.cu -- row gather into sorted order, the SiLU pass after a K-split gate_up,
+// and the weighted top-k combine.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -8,24 +9,19 @@ namespace moe {
 namespace {
 
 // x_sorted[row] = x[sorted_p[row] / k] for real rows, zero for padding rows; one warp
-// per row, 16-byte vectors.  The same launch zeroes the fp32 combine accumulator and
-// the call's device status word, so the forward needs no memset nodes.
+// per row, 16-byte vectors.  Lane 0 records pair_row[p] = row for the combine.  The
+// same launch zeroes the call's device status word and the GEMMs' tile counters, so
+// the forward needs no memset nodes.
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ sorted_p,
                                                           const int32_t* __restrict__ totals, int64_t max_rows, int vec_per_row,
-                                                          int k, int P, uint4* __restrict__ xs, float4* __restrict__ acc,
-                                                          int64_t n_acc4, int32_t* __restrict__ status,
-                                                          int32_t* __restrict__ ctr, int n_ctr,
-                                                          float4* __restrict__ g_acc, int g_cols4) {
+                                                          int k, int P, uint4* __restrict__ xs,
+                                                          int32_t* __restrict__ pair_row, int32_t* __restrict__ status,
+                                                          int32_t* __restrict__ ctr, int n_ctr) {
   pdl_trigger();   // the next kernel waits for this grid before reading what it writes
   const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t nthr = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t i = tid; i < n_acc4; i += nthr) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   if (tid == 0) *status = 0;
   for (int64_t i = tid; i < n_ctr; i += nthr) ctr[i] = 0;
-  if (g_acc) {
-    const int64_t n_g4 = static_cast<int64_t>(totals[0]) * g_cols4;
-    for (int64_t i = tid; i < n_g4; i += nthr) g_acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-  }
   const int lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (row >= max_rows || row >= totals[0]) return;
@@ -34,62 +30,155 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
   if (p >= P) {
     for (int v = lane; v < vec_per_row; v += 32) dst[v] = make_uint4(0, 0, 0, 0);
   } else {
+    if (lane == 0) pair_row[p] = static_cast<int32_t>(row);
     const uint4* src = x + static_cast<int64_t>(p / k) * vec_per_row;
-    for (int v = lane; v < vec_per_row; v += 32) dst[v] = __ldg(src + v);
+    int v = lane;
+    for (; v + 96 < vec_per_row; v += 128) {   // four loads in flight per lane
+      const uint4 a = __ldg(src + v), b = __ldg(src + v + 32), c = __ldg(src + v + 64), d = __ldg(src + v + 96);
+      dst[v] = a;
+      dst[v + 32] = b;
+      dst[v + 64] = c;
+      dst[v + 96] = d;
+    }
+    for (; v < vec_per_row; v += 32) dst[v] = __ldg(src + v);
   }
 }
 
-__global__ void __launch_bounds__(256) finalize_kernel(const float4* __restrict__ acc, uint2* __restrict__ out, int64_t n4) {
-  pdl_wait();   // out_acc is complete once the down GEMM has finished
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const float4 v = acc[i];
-    __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y);
-    __nv_bfloat162 b = __floats2bfloat162_rn(v.z, v.w);
-    out[i] = make_uint2(*reinterpret_cast<uint32_t*>(&a), *reinterpret_cast<uint32_t*>(&b));
+__device__ __forceinline__ void unpack_bf16x8(const uint4& v, float* f) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// One warp per (token, column slab): lanes j < k look up the token's pairs -- a pair's
+// row is trusted only if the sorted order really holds the pair there (the row record
+// of a dropped pair is stale), so dropped pairs add nothing -- then every lane
+// combines 8 columns at a time over the slab.  Large batches give a warp a whole token
+// (ns = 1); small ones split the columns so that enough warps stream.  Pairs in
+// ascending j, splits in ascending order: the result does not depend on which CTA of
+// the GEMM finished first.
+constexpr int kCombineThreads = 256;
+template <bool SPLIT>
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const void* __restrict__ y, int ksplit,
+                                                                  int64_t part_rows,
+                                                                  const int32_t* __restrict__ pair_row,
+                                                                  const int32_t* __restrict__ sorted_p,
+                                                                  const int32_t* __restrict__ totals,
+                                                                  const float* __restrict__ topk_w, int64_t T, int k,
+                                                                  int H8, int ns, uint4* __restrict__ out) {
+  __shared__ int32_t s_row[kCombineThreads / 32][MOE_LORA_MAX_TOPK];
+  __shared__ float s_w[kCombineThreads / 32][MOE_LORA_MAX_TOPK];
+  pdl_wait();   // the down GEMM's rows are complete
+  const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+  const int64_t gw = static_cast<int64_t>(blockIdx.x) * (kCombineThreads / 32) + wib;
+  if (gw >= T * ns) return;
+  const int64_t t = gw / ns;
+  const int slab = static_cast<int>(gw - t * ns);
+  int r = -1;
+  float w = 0.f;
+  if (lane < k) {
+    const int64_t p = t * k + lane;
+    r = pair_row[p];
+    if (r < 0 || r >= totals[0] || sorted_p[r] != p) r = -1;
+    else w = topk_w[p];
+  }
+  // compact the valid pairs, keeping ascending j
+  const unsigned valid = __ballot_sync(0xffffffffu, r >= 0);
+  if (r >= 0) {
+    const int slot = __popc(valid & ((1u << lane) - 1u));
+    s_row[wib][slot] = r;
+    s_w[wib][slot] = w;
+  }
+  __syncwarp();
+  const int n = __popc(valid);
+  const int per = (H8 + ns - 1) / ns;
+  const int c_end = min(H8, (slab + 1) * per);
+  for (int c = slab * per + lane; c < c_end; c += 32) {
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int j0 = 0; j0 < n; j0 += 4) {
+      float d[4][8];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) d[u][q] = 0.f;
+        if (j0 + u < n) {
+          const int64_t rr = s_row[wib][j0 + u];
+          if constexpr (!SPLIT) {
+            unpack_bf16x8(__ldg(reinterpret_cast<const uint4*>(y) + rr * H8 + c), d[u]);
+          } else {
+            for (int sp = 0; sp < ksplit; ++sp) {
+              const float4* src = reinterpret_cast<const float4*>(y) + ((sp * part_rows + rr) * H8 + c) * 2;
+              const float4 a = __ldcg(src), b = __ldcg(src + 1);
+              d[u][0] += a.x; d[u][1] += a.y; d[u][2] += a.z; d[u][3] += a.w;
+              d[u][4] += b.x; d[u][5] += b.y; d[u][6] += b.z; d[u][7] += b.w;
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (j0 + u < n) {
+          const float wu = s_w[wib][j0 + u];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) acc[q] += wu * d[u][q];
+        }
+      }
+    }
+    out[t * H8 + c] = make_uint4(pack2(acc[0], acc[1]), pack2(acc[2], acc[3]), pack2(acc[4], acc[5]),
+                                 pack2(acc[6], acc[7]));
   }
 }
 
 }  // namespace
 
 cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* sorted_p, const int32_t* totals, int64_t max_rows,
-                               int H, int k, int P, uint16_t* x_sorted, float* out_acc, int64_t n_acc,
-                               int32_t* status, int32_t* ctr, int n_ctr, float* g_acc, int g_cols, cudaStream_t s) {
+                               int H, int k, int P, uint16_t* x_sorted, int32_t* pair_row, int32_t* status,
+                               int32_t* ctr, int n_ctr, cudaStream_t s) {
   const int rows_per_cta = 8;
   int64_t grid = (max_rows + rows_per_cta - 1) / rows_per_cta;
-  // enough threads for the zeroing too (about 16 float4 per thread, at most 8 CTAs per SM)
-  const int64_t zero4 = n_acc / 4 + (g_acc ? max_rows * (g_cols / 4) : 0);
-  int64_t zgrid = (zero4 / 16 + 255) / 256;
-  if (zgrid > 152 * 8) zgrid = 152 * 8;
-  if (grid < zgrid) grid = zgrid;
   if (grid < 1) grid = 1;
   gather_rows_kernel<<<static_cast<unsigned>(grid), rows_per_cta * 32, 0, s>>>(
       reinterpret_cast<const uint4*>(x), sorted_p, totals, max_rows, H / 8, k, P, reinterpret_cast<uint4*>(x_sorted),
-      reinterpret_cast<float4*>(out_acc), n_acc / 4, status, ctr, n_ctr, reinterpret_cast<float4*>(g_acc), g_cols / 4);
+      pair_row, status, ctr, n_ctr);
   return cudaGetLastError();
 }
 
 namespace {
-// h[row][i] = bf16(silu(g[row][i]) * g[row][I + i]) for rows < totals[0]; 4 features per thread.
-__global__ void __launch_bounds__(256) silu_rows_kernel(const float4* __restrict__ g, const int32_t* __restrict__ totals,
-                                                        int I4, uint2* __restrict__ h) {
+// h[row][i] = bf16(silu(g[row][i]) * g[row][I + i]) for rows < totals[0], g the sum of the
+// K splits' partials in split order; 4 features per thread.
+__global__ void __launch_bounds__(256) silu_rows_kernel(const float4* __restrict__ g, int ksplit, int64_t part_rows,
+                                                        const int32_t* __restrict__ totals, int I4,
+                                                        uint2* __restrict__ h) {
   pdl_wait();      // the gate_up partial sums are complete
   pdl_trigger();
   const int64_t n = static_cast<int64_t>(totals[0]) * I4;
+  const int64_t split_stride = part_rows * 2 * I4;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t row = i / I4, c = i % I4;
-    const float4 a = g[row * 2 * I4 + c], b = g[row * 2 * I4 + I4 + c];
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+    for (int sp = 0; sp < ksplit; ++sp) {
+      const float4* src = g + sp * split_stride + row * 2 * I4;
+      const float4 ga = __ldcg(src + c), gb = __ldcg(src + I4 + c);
+      a.x += ga.x; a.y += ga.y; a.z += ga.z; a.w += ga.w;
+      b.x += gb.x; b.y += gb.y; b.z += gb.z; b.w += gb.w;
+    }
     auto silu = [](float z) { return z / (1.0f + __expf(-z)); };
-    __nv_bfloat162 lo = __floats2bfloat162_rn(silu(a.x) * b.x, silu(a.y) * b.y);
-    __nv_bfloat162 hi = __floats2bfloat162_rn(silu(a.z) * b.z, silu(a.w) * b.w);
-    h[i] = make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+    h[i] = make_uint2(pack2(silu(a.x) * b.x, silu(a.y) * b.y), pack2(silu(a.z) * b.z, silu(a.w) * b.w));
   }
 }
 }  // namespace
 
-cudaError_t launch_silu_rows(const float* g_acc, const int32_t* totals, int64_t max_rows, int I, uint16_t* h,
-                             bool pdl, cudaStream_t s) {
+cudaError_t launch_silu_rows(const float* g_part, int ksplit, int64_t part_rows, const int32_t* totals,
+                             int64_t max_rows, int I, uint16_t* h, bool pdl, cudaStream_t s) {
   int64_t grid = (max_rows * (I / 4) + 255) / 256;
   if (grid > 152 * 8) grid = 152 * 8;
   if (grid < 1) grid = 1;
@@ -102,26 +191,40 @@ cudaError_t launch_silu_rows(const float* g_acc, const int32_t* totals, int64_t 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, silu_rows_kernel, reinterpret_cast<const float4*>(g_acc), totals, I / 4,
-                            reinterpret_cast<uint2*>(h));
+  return cudaLaunchKernelEx(&cfg, silu_rows_kernel, reinterpret_cast<const float4*>(g_part), ksplit, part_rows, totals,
+                            I / 4, reinterpret_cast<uint2*>(h));
 }
 
-cudaError_t launch_finalize(const float* acc, uint16_t* out, int64_t n, bool pdl, cudaStream_t s) {
-  if (n <= 0) return cudaSuccess;
-  const int64_t n4 = n / 4;
-  int64_t grid = (n4 + 255) / 256;
-  if (grid > 152 * 8) grid = 152 * 8;
+cudaError_t launch_combine(const void* y, int ksplit, int64_t part_rows, const int32_t* pair_row,
+                           const int32_t* sorted_p, const int32_t* totals, const float* topk_w, int64_t T, int k,
+                           int H, uint16_t* out, bool pdl, cudaStream_t s) {
+  if (T <= 0) return cudaSuccess;
+  const int H8 = H / 8;
+  // column slabs per token: at least ~16 warps per SM (152 SMs) when T is small,
+  // each slab at least one 32-lane sweep of columns
+  const int64_t want_warps = 152 * 16;
+  int64_t ns = T >= want_warps ? 1 : (want_warps + T - 1) / T;
+  const int64_t max_ns = (H8 + 31) / 32;
+  if (ns > max_ns) ns = max_ns;
+  const int64_t warps = T * ns;
+  const int64_t blocks = (warps + kCombineThreads / 32 - 1) / (kCombineThreads / 32);
+  if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-  cfg.blockDim = dim3(256, 1, 1);
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
+  cfg.blockDim = dim3(kCombineThreads, 1, 1);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, finalize_kernel, reinterpret_cast<const float4*>(acc),
-                            reinterpret_cast<uint2*>(out), n4);
+  uint4* o = reinterpret_cast<uint4*>(out);
+  const int nsi = static_cast<int>(ns);
+  if (ksplit > 1)
+    return cudaLaunchKernelEx(&cfg, combine_kernel<true>, y, ksplit, part_rows, pair_row, sorted_p, totals, topk_w, T,
+                              k, H8, nsi, o);
+  return cudaLaunchKernelEx(&cfg, combine_kernel<false>, y, ksplit, part_rows, pair_row, sorted_p, totals, topk_w, T,
+                            k, H8, nsi, o);
 }
 
 }  // namespace moe

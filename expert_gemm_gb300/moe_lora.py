@@ -22,7 +22,8 @@ MAX_ADAPTERS, MAX_RANK, MAX_EXPERTS, MAX_TOPK = 256, 64, 1024, 32
 
 EXPORTS = ["moe_lora_align_capacity", "moe_lora_workspace_size", "moe_lora_pick_block_m", "moe_lora_route",
            "moe_lora_align", "moe_lora_forward", "moe_lora_layer_workspace_size", "moe_lora_layer_host",
-           "moe_lora_status_string", "moe_lora_last_error", "moe_lora_version", "moe_lora_align_static"]
+           "moe_lora_status_string", "moe_lora_last_error", "moe_lora_version", "moe_lora_align_static",
+           "moe_lora_route_align", "moe_lora_plan_query"]
 STATIC_SCRATCH_BYTES = 4 << 20
 
 
@@ -34,6 +35,15 @@ class Dims(C.Structure):
 class AlignBuf(C.Structure):
     _fields_ = [("sorted_p", C.c_void_p), ("expert_begin", C.c_void_p), ("block_expert", C.c_void_p),
                 ("block_runs", C.c_void_p), ("runs", C.c_void_p), ("totals", C.c_void_p)]
+
+
+class Plan(C.Structure):
+    _fields_ = [("block_m", C.c_int32), ("table_row", C.c_int32), ("weight_streaming", C.c_int32),
+                ("ksplit", C.c_int32 * 4), ("k_tile", C.c_int32 * 4), ("stages", C.c_int32 * 4),
+                ("launches_route_align", C.c_int32), ("launches_forward", C.c_int32)]
+
+
+GEMMS = ("shrink_gu", "gate_up", "shrink_dn", "down")
 
 
 class MoeLoraError(RuntimeError):
@@ -63,6 +73,8 @@ def load(path: str = LIB_PATH):
     lib.moe_lora_route.argtypes = [vp, i64, i32, i32, vp, vp, vp]
     lib.moe_lora_align.argtypes = [DP, vp, vp, AP, vp, sz, vp]
     lib.moe_lora_align_static.argtypes = [DP, vp, vp, AP, vp]
+    lib.moe_lora_route_align.argtypes = [DP, vp, vp, vp, vp, AP, vp, sz, vp]
+    lib.moe_lora_plan_query.argtypes = [DP, C.POINTER(Plan)]
     lib.moe_lora_forward.argtypes = [DP, vp, vp, AP, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp, vp]
     lib.moe_lora_layer_host.argtypes = [DP, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, C.POINTER(i64), vp]
     lib.moe_lora_status_string.restype = C.c_char_p
@@ -71,7 +83,7 @@ def load(path: str = LIB_PATH):
     lib.moe_lora_version.restype = C.c_int
     for name in ("moe_lora_align_capacity", "moe_lora_workspace_size", "moe_lora_layer_workspace_size",
                  "moe_lora_route", "moe_lora_align", "moe_lora_forward", "moe_lora_layer_host",
-                 "moe_lora_align_static"):
+                 "moe_lora_align_static", "moe_lora_route_align", "moe_lora_plan_query"):
         getattr(lib, name).restype = C.c_int
     _lib = lib
     return lib
@@ -128,6 +140,16 @@ def pick_block_m(T: int, k: int, E: int) -> int:
     return load().moe_lora_pick_block_m(T, k, E)
 
 
+def plan(d: LayerDims) -> dict:
+    """moe_lora_plan_query as a dict (host only)."""
+    p = Plan()
+    _check(load().moe_lora_plan_query(C.byref(d.c()), C.byref(p)))
+    return {"block_m": p.block_m, "table_row": p.table_row, "weight_streaming": bool(p.weight_streaming),
+            "ksplit": dict(zip(GEMMS, p.ksplit)), "k_tile": dict(zip(GEMMS, p.k_tile)),
+            "stages": dict(zip(GEMMS, p.stages)), "launches_route_align": p.launches_route_align,
+            "launches_forward": p.launches_forward}
+
+
 def align_capacity(d: LayerDims):
     r, b, n = C.c_int64(), C.c_int64(), C.c_int64()
     _check(load().moe_lora_align_capacity(C.byref(d.c()), C.byref(r), C.byref(b), C.byref(n)))
@@ -181,8 +203,15 @@ def align_static(d: LayerDims, topk_ids, lora_ids, bufs: dict, stream=None):
                                         _stream(stream)))
 
 
+def route_align(d: LayerDims, logits, lora_ids, topk_ids, topk_w, bufs: dict, workspace, stream=None):
+    """route + align; one launch when T*k <= 4096.  topk_ids, topk_w and bufs are outputs."""
+    _check(load().moe_lora_route_align(C.byref(d.c()), _ptr(logits), _ptr(lora_ids), _ptr(topk_ids), _ptr(topk_w),
+                                       C.byref(_abuf(bufs)), _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
 NUM_STAGES = 6
-STAGES = ("gather", "shrink_gu", "gate_up", "shrink_dn", "down", "finalize")
+STAGES = ("gather", "shrink_gu", "gate_up", "shrink_dn", "down", "combine")
 
 
 def forward(d: LayerDims, x, topk_w, bufs: dict, w: dict, out, workspace, dev_status, stream=None,
@@ -215,7 +244,7 @@ def layer_host(d: LayerDims, logits_host, lora_ids_host, x_host, w: dict, out_ho
 class Layer:
     """One MoE-LoRA layer with device-resident weights and preallocated scratch.
 
-    `step(logits, lora_ids, x)` runs route -> align -> forward on device tensors and
+    `step(logits, lora_ids, x)` runs route+align -> forward on device tensors and
     returns the bf16 output tensor; `step_host(...)` runs the whole layer from host
     buffers through moe_lora_layer_host.
     """
@@ -236,8 +265,7 @@ class Layer:
         self._ws_layer = None
 
     def step(self, logits, lora_ids, x, stream=None, stage_events=None):
-        route(logits, self.d.k, self.topk_ids, self.topk_w, stream)
-        align(self.d, self.topk_ids, lora_ids, self.bufs, self.ws_align, stream)
+        route_align(self.d, logits, lora_ids, self.topk_ids, self.topk_w, self.bufs, self.ws_align, stream)
         forward(self.d, x, self.topk_w, self.bufs, self.w, self.out, self.ws_fwd, self.status, stream,
                 stage_events)
         return self.out

@@ -68,8 +68,8 @@ enum {
 #define MOE_LORA_STAGE_SHRINK_GU 1   /* gate_up_shrink                         */
 #define MOE_LORA_STAGE_GATE_UP 2     /* gate_up GEMM + expand + SiLU gating    */
 #define MOE_LORA_STAGE_SHRINK_DN 3   /* down_shrink                            */
-#define MOE_LORA_STAGE_DOWN 4        /* down GEMM + expand + weighted combine  */
-#define MOE_LORA_STAGE_FINALIZE 5    /* fp32 accumulation -> bf16 output       */
+#define MOE_LORA_STAGE_DOWN 4        /* down GEMM + expand, one row per pair   */
+#define MOE_LORA_STAGE_COMBINE 5     /* weighted top-k combine -> bf16 output  */
 #define MOE_LORA_NUM_STAGES 6
 
 /* Limits of the compiled kernels (MOE_LORA_EUNSUPPORTED beyond them). */
@@ -88,7 +88,8 @@ typedef struct moe_lora_dims {
     int32_t L;        /* adapters, 0..MOE_LORA_MAX_ADAPTERS                             */
     int32_t r_max;    /* storage rank: rows of A, columns of Bt; multiple of 8, <= 64   */
     int32_t block_m;  /* rows per align block: 16, 32, 64 (weight-streaming kernels)    */
-                      /* or 128, 256 (token-tiled kernels); see moe_lora_pick_block_m   */
+                      /* or 128, 256 (token-tiled kernels); 0 = the tile table's choice */
+                      /* for (T, k, E) (moe_lora_pick_block_m, moe_lora_plan_query)     */
     const int32_t *ranks; /* HOST array [L]: rank of adapter a, 1 <= ranks[a] <= r_max  */
 } moe_lora_dims;
 
@@ -124,9 +125,29 @@ int moe_lora_align_capacity(const moe_lora_dims *d, int64_t *max_rows, int64_t *
  * with forward's region at offset align_bytes).  Returns a status. */
 int moe_lora_workspace_size(const moe_lora_dims *d, size_t *align_bytes, size_t *forward_bytes);
 
-/* A block_m suited to T*k pairs over E experts (16..64 when experts see few tokens,
- * 128 when they see many). */
+/* The compiled-in tile table's block_m for T*k pairs over E experts: the shape class
+ * is the pairs per expert T*k/E (16, 32, 64 weight-streaming up to 10, 24, 95 pairs per
+ * expert; 128 token-tiled above).  The pages pick tuned tile configurations per shape
+ * ([AWS] "Tuning kernel configurations for Amazon SageMaker AI and Amazon Bedrock";
+ * [KO] "Amazon 전용 튜닝"). */
 int32_t moe_lora_pick_block_m(int64_t T, int32_t k, int32_t E);
+
+/* What the calls will launch for these dims: the tile-table row and the per-GEMM
+ * choices.  GEMM index: 0 gate_up shrink, 1 gate_up, 2 down shrink, 3 down. */
+typedef struct moe_lora_plan {
+    int32_t block_m;              /* token tile = align block (dims.block_m, or the table's) */
+    int32_t table_row;            /* row of the compiled tile table whose constants apply    */
+    int32_t weight_streaming;     /* 1: tiles of 128 weight rows x block_m tokens;
+                                     0: tiles of 128 tokens x 256 weight rows               */
+    int32_t ksplit[4];            /* K splits per GEMM (0: not launched, L == 0 shrinks)     */
+    int32_t k_tile[4];            /* K elements per pipeline stage                          */
+    int32_t stages[4];            /* pipeline stages in shared memory                       */
+    int32_t launches_route_align; /* kernel launches of one moe_lora_route_align           */
+    int32_t launches_forward;     /* kernel launches of one moe_lora_forward               */
+} moe_lora_plan;
+
+/* Fills *out for dims d (host only: no device call).  Returns a status. */
+int moe_lora_plan_query(const moe_lora_dims *d, moe_lora_plan *out);
 
 /* ------------------------------------------------------------ the calls -- */
 
@@ -153,6 +174,21 @@ int moe_lora_align(const moe_lora_dims *d, const int32_t *topk_ids, const int32_
                    void *stream);
 
 /*
+ * moe_lora_route followed by moe_lora_align, with the same arguments and results
+ * (topk_ids and topk_w are outputs here).  The pages route, then group the routed
+ * tokens per (expert, adapter) for the fused MoE-LoRA kernels ([AWS] "Implementing
+ * multi-LoRA inference for MoE models in vLLM"; [KO] "MoE 모델을 위한 Multi-LoRA
+ * 서빙"); a batch of at most 4096 pairs (T*k <= 4096) is routed and aligned by one
+ * single-CTA launch, larger batches take the two calls' launches.
+ *   logits [T][E] fp32, lora_ids [T] int32: device, read
+ *   topk_ids [T][k] int32, topk_w [T][k] fp32: device, written
+ *   workspace: device scratch of at least align_bytes (moe_lora_workspace_size)
+ */
+int moe_lora_route_align(const moe_lora_dims *d, const float *logits, const int32_t *lora_ids,
+                         int32_t *topk_ids, float *topk_w, const moe_lora_align_buf *out,
+                         void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * The fused expert computation over an aligned pair list: gate_up GEMM with its
  * LoRA shrink and expand, SiLU gating, down GEMM with its LoRA shrink and expand,
  * and the weighted top-k combine.
@@ -171,6 +207,10 @@ int moe_lora_align(const moe_lora_dims *d, const int32_t *topk_ids, const int32_
  *   stage_events  NULL, or MOE_LORA_NUM_STAGES + 1 cudaEvent_t recorded on `stream`
  *              before the first stage and after each stage (for timing)
  * LoRA tensors may be NULL when L == 0.
+ * Deterministic: no step accumulates with atomics.  Each pair's expert output gets
+ * its own row (K-split partial sums their own buffers), and the combine adds a
+ * token's k rows in ascending j, so the same inputs give the same output bytes on
+ * every call.
  */
 int moe_lora_forward(const moe_lora_dims *d, const uint16_t *x, const float *topk_w,
                      const moe_lora_align_buf *aligned,

@@ -79,7 +79,7 @@ def test_every_block_size(ml, torch, oracle, block_m):
 @pytest.mark.parametrize("block_m", [16, 32])
 def test_down_split_k(ml, torch, oracle, block_m):
     """Few tokens over a long I: the weight-streaming down GEMM runs with K split 4 ways,
-    partial sums meeting in the fp32 accumulator."""
+    each split storing fp32 partial rows that the combine adds in split order."""
     wl = W.custom(name="splitk", T=8, H=256, I=2048, E=4, k=2, L=2, ranks=(16, 32), lora_mode="uniform_with_none")
     run_case(ml, torch, oracle, wl, block_m=block_m)
 
@@ -92,8 +92,8 @@ def test_shrink_split_k(ml, torch, oracle):
 
 
 def test_gate_up_split_k(ml, torch, oracle):
-    """Few feature tiles: the weight-streaming gate_up splits K, its fp32 partials meet
-    before SiLU; the down GEMM splits too."""
+    """Few feature tiles: the weight-streaming gate_up splits K, its fp32 partials are
+    added in split order before SiLU."""
     wl = W.custom(name="gusplit", T=8, H=1024, I=512, E=2, k=1, L=2, ranks=(16, 32), lora_mode="uniform_with_none")
     run_case(ml, torch, oracle, wl, block_m=16)
 
@@ -151,6 +151,11 @@ def test_invalid_ids_dropped(ml, torch, oracle):
     lora[9] = -5
     d = dims_of(wl, 16, ml)
     layer = ml.Layer(d, dev_weights(w, torch))
+    # stale scratch: every int32 of the forward workspace names an in-range row, so a
+    # dropped pair's row record points at some real row unless the combine checks it
+    rows = int(ml.align_capacity(d)[0])
+    ws32 = layer.ws_fwd[: layer.ws_fwd.numel() // 4 * 4].view(torch.int32)
+    ws32.copy_(torch.randint(0, rows, ws32.shape, dtype=torch.int32, device="cuda"))
     ids_d, tw_d = to_dev(ids, torch), to_dev(tw.astype(np.float32), torch)
     ml.align(d, ids_d, to_dev(lora, torch), layer.bufs, layer.ws_align)
     ml.forward(d, to_dev(x, torch), tw_d, layer.bufs, layer.w, layer.out, layer.ws_fwd, layer.status)
@@ -161,6 +166,63 @@ def test_invalid_ids_dropped(ml, torch, oracle):
     ref = oracle.forward(x, ids, tw.astype(np.float32), lora, w)
     elem, _ = parity_error(layer.out.float().cpu().numpy(), ref)
     assert elem <= TOL
+
+
+@pytest.mark.parametrize("case", ["decode_bm16", "gusplit_bm16", "mid_bm128", "mid_bm256"])
+def test_deterministic_bytes(ml, torch, case):
+    """No atomics on the path: repeated calls give identical output bytes, also after
+    another batch has run through the same buffers (K-split partial buffers and the
+    bf16 row path both covered)."""
+    shapes = {
+        "decode": W.get("decode"),
+        "gusplit": W.custom(name="gusplit", T=8, H=1024, I=512, E=2, k=1, L=2, ranks=(16, 32),
+                            lora_mode="uniform_with_none"),
+        "mid": W.custom(name="mid", T=700, H=384, I=448, E=6, k=2, L=3, ranks=(16, 32, 8),
+                        lora_mode="uniform_with_none"),
+    }
+    name, bm = case.split("_bm")
+    wl = shapes[name]
+    logits, lora, x, w = inputs(wl)
+    layer = ml.Layer(dims_of(wl, int(bm), ml), dev_weights(w, torch))
+    lg, lr, xd = to_dev(logits, torch), to_dev(lora, torch), to_dev(x, torch)
+    first = layer.step(lg, lr, xd).clone()
+    g = np.random.default_rng(9)
+    layer.step(to_dev(g.standard_normal(logits.shape).astype(np.float32), torch), lr,
+               to_dev(W.f32_to_bf16_bits(g.standard_normal(x.shape).astype(np.float32)), torch))
+    for _ in range(3):
+        again = layer.step(lg, lr, xd)
+        torch.cuda.synchronize()
+        assert torch.equal(first.view(torch.int16), again.view(torch.int16))
+    assert int(layer.status.item()) == 0
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode", "sweep_T256", "sweep_T4096"])
+def test_route_align_matches_separate_calls(ml, torch, name):
+    """moe_lora_route_align (one launch up to 4096 pairs, else route + align launches)
+    gives the same bytes as moe_lora_route followed by moe_lora_align."""
+    wl = W.get(name)
+    logits, lora = W.make_routing(wl, 0)
+    bm = ml.pick_block_m(wl.T, wl.k, wl.E)
+    d = dims_of(wl, bm, ml)
+    a_bytes, _ = ml.workspace_size(d)
+    lg, lr = to_dev(logits, torch), to_dev(lora, torch)
+    res = []
+    for fused in (False, True):
+        bufs = ml.alloc_align(d)
+        ws = torch.empty(max(a_bytes, 256), dtype=torch.uint8, device="cuda")
+        ids = torch.full((wl.T, wl.k), -9, dtype=torch.int32, device="cuda")
+        tw = torch.full((wl.T, wl.k), -9.0, dtype=torch.float32, device="cuda")
+        if fused:
+            ml.route_align(d, lg, lr, ids, tw, bufs, ws)
+        else:
+            ml.route(lg, wl.k, ids, tw)
+            ml.align(d, ids, lr, bufs, ws)
+        torch.cuda.synchronize()
+        res.append((ids.cpu().numpy(), tw.cpu().numpy(), align_to_numpy(bufs)))
+    (i0, w0, a0), (i1, w1, a1) = res
+    assert np.array_equal(i0, i1)
+    assert np.array_equal(w0.view(np.int32), w1.view(np.int32))
+    assert_align_equal(a1, a0)
 
 
 def test_empty_batch(ml, torch):

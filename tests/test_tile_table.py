@@ -1,0 +1,100 @@
+"""The compiled-in tile table and the launch plan (host logic only, no GPU).
+
+The shape class is the pairs per expert T*k/E; each workload lands in the row the
+table states, block_m = 0 resolves to that row everywhere, and the plan's K splits
+and launch counts follow the rules written beside the table.
+"""
+import pytest
+
+from expert_gemm_gb300 import moe_lora as ml
+from expert_gemm_gb300 import workloads as W
+
+
+def dims(wl, block_m):
+    return ml.LayerDims(T=wl.T, H=wl.H, I=wl.I, E=wl.E, k=wl.k, L=wl.L, r_max=wl.r_max, block_m=block_m,
+                        ranks=tuple(wl.ranks))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    from expert_gemm_gb300 import build
+    build.build()
+    return ml.load()
+
+
+# (name, block_m the table must pick)
+EXPECTED = [("tiny", 32), ("decode", 16), ("prefill", 128), ("wide", 128), ("dense_decode", 32),
+            ("sweep_T1", 16), ("sweep_T16", 16), ("sweep_T256", 32), ("sweep_T4096", 128)]
+
+
+@pytest.mark.parametrize("name,bm", EXPECTED)
+def test_class_of_each_workload(name, bm):
+    wl = W.get(name)
+    assert ml.pick_block_m(wl.T, wl.k, wl.E) == bm
+    p = ml.plan(dims(wl, 0))
+    assert p["block_m"] == bm
+    assert p["weight_streaming"] == (bm < 128)
+
+
+def test_class_boundaries():
+    """Pairs per expert above 10, 24 and 95 move to the next row."""
+    E, k = 8, 1
+    for ppe, bm in [(1, 16), (10, 16), (11, 32), (24, 32), (25, 64), (95, 64), (96, 128), (5000, 128)]:
+        assert ml.pick_block_m(ppe * E, k, E) == bm, (ppe, bm)
+    assert ml.pick_block_m(0, 1, 8) == 16
+
+
+@pytest.mark.parametrize("name", [n for n, _ in EXPECTED])
+def test_auto_block_m_resolves_everywhere(name):
+    """block_m = 0 gives the same capacities, workspace sizes and plan as the explicit pick."""
+    wl = W.get(name)
+    bm = ml.pick_block_m(wl.T, wl.k, wl.E)
+    a, b = dims(wl, 0), dims(wl, bm)
+    assert ml.align_capacity(a) == ml.align_capacity(b)
+    assert ml.workspace_size(a) == ml.workspace_size(b)
+    assert ml.layer_workspace_size(a) == ml.layer_workspace_size(b)
+    assert ml.plan(a) == ml.plan(b)
+
+
+def test_decode_plan():
+    """Decode layer (64 pairs over 32 experts, H = I = 2880): 16-token weight-streaming
+    tiles; the down GEMM (12 feature tiles per block) splits K three ways to give each
+    of the 152 SMs about six tiles; gate_up (23 tiles per block) needs no split; the
+    2880-long shrinks stay whole (45 K-tiles < 64)."""
+    p = ml.plan(dims(W.get("decode"), 0))
+    assert p["ksplit"] == {"shrink_gu": 1, "gate_up": 1, "shrink_dn": 1, "down": 3}
+    assert p["k_tile"] == {"shrink_gu": 64, "gate_up": 64, "shrink_dn": 64, "down": 64}
+    assert p["launches_route_align"] == 1
+    assert p["launches_forward"] == 6      # gather, 2 shrinks, gate_up, down, combine
+
+
+def test_prefill_plan():
+    p = ml.plan(dims(W.get("prefill"), 0))
+    assert p["block_m"] == 128 and not p["weight_streaming"]
+    assert p["ksplit"] == {"shrink_gu": 1, "gate_up": 1, "shrink_dn": 1, "down": 1}
+    assert p["launches_route_align"] == 4  # 102400 pairs: route, then chunk/scan/scatter
+    assert p["launches_forward"] == 6
+
+
+def test_split_plans():
+    """Shapes the GPU tests use to exercise each K split."""
+    gu = W.custom(name="gusplit", T=8, H=1024, I=512, E=2, k=1, L=2, ranks=(16, 32), lora_mode="uniform_with_none")
+    p = ml.plan(dims(gu, 16))
+    assert p["ksplit"]["gate_up"] > 1 and p["ksplit"]["down"] == 1   # I = 512: 8 K-tiles, too few to split
+    assert p["launches_forward"] == 7      # + the SiLU pass after the split gate_up
+    sh = W.custom(name="shsplit", T=6, H=256, I=8192, E=2, k=1, L=3, ranks=(16, 64, 32), lora_mode="uniform")
+    p = ml.plan(dims(sh, 16))
+    assert p["ksplit"]["shrink_dn"] > 1 and p["ksplit"]["shrink_gu"] == 1
+    l0 = W.custom(name="l0", T=48, H=256, I=256, E=4, k=2, L=0, ranks=(), lora_mode="none")
+    p = ml.plan(dims(l0, 16))
+    assert p["ksplit"]["shrink_gu"] == 0 and p["ksplit"]["shrink_dn"] == 0
+    assert p["launches_forward"] == 4
+
+
+def test_every_compiled_block_size_has_a_plan():
+    wl = W.get("decode")
+    for bm in (16, 32, 64, 128, 256):
+        p = ml.plan(dims(wl, bm))
+        assert p["block_m"] == bm and all(s >= 2 for s in p["stages"].values())
+    with pytest.raises(ml.MoeLoraError):
+        ml.plan(dims(wl, 48))
