@@ -46,22 +46,29 @@ namespace moe {
 template <int MODE, bool SWAP, int BT>
 struct GemmCfg {
   static constexpr bool kLora = MODE != kShrink;
+  // 256-token blocks of gate_up / down run on a CTA pair (a cluster of 2): one 2-SM
+  // MMA of M = 256 tokens x N = 256 weight rows per K-step; each CTA stages its own
+  // 128 token rows and half of the weight rows, and holds its tokens' accumulator.
+  static constexpr bool CTA2 = !SWAP && BT == 256 && MODE != kShrink;
+  static constexpr int TROWS = CTA2 ? 128 : BT;       // token rows staged by this CTA
   static constexpr int BK = gemm_bk(MODE, BT);        // K elements per stage
   static constexpr int ROWB = BK * 2;                 // bytes of one staged row = swizzle span
   static constexpr uint32_t SW = BK == 64 ? kSw128 : kSw64;
   static constexpr uint32_t SBO = 8 * ROWB;           // bytes between 8-row core groups
   static constexpr int CPS = BK / kRankChunk;         // LoRA rank chunks per stage
   // weight-side rows staged per K-tile
-  static constexpr int WROWS = MODE == kShrink ? (SWAP ? 128 : 64) : 256;
+  static constexpr int WROWS = MODE == kShrink ? (SWAP ? 128 : 64) : (CTA2 ? 128 : 256);
   static constexpr int W_BYTES = WROWS * ROWB;
-  static constexpr int T_BYTES = BT * ROWB;
+  static constexpr int T_BYTES = TROWS * ROWB;
   static constexpr int STAGE_BYTES = W_BYTES + T_BYTES;
+  // a CTA pair's 32 KB stages: as many as fit next to the barrier block (7 = 227 KB)
   static constexpr int STAGES = MODE == kShrink ? 4
                                 : SWAP           ? (BT <= 16 ? 6 : 5)
+                                : CTA2           ? (224 * 1024) / STAGE_BYTES
                                                  : (192 * 1024) / STAGE_BYTES;
   // accumulators: non-swapped MT tiles of M=128 tokens x N; swapped NH tiles of 128 x BT
   static constexpr int NH = MODE == kShrink ? 1 : 2;
-  static constexpr int MT = SWAP ? 1 : BT / 128;
+  static constexpr int MT = SWAP ? 1 : TROWS / 128;
   static constexpr int NACC = MODE == kShrink ? 64 : 256;   // columns of one non-swapped accumulator
   static constexpr int ACC_COLS = SWAP ? NH * BT : MT * NACC;
   static constexpr int NBUF = 2 * ACC_COLS <= 512 ? 2 : 1;  // TMEM accumulator buffers
@@ -75,6 +82,7 @@ struct GemmCfg {
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
   static_assert(W_BYTES % 1024 == 0 && T_BYTES % 1024 == 0, "stage regions keep 1024-byte alignment");
   static_assert(STAGES >= 2 && STAGES <= 8, "pipeline depth");
+  static_assert(!kLora || CPS * (WROWS + TROWS) * 32 <= STAGE_BYTES, "LoRA chunks of a stage fit its slot");
 };
 
 // One unit of work.  kShrink: one adapter run.  kGateUp / kDown: one (K split, token
@@ -194,6 +202,7 @@ __global__ void __launch_bounds__(192, 1)
   using C = GemmCfg<MODE, SWAP, BT>;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = C::CTA2 ? cluster_ctarank() : 0u;   // 0: issues the pair's MMAs
 
   // Ordering with the previous kernel of the stream (programmatic dependent launch):
   // the shrink reads token rows written by it, so it waits before anything else and
@@ -221,7 +230,7 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int j = 0; j < 2; ++j) {
       mbar_init(&bars->acc_full[j], 1);
-      mbar_init(&bars->acc_empty[j], 4);
+      mbar_init(&bars->acc_empty[j], C::CTA2 ? 8 : 4);   // a pair: both CTAs' epilogue warps
     }
     for (int j = 0; j < C::SD; ++j) {
       mbar_init(&bars->sched_full[j], 1);
@@ -232,11 +241,17 @@ __global__ void __launch_bounds__(192, 1)
     fence_barrier_init();
   }
   if (warp == 1) {
-    tmem_alloc(&bars->tmem_base, C::TMEM_COLS);
-    tmem_relinquish();
+    if constexpr (C::CTA2) {
+      tmem_alloc_pair(&bars->tmem_base, C::TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(&bars->tmem_base, C::TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before_sync();
   __syncthreads();
+  if constexpr (C::CTA2) cluster_sync();   // the peer's barriers exist before any remote arrival
   tc_fence_after_sync();
   const uint32_t tmem = bars->tmem_base;
 
@@ -250,10 +265,15 @@ __global__ void __launch_bounds__(192, 1)
         tma_prefetch_desc(&maps.ls);
       }
       bool waited_pdl = false;
-      int gs = 0;   // stages issued by this CTA (continues across tiles)
+      int gs = 0;        // stages issued by this CTA (continues across tiles)
+      int pst = 0;       // gs % STAGES
+      uint32_t pph = 0;  // (gs / STAGES) & 1
       for (int i = 0;; ++i) {
         // take the next tile and publish it (n_live = no more work)
-        const int tau = aborted(bars) ? n_live : atomicAdd(prm.tile_ctr, 1);
+        // a CTA pair walks a fixed stride of tiles (both CTAs must take the same ones)
+        const int tau = aborted(bars) ? n_live
+                        : C::CTA2     ? static_cast<int>(blockIdx.x >> 1) + i * static_cast<int>(gridDim.x >> 1)
+                                      : atomicAdd(prm.tile_ctr, 1);
         const int slot = i & 3;
         if (!mbar_wait(&bars->sched_empty[slot], ((i >> 2) & 1) ^ 1)) {
           record_timeout(bars, prm.status);
@@ -267,14 +287,14 @@ __global__ void __launch_bounds__(192, 1)
         if (tau >= n_live) break;
         int lr = 0, lc = 0;   // LoRA run and first rank chunk of the next LoRA stage
         bool ok = true;
-        for (int it = 0; it < t.n_it; ++it, ++gs) {
-          const int s = gs % C::STAGES;
-          const uint32_t ph = (gs / C::STAGES) & 1;
+        for (int it = 0; it < t.n_it; ++it) {
+          const int s = pst;
+          const uint32_t ph = pph;
           if (aborted(bars)) {
             ok = false;
             break;
           }
-          if (!mbar_wait(&bars->empty[s], ph ^ 1)) {
+          if (!(C::CTA2 ? mbar_wait_cluster(&bars->empty[s], ph ^ 1) : mbar_wait(&bars->empty[s], ph ^ 1))) {
             record_timeout(bars, prm.status);
             ok = false;
             break;
@@ -282,7 +302,17 @@ __global__ void __launch_bounds__(192, 1)
           uint8_t* wdst = smem + s * C::STAGE_BYTES;
           uint8_t* tdst = wdst + C::W_BYTES;
           uint64_t* fb = &bars->full[s];
-          if (it < t.nk) {
+          // a pair's loads all complete on the even CTA's barrier, which expects both halves
+          const uint32_t fb_pair = C::CTA2 ? mapa_shared(fb, 0) : 0u;
+          if (C::CTA2 && it < t.nk) {
+            const int k0 = (t.kb0 + it) * C::BK;
+            if (rank == 0) mbar_arrive_expect_tx(fb, 2 * (C::W_BYTES + C::T_BYTES));
+            if constexpr (MODE == kGateUp)
+              tma_load_4d_pair(wdst, &maps.w, fb_pair, k0, t.f0, static_cast<int>(rank), t.e);  // gate | up rows
+            else
+              tma_load_3d_pair(wdst, &maps.w, fb_pair, k0, t.f0 + 128 * static_cast<int>(rank), t.e);
+            tma_load_2d_pair(tdst, &maps.tok, fb_pair, k0, t.row0 + 128 * static_cast<int>(rank));
+          } else if (it < t.nk) {
             const int k0 = (t.kb0 + it) * C::BK;
             if constexpr (MODE == kGateUp) {
               mbar_arrive_expect_tx(fb, C::W_BYTES + C::T_BYTES);
@@ -309,18 +339,32 @@ __global__ void __launch_bounds__(192, 1)
             const int nch = (prm.ranks[a] + kRankChunk - 1) / kRankChunk;
             const int nc = nch - lc < C::CPS ? nch - lc : C::CPS;
             const int ae = a * prm.E + t.e;
-            mbar_arrive_expect_tx(fb, nc * (C::WROWS * 32 + BT * 32));
-            for (int j = 0; j < nc; ++j) {
-              const int c = lc + j;
-              uint8_t* wc = wdst + j * (C::WROWS * 32);
-              if constexpr (MODE == kGateUp) {
-                tma_load_4d(wc, &maps.lw, fb, c * kRankChunk, t.f0, 0, ae);
-                tma_load_4d(wc + 128 * 32, &maps.lw, fb, c * kRankChunk, t.f0, 1, ae);
-              } else {
-                tma_load_3d(wc, &maps.lw, fb, c * kRankChunk, t.f0, ae);
-                tma_load_3d(wc + 128 * 32, &maps.lw, fb, c * kRankChunk, t.f0 + 128, ae);
+            if constexpr (C::CTA2) {
+              if (rank == 0) mbar_arrive_expect_tx(fb, 2 * nc * (C::WROWS * 32 + C::TROWS * 32));
+              const int rk = static_cast<int>(rank);
+              for (int j = 0; j < nc; ++j) {
+                const int c = lc + j;
+                uint8_t* wc = wdst + j * (C::WROWS * 32);
+                if constexpr (MODE == kGateUp)
+                  tma_load_4d_pair(wc, &maps.lw, fb_pair, c * kRankChunk, t.f0, rk, ae);
+                else
+                  tma_load_3d_pair(wc, &maps.lw, fb_pair, c * kRankChunk, t.f0 + 128 * rk, ae);
+                tma_load_3d_pair(tdst + j * (C::TROWS * 32), &maps.ls, fb_pair, c * kRankChunk, 128 * rk, run);
               }
-              tma_load_3d(tdst + j * (BT * 32), &maps.ls, fb, c * kRankChunk, 0, run);
+            } else {
+              mbar_arrive_expect_tx(fb, nc * (C::WROWS * 32 + C::TROWS * 32));
+              for (int j = 0; j < nc; ++j) {
+                const int c = lc + j;
+                uint8_t* wc = wdst + j * (C::WROWS * 32);
+                if constexpr (MODE == kGateUp) {
+                  tma_load_4d(wc, &maps.lw, fb, c * kRankChunk, t.f0, 0, ae);
+                  tma_load_4d(wc + 128 * 32, &maps.lw, fb, c * kRankChunk, t.f0, 1, ae);
+                } else {
+                  tma_load_3d(wc, &maps.lw, fb, c * kRankChunk, t.f0, ae);
+                  tma_load_3d(wc + 128 * 32, &maps.lw, fb, c * kRankChunk, t.f0 + 128, ae);
+                }
+                tma_load_3d(tdst + j * (C::TROWS * 32), &maps.ls, fb, c * kRankChunk, 0, run);
+              }
             }
             lc += nc;
             if (lc >= nch) {
@@ -328,19 +372,51 @@ __global__ void __launch_bounds__(192, 1)
               ++lr;
             }
           }
+          ++gs;
+          if (++pst == C::STAGES) {
+            pst = 0;
+            pph ^= 1;
+          }
         }
         if (!ok) break;
       }
       // Leave no copy in flight after an abort: wait (bounded) for the last stages issued.
-      if (aborted(bars)) {
+      // (In a pair the even CTA's barriers count both CTAs' copies; the odd CTA stays
+      // resident until the closing cluster barrier, after the even CTA has drained.)
+      if (aborted(bars) && rank == 0) {
         for (int g = gs - C::STAGES < 0 ? 0 : gs - C::STAGES; g < gs; ++g)
-          (void)mbar_wait(&bars->full[g % C::STAGES], (g / C::STAGES) & 1);
+          (void)mbar_wait_cluster(&bars->full[g % C::STAGES], (g / C::STAGES) & 1);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      int gs = 0;
+    if (C::CTA2 && lane == 0 && rank != 0) {
+      // The odd CTA of a pair issues no MMA (the even CTA's 2-SM MMAs fill its TMEM);
+      // it only hands its ring slots back.
+      for (int i = 0;; ++i) {
+        const Tile* tp = sched_read(bars, i, prm.status);
+        if (!tp) break;
+        const int tau = tp->h.tau;
+        mbar_arrive(&bars->sched_empty[i & 3]);
+        if (tau >= n_live) break;
+      }
+    } else if (lane == 0) {
+      // pair (2-SM) or single-CTA MMA, and commits that reach both CTAs of a pair
+      auto mma = [&](uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accum) {
+        if constexpr (C::CTA2) tc_mma_pair(d, a, b, idesc, accum);
+        else tc_mma(d, a, b, idesc, accum);
+      };
+      auto commit = [&](uint64_t* bar) {
+        if constexpr (C::CTA2) tc_commit_pair(bar, 0x3);
+        else tc_commit(bar);
+      };
+      constexpr int kM = C::CTA2 ? 256 : 128;
+      // stage-0 descriptors: base K-steps (128/64-byte swizzle rows), LoRA K-steps (32-byte)
+      const uint32_t sbase = smem_u32(smem);
+      const uint64_t dW = smem_desc(sbase, C::SBO, C::SW), dT = smem_desc(sbase + C::W_BYTES, C::SBO, C::SW);
+      const uint64_t dWl = smem_desc(sbase, 256, kSw32), dTl = smem_desc(sbase + C::W_BYTES, 256, kSw32);
+      int st = 0;          // stage of the next K-step (continues across tiles)
+      uint32_t sph = 0;    // its phase parity
       for (int i = 0;; ++i) {
         const Tile* tp = sched_read(bars, i, prm.status);
         if (!tp) break;
@@ -350,48 +426,44 @@ __global__ void __launch_bounds__(192, 1)
           break;
         }
         const int ab = i % C::NBUF;
-        if (!mbar_wait(&bars->acc_empty[ab], ((i / C::NBUF) & 1) ^ 1)) {
+        const uint32_t eph = ((i / C::NBUF) & 1) ^ 1;
+        if (!(C::CTA2 ? mbar_wait_cluster(&bars->acc_empty[ab], eph) : mbar_wait(&bars->acc_empty[ab], eph))) {
           record_timeout(bars, prm.status);
           break;
         }
         tc_fence_after_sync();
         const uint32_t acc_base = tmem + ab * C::ACC_COLS;
+        // instruction descriptors of this tile's base and LoRA K-steps
+        const uint32_t id_base = SWAP ? idesc_bf16_f32(128, BT)
+                                      : idesc_bf16_f32(kM, MODE == kShrink ? t.snch * kRankChunk : 256);
+        constexpr uint32_t id_lora = SWAP ? idesc_bf16_f32(128, BT) : idesc_bf16_f32(kM, 256);
         uint32_t acc = 0;
         int lr = 0, lc = 0;
         bool ok = true;
-        for (int it = 0; it < t.n_it; ++it, ++gs) {
-          const int s = gs % C::STAGES;
-          const uint32_t ph = (gs / C::STAGES) & 1;
-          if (aborted(bars)) {
-            ok = false;
-            break;
-          }
-          if (!mbar_wait(&bars->full[s], ph)) {
+        // The hot loop issues from one thread: descriptors are the stage-0 ones plus
+        // constant offsets (16-byte units), stage and phase advance by increment, and
+        // no flag is polled (every wait is bounded, and a failed one ends the loop).
+        for (int it = 0; it < t.n_it; ++it) {
+          if (!(C::CTA2 ? mbar_wait_cluster(&bars->full[st], sph) : mbar_wait(&bars->full[st], sph))) {
             record_timeout(bars, prm.status);
             ok = false;
             break;
           }
           tc_fence_after_sync();
-          const uint32_t wbase = smem_u32(smem + s * C::STAGE_BYTES);
-          const uint32_t tbase = wbase + C::W_BYTES;
+          const uint64_t so = static_cast<uint64_t>(st) * (C::STAGE_BYTES >> 4);
           if (it < t.nk) {
 #pragma unroll
             for (int kk = 0; kk < C::BK / 16; ++kk) {
+              const uint64_t ko = so + static_cast<uint64_t>(kk * 2);   // 32 bytes of K per step
               if constexpr (!SWAP) {
-                const uint32_t n_mma = MODE == kShrink ? t.snch * kRankChunk : 256;
-                const uint64_t bd = smem_desc(wbase + kk * 32, C::SBO, C::SW);
 #pragma unroll
-                for (int mt = 0; mt < C::MT; ++mt) {
-                  const uint64_t ad = smem_desc(tbase + mt * 128 * C::ROWB + kk * 32, C::SBO, C::SW);
-                  tc_mma(acc_base + mt * C::NACC, ad, bd, idesc_bf16_f32(128, n_mma), acc);
-                }
+                for (int mt = 0; mt < C::MT; ++mt)
+                  mma(acc_base + mt * C::NACC, dT + ko + static_cast<uint64_t>(mt * 8 * C::ROWB), dW + ko, id_base,
+                      acc);
               } else {
-                const uint64_t bd = smem_desc(tbase + kk * 32, C::SBO, C::SW);
 #pragma unroll
-                for (int h = 0; h < C::NH; ++h) {
-                  const uint64_t ad = smem_desc(wbase + h * 128 * C::ROWB + kk * 32, C::SBO, C::SW);
-                  tc_mma(acc_base + h * BT, ad, bd, idesc_bf16_f32(128, BT), acc);
-                }
+                for (int h = 0; h < C::NH; ++h)
+                  tc_mma(acc_base + h * BT, dW + ko + static_cast<uint64_t>(h * 8 * C::ROWB), dT + ko, id_base, acc);
               }
               acc = 1;
             }
@@ -404,30 +476,30 @@ __global__ void __launch_bounds__(192, 1)
               ++lr;
             }
             for (int c = 0; c < nc; ++c) {
-              const uint32_t wc = wbase + c * (C::WROWS * 32);
-              const uint32_t tc = tbase + c * (BT * 32);
+              const uint64_t wo = so + static_cast<uint64_t>(c * (C::WROWS * 2));   // WROWS x 32 bytes
+              const uint64_t to = so + static_cast<uint64_t>(c * (C::TROWS * 2));
               if constexpr (!SWAP) {
-                const uint64_t bd = smem_desc(wc, 256, kSw32);
 #pragma unroll
                 for (int mt = 0; mt < C::MT; ++mt)
-                  tc_mma(acc_base + mt * C::NACC, smem_desc(tc + mt * 128 * 32, 256, kSw32), bd,
-                         idesc_bf16_f32(128, 256), 1);
+                  mma(acc_base + mt * C::NACC, dTl + to + static_cast<uint64_t>(mt * 256), dWl + wo, id_lora, 1);
               } else {
-                const uint64_t bd = smem_desc(tc, 256, kSw32);
 #pragma unroll
                 for (int h = 0; h < C::NH; ++h)
-                  tc_mma(acc_base + h * BT, smem_desc(wc + h * 128 * 32, 256, kSw32), bd,
-                         idesc_bf16_f32(128, BT), 1);
+                  tc_mma(acc_base + h * BT, dWl + wo + static_cast<uint64_t>(h * 256), dTl + to, id_lora, 1);
               }
             }
           }
-          tc_commit(&bars->empty[s]);
+          commit(&bars->empty[st]);
+          if (++st == C::STAGES) {
+            st = 0;
+            sph ^= 1;
+          }
         }
-        tc_commit(&bars->acc_full[ab]);   // also after an abort, so the epilogue is released
+        commit(&bars->acc_full[ab]);   // also after an abort, so the epilogue is released
         mbar_arrive(&bars->sched_empty[i & 3]);
         if (!ok) break;
       }
-      tc_commit(&bars->drain);   // arrives once every MMA issued above has completed
+      commit(&bars->drain);   // arrives once every MMA issued above has completed
     }
   } else {
     // ------------------------------------------------------------ epilogue
@@ -443,12 +515,14 @@ __global__ void __launch_bounds__(192, 1)
         break;
       }
       const int ab = i % C::NBUF;
-      const bool got = mbar_wait(&bars->acc_full[ab], (i / C::NBUF) & 1);
+      const uint32_t fph = (i / C::NBUF) & 1;
+      const bool got = C::CTA2 ? mbar_wait_cluster(&bars->acc_full[ab], fph) : mbar_wait(&bars->acc_full[ab], fph);
       if (!got) record_timeout(bars, prm.status);
       tc_fence_after_sync();
       const bool ok = got && !aborted(bars);
       const uint32_t tq = tmem + ab * C::ACC_COLS + (static_cast<uint32_t>(q * 32) << 16);
-      const int row0 = t.row0, f0 = t.f0;
+      // first token row of this CTA's accumulator (a pair's odd CTA holds rows 128..255)
+      const int row0 = t.row0 + 128 * static_cast<int>(rank), f0 = t.f0;
       if (ok) {
         uint32_t v[16], u[16];
         if constexpr (MODE == kShrink) {
@@ -639,7 +713,8 @@ __global__ void __launch_bounds__(192, 1)
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(&bars->acc_empty[ab]);
+        if (C::CTA2 && rank != 0) mbar_arrive_cluster(mapa_shared(&bars->acc_empty[ab], 0));
+        else mbar_arrive(&bars->acc_empty[ab]);
         mbar_arrive(&bars->sched_empty[i & 3]);
       }
       if (!ok) break;
@@ -651,11 +726,16 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after_sync();
-    // every MMA of this CTA has completed before its TMEM is freed
-    if (lane == 0) (void)mbar_wait(&bars->drain, 0);
+    // every MMA of this CTA (of a pair: of the even CTA, into both) has completed
+    // before its TMEM is freed
+    if (lane == 0) (void)(C::CTA2 ? mbar_wait_cluster(&bars->drain, 0) : mbar_wait(&bars->drain, 0));
     __syncwarp();
-    tmem_dealloc(tmem, C::TMEM_COLS);
+    if constexpr (C::CTA2) tmem_dealloc_pair(tmem, C::TMEM_COLS);
+    else tmem_dealloc(tmem, C::TMEM_COLS);
   }
+  // a pair: neither CTA leaves while the other may still arrive on its barriers or
+  // have the MMA read its shared memory
+  if constexpr (C::CTA2) cluster_sync();
 }
 
 template <int MODE, bool SWAP, int BT>
@@ -670,32 +750,56 @@ cudaError_t launch_gemm_t(const GemmMaps& maps, const GemmParams& prm, int64_t m
   // Persistent grid: as many CTAs as fit on the device at once, no more than tiles.
   // The attribute and the occupancy are settled on the first launch of this kernel
   // (per process: one device model), so later launches make no such calls.
-  static int per_sm = 0, sms = 0;
-  if (per_sm == 0) {
-    int dev = 0, occ = 0;
-    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-    if (err == cudaSuccess) err = cudaGetDevice(&dev);
-    if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (err == cudaSuccess) err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, 192, C::SMEM_BYTES);
-    if (err != cudaSuccess) return err;
-    if (occ < 1) occ = 1;
-    // co-resident CTAs share TMEM: keep their accumulators within its 512 columns
-    while (occ > 1 && occ * C::TMEM_COLS > 512) --occ;
-    per_sm = occ;
-  }
-  int64_t grid = static_cast<int64_t>(sms) * per_sm;
-  if (grid > cap_tiles) grid = cap_tiles;
-
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
   cfg.blockDim = dim3(192, 1, 1);
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;   // CTA pairs (used only by the 2-SM kernels)
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = C::CTA2 ? attr : attr + 1;
+  cfg.numAttrs = (C::CTA2 ? 1 : 0) + (pdl ? 1 : 0);
+
+  // Persistent grid: as many CTAs (CTA pairs) as fit on the device at once, no more
+  // than tiles.  The attribute and the occupancy are settled on the first launch of
+  // this kernel (per process: one device model), so later launches make no such calls.
+  static int64_t max_ctas = 0;
+  if (max_ctas == 0) {
+    int dev = 0, sms = 0, occ = 0;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (err == cudaSuccess) err = cudaGetDevice(&dev);
+    if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (err != cudaSuccess) return err;
+    if constexpr (C::CTA2) {
+      // one pair per two SMs at most (a CTA needs all of its SM's TMEM)
+      cudaLaunchConfig_t q = cfg;
+      q.gridDim = dim3(static_cast<unsigned>(sms & ~1), 1, 1);
+      q.numAttrs = 1;   // the cluster dimension only
+      err = cudaOccupancyMaxActiveClusters(&occ, kern, &q);
+      if (err != cudaSuccess) return err;
+      if (occ < 1) occ = 1;
+      if (occ > sms / 2) occ = sms / 2;
+      max_ctas = 2 * static_cast<int64_t>(occ);
+    } else {
+      err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, 192, C::SMEM_BYTES);
+      if (err != cudaSuccess) return err;
+      if (occ < 1) occ = 1;
+      // co-resident CTAs share TMEM: keep their accumulators within its 512 columns
+      while (occ > 1 && occ * C::TMEM_COLS > 512) --occ;
+      max_ctas = static_cast<int64_t>(sms) * occ;
+    }
+  }
+  int64_t grid = max_ctas;
+  if constexpr (C::CTA2) {
+    if (grid > 2 * cap_tiles) grid = 2 * cap_tiles;   // a pair per tile at most
+  } else {
+    if (grid > cap_tiles) grid = cap_tiles;
+  }
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
   return cudaLaunchKernelEx(&cfg, kern, maps, prm);
 }
 

@@ -104,8 +104,9 @@ int validate_dims(const moe_lora_dims* d) {
 // each streamed weight tile serves -- and the class fixes the token tile (= align
 // block) and, for the weight-streaming kernels, the targets of the K-split rules,
 // which then weigh the tile counts against H, I and the SM count.  Rows were set from
-// GB300 sweeps over the workloads' shapes (256-row blocks are accepted but were
-// slower than 128 with double-buffered TMEM, so no class picks them).
+// GB300 sweeps over the workloads' shapes: 256-row blocks (CTA pairs, 2-SM MMA) win
+// once experts see hundreds of tokens; at ~256 pairs per expert their padding and
+// extra adapter runs per block cost more than the halved weight traffic saves.
 struct TileClass {
   double ppe_above;       // the class holds shapes whose T*k/E exceeds this
   int block_m;            // token tile: < 128 weight-streaming, >= 128 token-tiled
@@ -118,7 +119,8 @@ constexpr TileClass kTileTable[] = {
     {-1.0, 16, 2, 6, 64, 8},    // up to 10 pairs per expert (decode batches)
     {10.0, 32, 2, 6, 64, 8},    // 10 .. 24
     {24.0, 64, 2, 6, 64, 8},    // 24 .. 95
-    {95.0, 128, 1, 1, 0, 1},    // more than 95: token-tiled, compute-bound, no K split
+    {95.0, 128, 1, 1, 0, 1},    // 95 .. 511: token-tiled, compute-bound, no K split
+    {511.0, 256, 1, 1, 0, 1},   // more than 511: 256-token blocks on CTA pairs
 };
 constexpr int kTableRows = sizeof(kTileTable) / sizeof(kTileTable[0]);
 
@@ -447,6 +449,9 @@ int do_forward(const moe_lora_dims* d, const uint16_t* x, const float* topk_w, c
   const uint32_t bk_gu = (uint32_t)moe::gemm_bk(moe::kGateUp, BT), bk_dn = (uint32_t)moe::gemm_bk(moe::kDown, BT);
   const uint32_t bk_sh = (uint32_t)moe::gemm_bk(moe::kShrink, BT);
   auto swz = [](uint32_t bk) { return bk == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B; };
+  // token rows one CTA of a gate_up / down launch stages: 256-row blocks run on CTA
+  // pairs, each CTA taking its 128 rows
+  const uint32_t tok_rows = BT == 256 ? 128u : (uint32_t)BT;
   {
     const uint64_t dm[4] = {H, I, 2, E}, st[3] = {H * 2, I * H * 2, 2 * I * H * 2};
     const uint32_t bx[4] = {bk_gu, 128, 1, 1};
@@ -459,14 +464,14 @@ int do_forward(const moe_lora_dims* d, const uint16_t* x, const float* topk_w, c
   }
   {
     const uint64_t dm[2] = {H, rows}, st[1] = {H * 2};
-    const uint32_t bx[2] = {bk_gu, (uint32_t)BT};
+    const uint32_t bx[2] = {bk_gu, tok_rows};
     MOE_TRY(encode(&m_gu.tok, xs, 2, dm, st, bx, swz(bk_gu), "x_sorted"));
     const uint32_t bxs[2] = {bk_sh, (uint32_t)BT};
     MOE_TRY(encode(&m_sgu.tok, xs, 2, dm, st, bxs, swz(bk_sh), "x_sorted"));
   }
   {
     const uint64_t dm[2] = {I, rows}, st[1] = {I * 2};
-    const uint32_t bx[2] = {bk_dn, (uint32_t)BT};
+    const uint32_t bx[2] = {bk_dn, tok_rows};
     MOE_TRY(encode(&m_dn.tok, hs, 2, dm, st, bx, swz(bk_dn), "h_sorted"));
     const uint32_t bxs[2] = {bk_sh, (uint32_t)BT};
     MOE_TRY(encode(&m_sdn.tok, hs, 2, dm, st, bxs, swz(bk_sh), "h_sorted"));
@@ -494,7 +499,7 @@ int do_forward(const moe_lora_dims* d, const uint16_t* x, const float* topk_w, c
     }
     {
       const uint64_t dm[3] = {RP, (uint64_t)BT, nruns}, st[2] = {RP * 2, (uint64_t)BT * RP * 2};
-      const uint32_t bx[3] = {16, (uint32_t)BT, 1};
+      const uint32_t bx[3] = {16, tok_rows, 1};
       MOE_TRY(encode(&m_gu.ls, sgu, 3, dm, st, bx, CU_TENSOR_MAP_SWIZZLE_32B, "S_gu"));
       MOE_TRY(encode(&m_dn.ls, sdn, 3, dm, st, bx, CU_TENSOR_MAP_SWIZZLE_32B, "S_dn"));
     }

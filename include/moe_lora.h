@@ -127,7 +127,7 @@ int moe_lora_workspace_size(const moe_lora_dims *d, size_t *align_bytes, size_t 
 
 /* The compiled-in tile table's block_m for T*k pairs over E experts: the shape class
  * is the pairs per expert T*k/E (16, 32, 64 weight-streaming up to 10, 24, 95 pairs per
- * expert; 128 token-tiled above).  The pages pick tuned tile configurations per shape
+ * expert; 128 token-tiled up to 511; 256, token-tiled on CTA pairs, above).  The pages pick tuned tile configurations per shape
  * ([AWS] "Tuning kernel configurations for Amazon SageMaker AI and Amazon Bedrock";
  * [KO] "Amazon 전용 튜닝"). */
 int32_t moe_lora_pick_block_m(int64_t T, int32_t k, int32_t E);
@@ -138,7 +138,8 @@ typedef struct moe_lora_plan {
     int32_t block_m;              /* token tile = align block (dims.block_m, or the table's) */
     int32_t table_row;            /* row of the compiled tile table whose constants apply    */
     int32_t weight_streaming;     /* 1: tiles of 128 weight rows x block_m tokens;
-                                     0: tiles of 128 tokens x 256 weight rows               */
+                                     0: tiles of block_m tokens x 256 weight rows (256-token
+                                        tiles of gate_up/down run on a CTA pair)           */
     int32_t ksplit[4];            /* K splits per GEMM (0: not launched, L == 0 shrinks)     */
     int32_t k_tile[4];            /* K elements per pipeline stage                          */
     int32_t stages[4];            /* pipeline stages in shared memory                       */

@@ -70,7 +70,7 @@ def test_host_validation(ml):
 
 def test_pick_block_m(ml):
     assert ml.pick_block_m(16, 4, 32) == 16
-    assert ml.pick_block_m(25600, 4, 32) == 128
+    assert ml.pick_block_m(25600, 4, 32) == 256
     assert ml.pick_block_m(256, 8, 128) in (16, 32)
     assert ml.pick_block_m(4096, 8, 128) == 128
 

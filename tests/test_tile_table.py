@@ -23,7 +23,7 @@ def lib():
 
 
 # (name, block_m the table must pick)
-EXPECTED = [("tiny", 32), ("decode", 16), ("prefill", 128), ("wide", 128), ("dense_decode", 32),
+EXPECTED = [("tiny", 32), ("decode", 16), ("prefill", 256), ("wide", 256), ("dense_decode", 32),
             ("sweep_T1", 16), ("sweep_T16", 16), ("sweep_T256", 32), ("sweep_T4096", 128)]
 
 
@@ -37,9 +37,10 @@ def test_class_of_each_workload(name, bm):
 
 
 def test_class_boundaries():
-    """Pairs per expert above 10, 24 and 95 move to the next row."""
+    """Pairs per expert above 10, 24, 95 and 511 move to the next row."""
     E, k = 8, 1
-    for ppe, bm in [(1, 16), (10, 16), (11, 32), (24, 32), (25, 64), (95, 64), (96, 128), (5000, 128)]:
+    for ppe, bm in [(1, 16), (10, 16), (11, 32), (24, 32), (25, 64), (95, 64), (96, 128), (511, 128), (512, 256),
+                    (5000, 256)]:
         assert ml.pick_block_m(ppe * E, k, E) == bm, (ppe, bm)
     assert ml.pick_block_m(0, 1, 8) == 16
 
@@ -70,7 +71,8 @@ def test_decode_plan():
 
 def test_prefill_plan():
     p = ml.plan(dims(W.get("prefill"), 0))
-    assert p["block_m"] == 128 and not p["weight_streaming"]
+    assert p["block_m"] == 256 and not p["weight_streaming"]
+    assert p["stages"]["gate_up"] == 7 and p["stages"]["down"] == 7   # 32 KB stages of a CTA pair
     assert p["ksplit"] == {"shrink_gu": 1, "gate_up": 1, "shrink_dn": 1, "down": 1}
     assert p["launches_route_align"] == 4  # 102400 pairs: route, then chunk/scan/scatter
     assert p["launches_forward"] == 6
