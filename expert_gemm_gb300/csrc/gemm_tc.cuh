@@ -61,10 +61,8 @@ struct GemmCfg {
   static constexpr int W_BYTES = WROWS * ROWB;
   static constexpr int T_BYTES = TROWS * ROWB;
   static constexpr int STAGE_BYTES = W_BYTES + T_BYTES;
-  // a CTA pair's 32 KB stages: as many as fit next to the barrier block (7 = 227 KB)
   static constexpr int STAGES = MODE == kShrink ? 4
                                 : SWAP           ? (BT <= 16 ? 6 : 5)
-                                : CTA2           ? (224 * 1024) / STAGE_BYTES
                                                  : (192 * 1024) / STAGE_BYTES;
   // accumulators: non-swapped MT tiles of M=128 tokens x N; swapped NH tiles of 128 x BT
   static constexpr int NH = MODE == kShrink ? 1 : 2;
@@ -76,7 +74,7 @@ struct GemmCfg {
   static constexpr int TMEM_COLS =
       TMEM_NEED <= 32 ? 32 : TMEM_NEED <= 64 ? 64 : TMEM_NEED <= 128 ? 128 : TMEM_NEED <= 256 ? 256 : 512;
   static constexpr int SD = 4;                              // tile-id ring depth
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align slack*/ + 2048 /*barriers, tile ring*/;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align slack*/ + 4096 /*barriers, tile ring*/;
   static_assert(!SWAP || (BT == 16 || BT == 32 || BT == 64), "swapped tiles take 16/32/64 tokens");
   static_assert(SWAP || BT == 128 || BT == 256, "token-tiled blocks are 128 or 256 rows");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
@@ -103,6 +101,7 @@ struct TileHdr {
 struct Tile {
   TileHdr h;                    // copied to registers by every reader
   uint8_t nch[kMaxBlockRuns];   // rank chunks of each adapter run of the block
+  int16_t ad[kMaxBlockRuns];    // adapter of each run (the producer's LoRA loads)
 };
 
 struct GemmBars {
@@ -117,7 +116,7 @@ struct GemmBars {
   int32_t abort;
   Tile tiles[4];             // the tile ring (published with sched_full)
 };
-constexpr int kBarBytes = 2048;
+constexpr int kBarBytes = 4096;
 static_assert(sizeof(GemmBars) <= kBarBytes, "barrier block");
 
 __device__ __forceinline__ void record_timeout(GemmBars* bars, int32_t* status) {
@@ -141,7 +140,7 @@ __device__ __forceinline__ int live_tiles(const GemmParams& prm) {
 }
 
 template <int MODE, bool SWAP, int BT>
-__device__ __forceinline__ TileHdr decode_tile(int tau, const GemmParams& prm, uint8_t* nch_out) {
+__device__ __forceinline__ TileHdr decode_tile(int tau, const GemmParams& prm, uint8_t* nch_out, int16_t* ad_out) {
   using C = GemmCfg<MODE, SWAP, BT>;
   TileHdr t;
   t.tau = tau;
@@ -176,8 +175,10 @@ __device__ __forceinline__ TileHdr decode_tile(int tau, const GemmParams& prm, u
     t.nk = (ks + 1) * nk_all / prm.ksplit - t.kb0;
     t.n_it = t.nk;
     for (int r = 0; r < t.nruns; ++r) {
-      const int nch = (prm.ranks[prm.runs[4 * (t.run0 + r) + 1]] + kRankChunk - 1) / kRankChunk;
+      const int a = prm.runs[4 * (t.run0 + r) + 1];
+      const int nch = (prm.ranks[a] + kRankChunk - 1) / kRankChunk;
       nch_out[r] = static_cast<uint8_t>(nch);
+      ad_out[r] = static_cast<int16_t>(a);
       t.n_it += (nch + C::CPS - 1) / C::CPS;
     }
   }
@@ -281,7 +282,7 @@ __global__ void __launch_bounds__(192, 1)
         }
         TileHdr t;
         t.tau = n_live;
-        if (tau < n_live) t = decode_tile<MODE, SWAP, BT>(tau, prm, bars->tiles[slot].nch);
+        if (tau < n_live) t = decode_tile<MODE, SWAP, BT>(tau, prm, bars->tiles[slot].nch, bars->tiles[slot].ad);
         bars->tiles[slot].h = t;
         mbar_arrive(&bars->sched_full[slot]);   // release: the tile fields are visible to the readers
         if (tau >= n_live) break;
@@ -335,8 +336,8 @@ __global__ void __launch_bounds__(192, 1)
               waited_pdl = true;
             }
             const int run = t.run0 + lr;
-            const int a = prm.runs[4 * run + 1];
-            const int nch = (prm.ranks[a] + kRankChunk - 1) / kRankChunk;
+            const int a = bars->tiles[slot].ad[lr];
+            const int nch = bars->tiles[slot].nch[lr];
             const int nc = nch - lc < C::CPS ? nch - lc : C::CPS;
             const int ae = a * prm.E + t.e;
             if constexpr (C::CTA2) {
@@ -615,19 +616,26 @@ __global__ void __launch_bounds__(192, 1)
             for (int mt = 0; mt < C::MT; ++mt) {
               uint16_t* hrow = prm.h_out + static_cast<size_t>(row0 + mt * 128 + m) * I + f0;
               const uint32_t ta = tq + mt * C::NACC;
-              for (int c = 0; c < 128; c += 16) {
-                if (f0 + c >= I) break;
-                tmem_ld16(ta + c, v);          // gate features f0+c ..
-                tmem_ld16(ta + 128 + c, u);    // up features   f0+c ..
-                tmem_ld_wait();
-                uint32_t pk[8];
+              for (int c0 = 0; c0 < 128; c0 += 64) {   // 64 features per TMEM wait (I % 64 == 0)
+                if (f0 + c0 >= I) break;
+                uint32_t g[4][16], up[4][16];
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                  pk[j] = pack_bf16x2(silu_f(__uint_as_float(v[2 * j])) * __uint_as_float(u[2 * j]),
-                                      silu_f(__uint_as_float(v[2 * j + 1])) * __uint_as_float(u[2 * j + 1]));
-                uint4* dst = reinterpret_cast<uint4*>(hrow + c);
-                dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                for (int q4 = 0; q4 < 4; ++q4) {
+                  tmem_ld16(ta + c0 + 16 * q4, g[q4]);          // gate features
+                  tmem_ld16(ta + 128 + c0 + 16 * q4, up[q4]);   // up features
+                }
+                tmem_ld_wait();
+                uint4* dst = reinterpret_cast<uint4*>(hrow + c0);
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                  uint32_t pk[8];
+#pragma unroll
+                  for (int j = 0; j < 8; ++j)
+                    pk[j] = pack_bf16x2(silu_f(__uint_as_float(g[q4][2 * j])) * __uint_as_float(up[q4][2 * j]),
+                                        silu_f(__uint_as_float(g[q4][2 * j + 1])) * __uint_as_float(up[q4][2 * j + 1]));
+                  dst[2 * q4] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                  dst[2 * q4 + 1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                }
               }
             }
           } else {
@@ -747,9 +755,6 @@ cudaError_t launch_gemm_t(const GemmMaps& maps, const GemmParams& prm, int64_t m
   if constexpr (MODE == kShrink) cap_tiles = max_runs * prm.ksplit;
   else cap_tiles = max_blocks * prm.n_ft * prm.ksplit;
   if (cap_tiles <= 0) return cudaSuccess;
-  // Persistent grid: as many CTAs as fit on the device at once, no more than tiles.
-  // The attribute and the occupancy are settled on the first launch of this kernel
-  // (per process: one device model), so later launches make no such calls.
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(192, 1, 1);
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
@@ -769,10 +774,15 @@ cudaError_t launch_gemm_t(const GemmMaps& maps, const GemmParams& prm, int64_t m
   // this kernel (per process: one device model), so later launches make no such calls.
   static int64_t max_ctas = 0;
   if (max_ctas == 0) {
-    int dev = 0, sms = 0, occ = 0;
+    int dev = 0, sms = 0, occ = 0, smem_sm = 0, smem_rsv = 0;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    // all of the unified L1/shared array as shared memory, so co-resident CTAs fit
+    if (err == cudaSuccess)
+      err = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
     if (err == cudaSuccess) err = cudaGetDevice(&dev);
     if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (err == cudaSuccess) err = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    if (err == cudaSuccess) err = cudaDeviceGetAttribute(&smem_rsv, cudaDevAttrReservedSharedMemoryPerBlock, dev);
     if (err != cudaSuccess) return err;
     if constexpr (C::CTA2) {
       // one pair per two SMs at most (a CTA needs all of its SM's TMEM)
@@ -787,6 +797,17 @@ cudaError_t launch_gemm_t(const GemmMaps& maps, const GemmParams& prm, int64_t m
     } else {
       err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, 192, C::SMEM_BYTES);
       if (err != cudaSuccess) return err;
+      // The query can answer for a smaller shared-memory carveout than the launch gets;
+      // the CTAs that fit by shared memory, registers, threads and TMEM co-reside
+      // (measured: two 99 KB shrink CTAs per SM run together, the query says one).
+      cudaFuncAttributes fa{};
+      err = cudaFuncGetAttributes(&fa, kern);
+      if (err != cudaSuccess) return err;
+      int fit = smem_sm / (C::SMEM_BYTES + smem_rsv);
+      const int by_regs = fa.numRegs > 0 ? 65536 / (fa.numRegs * 192) : fit;
+      if (fit > by_regs) fit = by_regs;
+      if (fit > 2048 / 192) fit = 2048 / 192;
+      if (occ < fit) occ = fit;
       if (occ < 1) occ = 1;
       // co-resident CTAs share TMEM: keep their accumulators within its 512 columns
       while (occ > 1 && occ * C::TMEM_COLS > 512) --occ;
