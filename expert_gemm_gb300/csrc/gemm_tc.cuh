@@ -173,14 +173,17 @@ __device__ __forceinline__ TileHdr decode_tile(int tau, const GemmParams& prm, u
     }
     t.kb0 = ks * nk_all / prm.ksplit;
     t.nk = (ks + 1) * nk_all / prm.ksplit - t.kb0;
-    t.n_it = t.nk;
+    int chunks = 0;
     for (int r = 0; r < t.nruns; ++r) {
       const int a = prm.runs[4 * (t.run0 + r) + 1];
       const int nch = (prm.ranks[a] + kRankChunk - 1) / kRankChunk;
       nch_out[r] = static_cast<uint8_t>(nch);
       ad_out[r] = static_cast<int16_t>(a);
-      t.n_it += (nch + C::CPS - 1) / C::CPS;
+      chunks += nch;
     }
+    // the runs' rank chunks fill the LoRA stages back to back, CPS per stage
+    t.n_it = t.nk + (chunks + C::CPS - 1) / C::CPS;
+    t.snch = chunks;
   }
   t.e = prm.block_expert[t.b];
   t.row0 = t.b * BT;
@@ -335,28 +338,30 @@ __global__ void __launch_bounds__(192, 1)
               pdl_wait();
               waited_pdl = true;
             }
-            const int run = t.run0 + lr;
-            const int a = bars->tiles[slot].ad[lr];
-            const int nch = bars->tiles[slot].nch[lr];
-            const int nc = nch - lc < C::CPS ? nch - lc : C::CPS;
-            const int ae = a * prm.E + t.e;
+            // up to CPS rank chunks, continuing across run boundaries; chunk j of the
+            // stage: run lr, chunk lc of that run
+            const Tile& tl = bars->tiles[slot];
+            const int left = t.snch - (it - t.nk) * C::CPS;
+            const int nc = left < C::CPS ? left : C::CPS;
             if constexpr (C::CTA2) {
               if (rank == 0) mbar_arrive_expect_tx(fb, 2 * nc * (C::WROWS * 32 + C::TROWS * 32));
-              const int rk = static_cast<int>(rank);
-              for (int j = 0; j < nc; ++j) {
-                const int c = lc + j;
-                uint8_t* wc = wdst + j * (C::WROWS * 32);
+            } else {
+              mbar_arrive_expect_tx(fb, nc * (C::WROWS * 32 + C::TROWS * 32));
+            }
+            for (int j = 0; j < nc; ++j) {
+              const int run = t.run0 + lr;
+              const int ae = tl.ad[lr] * prm.E + t.e;
+              const int c = lc;
+              uint8_t* wc = wdst + j * (C::WROWS * 32);
+              uint8_t* tc = tdst + j * (C::TROWS * 32);
+              if constexpr (C::CTA2) {
+                const int rk = static_cast<int>(rank);
                 if constexpr (MODE == kGateUp)
                   tma_load_4d_pair(wc, &maps.lw, fb_pair, c * kRankChunk, t.f0, rk, ae);
                 else
                   tma_load_3d_pair(wc, &maps.lw, fb_pair, c * kRankChunk, t.f0 + 128 * rk, ae);
-                tma_load_3d_pair(tdst + j * (C::TROWS * 32), &maps.ls, fb_pair, c * kRankChunk, 128 * rk, run);
-              }
-            } else {
-              mbar_arrive_expect_tx(fb, nc * (C::WROWS * 32 + C::TROWS * 32));
-              for (int j = 0; j < nc; ++j) {
-                const int c = lc + j;
-                uint8_t* wc = wdst + j * (C::WROWS * 32);
+                tma_load_3d_pair(tc, &maps.ls, fb_pair, c * kRankChunk, 128 * rk, run);
+              } else {
                 if constexpr (MODE == kGateUp) {
                   tma_load_4d(wc, &maps.lw, fb, c * kRankChunk, t.f0, 0, ae);
                   tma_load_4d(wc + 128 * 32, &maps.lw, fb, c * kRankChunk, t.f0, 1, ae);
@@ -364,13 +369,12 @@ __global__ void __launch_bounds__(192, 1)
                   tma_load_3d(wc, &maps.lw, fb, c * kRankChunk, t.f0, ae);
                   tma_load_3d(wc + 128 * 32, &maps.lw, fb, c * kRankChunk, t.f0 + 128, ae);
                 }
-                tma_load_3d(tdst + j * (C::TROWS * 32), &maps.ls, fb, c * kRankChunk, 0, run);
+                tma_load_3d(tc, &maps.ls, fb, c * kRankChunk, 0, run);
               }
-            }
-            lc += nc;
-            if (lc >= nch) {
-              lc = 0;
-              ++lr;
+              if (++lc == tl.nch[lr]) {
+                lc = 0;
+                ++lr;
+              }
             }
           }
           ++gs;
@@ -439,7 +443,6 @@ __global__ void __launch_bounds__(192, 1)
                                       : idesc_bf16_f32(kM, MODE == kShrink ? t.snch * kRankChunk : 256);
         constexpr uint32_t id_lora = SWAP ? idesc_bf16_f32(128, BT) : idesc_bf16_f32(kM, 256);
         uint32_t acc = 0;
-        int lr = 0, lc = 0;
         bool ok = true;
         // The hot loop issues from one thread: descriptors are the stage-0 ones plus
         // constant offsets (16-byte units), stage and phase advance by increment, and
@@ -469,13 +472,9 @@ __global__ void __launch_bounds__(192, 1)
               acc = 1;
             }
           } else if constexpr (C::kLora) {
-            const int nch = tp->nch[lr];
-            const int nc = nch - lc < C::CPS ? nch - lc : C::CPS;
-            lc += nc;
-            if (lc >= nch) {
-              lc = 0;
-              ++lr;
-            }
+            // up to CPS rank chunks, of one or several runs (each chunk: its own S and Bt)
+            const int left = t.snch - (it - t.nk) * C::CPS;
+            const int nc = left < C::CPS ? left : C::CPS;
             for (int c = 0; c < nc; ++c) {
               const uint64_t wo = so + static_cast<uint64_t>(c * (C::WROWS * 2));   // WROWS x 32 bytes
               const uint64_t to = so + static_cast<uint64_t>(c * (C::TROWS * 2));
