@@ -84,15 +84,16 @@ struct GemmCfg {
 };
 
 // One unit of work.  kShrink: one adapter run.  kGateUp / kDown: one (K split, token
-// block, feature tile), feature tile fastest.  Only weight-streaming (swapped) gate_up
-// splits K; its partial pre-activations then meet in fp32 and SiLU runs afterwards.
+// block, feature tile), feature tile fastest, K split slowest.  Weight-streaming gate_up
+// and down split K when their tiles are too few for the SMs; every split stores its own
+// fp32 partial sums, added in split order by the pass after the kernel.
 // The producer decodes each tile once and publishes it in the shared ring, so the
 // MMA and epilogue warps never wait on the global routing metadata.
 constexpr int kMaxBlockRuns = 256;   // runs of one block <= its rows <= 256
 struct TileHdr {
   int tau;                // tile id; >= the live count ends the CTA's loop
   int b, e, row0, f0;
-  int run0, nruns;        // adapter runs of the block (first K split only)
+  int run0, nruns;        // adapter runs of the block (last K split only)
   int kb0, nk;            // base K-tiles of this split
   int n_it;               // pipeline stages of this tile
   int srun, sa, snch;     // kShrink: run, adapter, rank chunks
@@ -167,7 +168,9 @@ __device__ __forceinline__ TileHdr decode_tile(int tau, const GemmParams& prm, u
     const int ks = rest / nb;
     t.ks = ks;
     t.f0 = ft * (MODE == kGateUp ? 128 : 256);
-    if (ks == 0) {
+    // The LoRA K-steps ride on the last K split: its tiles come last in the tile order,
+    // so they reach the S tiles after the shrink kernel before has finished.
+    if (ks == prm.ksplit - 1) {
       t.run0 = prm.block_runs[t.b];
       t.nruns = prm.block_runs[t.b + 1] - t.run0;
     }
