@@ -94,7 +94,10 @@ cudaError_t launch_align(const AlignLaunch& a, cudaStream_t s);
 cudaError_t launch_route_align_small(const AlignLaunch& a, const float* logits, float* topk_w, int32_t* topk_ids,
                                      cudaStream_t s);
 
-// Gathers x rows into sorted order, records the sorted row of every placed pair in
+// Whether the gather copies in token order (a second launch that reads each x row once).
+inline bool gather_token_order(int64_t T, int H) { return T * static_cast<int64_t>(H) * 2 > (int64_t(64) << 20); }
+// Gathers x rows into sorted order (in token order when gather_token_order), records
+// the sorted row of every placed pair in
 // pair_row [T*k], and zeroes *status and the n_ctr tile counters of the forward's
 // GEMM launches.
 cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* sorted_p, const int32_t* totals, int64_t max_rows,

@@ -61,8 +61,10 @@ struct GemmCfg {
   static constexpr int W_BYTES = WROWS * ROWB;
   static constexpr int T_BYTES = TROWS * ROWB;
   static constexpr int STAGE_BYTES = W_BYTES + T_BYTES;
+  // (16-token weight-streaming tiles: 3 stages, so two CTAs share an SM and a GEMM CTA
+  // fits beside a shrink CTA -- measured faster on the decode shapes; 32/64: 5)
   static constexpr int STAGES = MODE == kShrink ? 4
-                                : SWAP           ? (BT <= 16 ? 6 : 5)
+                                : SWAP           ? (BT <= 16 ? 3 : 5)
                                                  : (192 * 1024) / STAGE_BYTES;
   // accumulators: non-swapped MT tiles of M=128 tokens x N; swapped NH tiles of 128 x BT
   static constexpr int NH = MODE == kShrink ? 1 : 2;

@@ -670,7 +670,10 @@ int moe_lora_plan_query(const moe_lora_dims* d, moe_lora_plan* out) {
       return fail(MOE_LORA_EUNSUPPORTED, "no GEMM compiled for block_m = %d", d->block_m);
   const int64_t P = d->T * d->k;
   p.launches_route_align = (P > 0 && P <= 4096) ? 1 : (P == 0 ? 1 : 4);
-  p.launches_forward = d->T == 0 ? 0 : 4 + (lora ? 2 : 0) + (l.ks_gu > 1 ? 1 : 0);
+  // gather (+ its token-order copy when x outgrows L2), shrinks, gate_up (+ SiLU pass
+  // after a K split), down, combine
+  p.launches_forward =
+      d->T == 0 ? 0 : 4 + (moe::gather_token_order(d->T, d->H) ? 1 : 0) + (lora ? 2 : 0) + (l.ks_gu > 1 ? 1 : 0);
   *out = p;
   return MOE_LORA_OK;
 }

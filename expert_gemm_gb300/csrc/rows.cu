@@ -8,15 +8,15 @@
 namespace moe {
 namespace {
 
-// x_sorted[row] = x[sorted_p[row] / k] for real rows, zero for padding rows; one warp
-// per row, 16-byte vectors.  Lane 0 records pair_row[p] = row for the combine.  The
-// same launch zeroes the call's device status word and the GEMMs' tile counters, so
-// the forward needs no memset nodes.
+// One warp per sorted row: lane 0 records pair_row[p] = row (for the combine and the
+// token-order copy), padding rows are zeroed, and with copy_rows the real rows get
+// x[sorted_p[row] / k] (16-byte vectors).  The same launch zeroes the call's device
+// status word and the GEMMs' tile counters, so the forward needs no memset nodes.
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ sorted_p,
                                                           const int32_t* __restrict__ totals, int64_t max_rows, int vec_per_row,
                                                           int k, int P, uint4* __restrict__ xs,
                                                           int32_t* __restrict__ pair_row, int32_t* __restrict__ status,
-                                                          int32_t* __restrict__ ctr, int n_ctr) {
+                                                          int32_t* __restrict__ ctr, int n_ctr, bool copy_rows) {
   pdl_trigger();   // the next kernel waits for this grid before reading what it writes
   const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t nthr = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -31,6 +31,7 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
     for (int v = lane; v < vec_per_row; v += 32) dst[v] = make_uint4(0, 0, 0, 0);
   } else {
     if (lane == 0) pair_row[p] = static_cast<int32_t>(row);
+    if (!copy_rows) return;
     const uint4* src = x + static_cast<int64_t>(p / k) * vec_per_row;
     int v = lane;
     for (; v + 96 < vec_per_row; v += 128) {   // four loads in flight per lane
@@ -41,6 +42,50 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
       dst[v + 96] = d;
     }
     for (; v < vec_per_row; v += 32) dst[v] = __ldg(src + v);
+  }
+}
+
+// Token order: one warp per token reads x[t] once and writes it to the sorted row of
+// each of its pairs (the sorted order puts a token's k copies far apart, so the row
+// order would read x from DRAM k times).  A pair's row is trusted only if the sorted
+// order holds the pair there.
+__global__ void __launch_bounds__(256) copy_tokens_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ pair_row,
+                                                          const int32_t* __restrict__ sorted_p,
+                                                          const int32_t* __restrict__ totals, int64_t T, int k,
+                                                          int vec_per_row, uint4* __restrict__ xs) {
+  __shared__ int32_t s_rows[8][MOE_LORA_MAX_TOPK];   // 256 threads: 8 warps
+  pdl_wait();      // pair_row of this call is complete
+  pdl_trigger();
+  const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + wib;
+  if (t >= T) return;
+  int r = -1;
+  if (lane < k) {
+    const int64_t p = t * k + lane;
+    r = pair_row[p];
+    if (r < 0 || r >= totals[0] || sorted_p[r] != p) r = -1;
+  }
+  // the token's rows, gathered while all lanes are converged; the copy loops below
+  // run a lane-dependent number of steps and read them from shared memory
+  const unsigned valid = __ballot_sync(0xffffffffu, r >= 0);
+  if (r >= 0) s_rows[wib][__popc(valid & ((1u << lane) - 1u))] = r;
+  __syncwarp();
+  const int n = __popc(valid);
+  const uint4* src = x + t * vec_per_row;
+  int v = lane;
+  for (; v + 96 < vec_per_row; v += 128) {   // four loads in flight per lane
+    const uint4 a = __ldg(src + v), b = __ldg(src + v + 32), c = __ldg(src + v + 64), d = __ldg(src + v + 96);
+    for (int j = 0; j < n; ++j) {
+      uint4* dst = xs + static_cast<int64_t>(s_rows[wib][j]) * vec_per_row;
+      dst[v] = a;
+      dst[v + 32] = b;
+      dst[v + 64] = c;
+      dst[v + 96] = d;
+    }
+  }
+  for (; v < vec_per_row; v += 32) {
+    const uint4 a = __ldg(src + v);
+    for (int j = 0; j < n; ++j) xs[static_cast<int64_t>(s_rows[wib][j]) * vec_per_row + v] = a;
   }
 }
 
@@ -56,6 +101,59 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4& v, float* f) {
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
   __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Columns c, c + 32, ... (U groups of 8) of token t: the sum over its n valid pairs in
+// ascending order of w_j * d_j, d_j the pair's row (bf16) or the sum of its K-split
+// fp32 partials in split order.
+template <bool SPLIT, int U>
+__device__ __forceinline__ void combine_cols(const void* __restrict__ y, int ksplit, int64_t part_rows, int H8,
+                                             const int32_t* rows, const float* ws, int n, int c, int64_t t,
+                                             uint4* __restrict__ out) {
+  float acc[U][8];
+#pragma unroll
+  for (int u = 0; u < U; ++u)
+#pragma unroll
+    for (int q = 0; q < 8; ++q) acc[u][q] = 0.f;
+  for (int j0 = 0; j0 < n; j0 += 4) {
+    float d[U][4][8];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) d[u][q4][q] = 0.f;
+        if (j0 + q4 < n) {
+          const int64_t rr = rows[j0 + q4];
+          const int cc = c + 32 * u;
+          if constexpr (!SPLIT) {
+            unpack_bf16x8(__ldg(reinterpret_cast<const uint4*>(y) + rr * H8 + cc), d[u][q4]);
+          } else {
+            for (int sp = 0; sp < ksplit; ++sp) {
+              const float4* src = reinterpret_cast<const float4*>(y) + ((sp * part_rows + rr) * H8 + cc) * 2;
+              const float4 a = __ldcg(src), b = __ldcg(src + 1);
+              d[u][q4][0] += a.x; d[u][q4][1] += a.y; d[u][q4][2] += a.z; d[u][q4][3] += a.w;
+              d[u][q4][4] += b.x; d[u][q4][5] += b.y; d[u][q4][6] += b.z; d[u][q4][7] += b.w;
+            }
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) {
+      if (j0 + q4 < n) {
+        const float w = ws[j0 + q4];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+#pragma unroll
+          for (int q = 0; q < 8; ++q) acc[u][q] += w * d[u][q4][q];
+      }
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < U; ++u)
+    out[t * H8 + c + 32 * u] = make_uint4(pack2(acc[u][0], acc[u][1]), pack2(acc[u][2], acc[u][3]),
+                                          pack2(acc[u][4], acc[u][5]), pack2(acc[u][6], acc[u][7]));
 }
 
 // One warp per (token, column slab): lanes j < k look up the token's pairs -- a pair's
@@ -101,40 +199,9 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const void* __
   const int n = __popc(valid);
   const int per = (H8 + ns - 1) / ns;
   const int c_end = min(H8, (slab + 1) * per);
-  for (int c = slab * per + lane; c < c_end; c += 32) {
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int j0 = 0; j0 < n; j0 += 4) {
-      float d[4][8];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-#pragma unroll
-        for (int q = 0; q < 8; ++q) d[u][q] = 0.f;
-        if (j0 + u < n) {
-          const int64_t rr = s_row[wib][j0 + u];
-          if constexpr (!SPLIT) {
-            unpack_bf16x8(__ldg(reinterpret_cast<const uint4*>(y) + rr * H8 + c), d[u]);
-          } else {
-            for (int sp = 0; sp < ksplit; ++sp) {
-              const float4* src = reinterpret_cast<const float4*>(y) + ((sp * part_rows + rr) * H8 + c) * 2;
-              const float4 a = __ldcg(src), b = __ldcg(src + 1);
-              d[u][0] += a.x; d[u][1] += a.y; d[u][2] += a.z; d[u][3] += a.w;
-              d[u][4] += b.x; d[u][5] += b.y; d[u][6] += b.z; d[u][7] += b.w;
-            }
-          }
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        if (j0 + u < n) {
-          const float wu = s_w[wib][j0 + u];
-#pragma unroll
-          for (int q = 0; q < 8; ++q) acc[q] += wu * d[u][q];
-        }
-      }
-    }
-    out[t * H8 + c] = make_uint4(pack2(acc[0], acc[1]), pack2(acc[2], acc[3]), pack2(acc[4], acc[5]),
-                                 pack2(acc[6], acc[7]));
-  }
+  // (one column group per step: two per step, more loads in flight, measured slower)
+  for (int c = slab * per + lane; c < c_end; c += 32)
+    combine_cols<SPLIT, 1>(y, ksplit, part_rows, H8, s_row[wib], s_w[wib], n, c, t, out);
 }
 
 }  // namespace
@@ -145,10 +212,27 @@ cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* sorted_p, const
   const int rows_per_cta = 8;
   int64_t grid = (max_rows + rows_per_cta - 1) / rows_per_cta;
   if (grid < 1) grid = 1;
+  // When x is larger than half the 129 MB L2, its k re-reads in sorted-row order come
+  // from DRAM: copy in token order then (x read once).  Otherwise one row-order pass.
+  const bool token_order = gather_token_order(P / k, H);
   gather_rows_kernel<<<static_cast<unsigned>(grid), rows_per_cta * 32, 0, s>>>(
       reinterpret_cast<const uint4*>(x), sorted_p, totals, max_rows, H / 8, k, P, reinterpret_cast<uint4*>(x_sorted),
-      pair_row, status, ctr, n_ctr);
-  return cudaGetLastError();
+      pair_row, status, ctr, n_ctr, !token_order);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess || !token_order) return err;
+  const int64_t T = P / k;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((T + 7) / 8), 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, copy_tokens_kernel, reinterpret_cast<const uint4*>(x),
+                            static_cast<const int32_t*>(pair_row), sorted_p, totals, T, k, H / 8,
+                            reinterpret_cast<uint4*>(x_sorted));
 }
 
 namespace {

@@ -75,7 +75,7 @@ def test_prefill_plan():
     assert p["stages"]["gate_up"] == 6 and p["stages"]["down"] == 6   # 32 KB stages of a CTA pair
     assert p["ksplit"] == {"shrink_gu": 1, "gate_up": 1, "shrink_dn": 1, "down": 1}
     assert p["launches_route_align"] == 4  # 102400 pairs: route, then chunk/scan/scatter
-    assert p["launches_forward"] == 6
+    assert p["launches_forward"] == 7      # the gather copies in token order: a second launch
 
 
 def test_split_plans():
