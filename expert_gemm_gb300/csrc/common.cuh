@@ -33,6 +33,7 @@ constexpr int kRankChunk = 16;  // LoRA rank elements per MMA K-step
 // Parameters of one grouped-GEMM launch (passed by value, read-only on the device).
 struct GemmParams {
   const int32_t* block_expert;  // [blocks]
+  const int32_t* expert_begin;  // [E+1] first sorted row of each expert
   const int32_t* block_runs;    // [blocks+1]
   const int32_t* runs;          // [runs][4] {block, adapter, begin, end}
   const int32_t* totals;        // {rows, blocks, runs, dropped}

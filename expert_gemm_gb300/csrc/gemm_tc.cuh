@@ -143,7 +143,8 @@ __device__ __forceinline__ int live_tiles(const GemmParams& prm) {
 }
 
 template <int MODE, bool SWAP, int BT>
-__device__ __forceinline__ TileHdr decode_tile(int tau, const GemmParams& prm, uint8_t* nch_out, int16_t* ad_out) {
+__device__ __forceinline__ TileHdr decode_tile(int tau, const GemmParams& prm, uint8_t* nch_out, int16_t* ad_out,
+                                               int workers) {
   using C = GemmCfg<MODE, SWAP, BT>;
   TileHdr t;
   t.tau = tau;
@@ -163,11 +164,34 @@ __device__ __forceinline__ TileHdr decode_tile(int tau, const GemmParams& prm, u
     t.nk = (t.ks + 1) * nk_all / prm.ksplit - t.kb0;
     t.n_it = t.nk;
   } else {
+    // Order: K split slowest; then expert by expert; inside an expert, groups of G
+    // feature tiles, and inside a group block-major.  The blocks of one expert then
+    // share each group's weight tiles while they are resident in L2 (an expert's whole
+    // weight matrix can exceed L2); G * (the expert's blocks) ~ the concurrent workers.
+    // One block per expert (decode) gives G = n_ft: feature tile fastest.
     const int nb = prm.totals[1];
-    const int ft = tau % prm.n_ft;
-    const int rest = tau / prm.n_ft;
-    t.b = rest % nb;
-    const int ks = rest / nb;
+    const int per_split = nb * prm.n_ft;
+    const int ks = tau / per_split;
+    const int rest = tau - ks * per_split;
+    const int e = prm.block_expert[rest / prm.n_ft];   // an expert's tiles are its blocks' tiles
+    const int blk0 = prm.expert_begin[e] / BT;
+    const int nbe = prm.expert_begin[e + 1] / BT - blk0;
+    const int local = rest - blk0 * prm.n_ft;
+    int G = workers / nbe;
+    if (G < 1) G = 1;
+    if (G > prm.n_ft) G = prm.n_ft;
+    const int full = (prm.n_ft / G) * G;           // feature tiles in whole groups
+    int ft, bl;
+    if (local < full * nbe) {
+      const int g = local / (G * nbe), r = local - g * (G * nbe);
+      bl = r / G;
+      ft = g * G + (r - bl * G);
+    } else {
+      const int Gl = prm.n_ft - full, r = local - full * nbe;
+      bl = r / Gl;
+      ft = full + (r - bl * Gl);
+    }
+    t.b = blk0 + bl;
     t.ks = ks;
     t.f0 = ft * (MODE == kGateUp ? 128 : 256);
     // The LoRA K-steps ride on the last K split: its tiles come last in the tile order,
@@ -290,7 +314,9 @@ __global__ void __launch_bounds__(192, 1)
         }
         TileHdr t;
         t.tau = n_live;
-        if (tau < n_live) t = decode_tile<MODE, SWAP, BT>(tau, prm, bars->tiles[slot].nch, bars->tiles[slot].ad);
+        if (tau < n_live)
+          t = decode_tile<MODE, SWAP, BT>(tau, prm, bars->tiles[slot].nch, bars->tiles[slot].ad,
+                                          C::CTA2 ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x));
         bars->tiles[slot].h = t;
         mbar_arrive(&bars->sched_full[slot]);   // release: the tile fields are visible to the readers
         if (tau >= n_live) break;

@@ -513,6 +513,7 @@ int do_forward(const moe_lora_dims* d, const uint16_t* x, const float* topk_w, c
 
   moe::GemmParams p{};
   p.block_expert = al->block_expert;
+  p.expert_begin = al->expert_begin;
   p.block_runs = al->block_runs;
   p.runs = al->runs;
   p.totals = al->totals;
