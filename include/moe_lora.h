@@ -127,7 +127,7 @@ int moe_lora_workspace_size(const moe_lora_dims *d, size_t *align_bytes, size_t 
 
 /* The compiled-in tile table's block_m for T*k pairs over E experts: the shape class
  * is the pairs per expert T*k/E (16, 32, 64 weight-streaming up to 10, 24, 95 pairs per
- * expert; 128 token-tiled up to 511; 256, token-tiled on CTA pairs, above).  The pages pick tuned tile configurations per shape
+ * expert; 128 token-tiled up to 2047; 256, token-tiled on CTA pairs, above).  The pages pick tuned tile configurations per shape
  * ([AWS] "Tuning kernel configurations for Amazon SageMaker AI and Amazon Bedrock";
  * [KO] "Amazon 전용 튜닝"). */
 int32_t moe_lora_pick_block_m(int64_t T, int32_t k, int32_t E);

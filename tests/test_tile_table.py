@@ -23,7 +23,7 @@ def lib():
 
 
 # (name, block_m the table must pick)
-EXPECTED = [("tiny", 32), ("decode", 16), ("prefill", 256), ("wide", 256), ("dense_decode", 32),
+EXPECTED = [("tiny", 32), ("decode", 16), ("prefill", 256), ("wide", 128), ("dense_decode", 32),
             ("sweep_T1", 16), ("sweep_T16", 16), ("sweep_T256", 32), ("sweep_T4096", 128)]
 
 
@@ -37,9 +37,9 @@ def test_class_of_each_workload(name, bm):
 
 
 def test_class_boundaries():
-    """Pairs per expert above 10, 24, 95 and 511 move to the next row."""
+    """Pairs per expert above 10, 24, 95 and 2047 move to the next row."""
     E, k = 8, 1
-    for ppe, bm in [(1, 16), (10, 16), (11, 32), (24, 32), (25, 64), (95, 64), (96, 128), (511, 128), (512, 256),
+    for ppe, bm in [(1, 16), (10, 16), (11, 32), (24, 32), (25, 64), (95, 64), (96, 128), (2047, 128), (2048, 256),
                     (5000, 256)]:
         assert ml.pick_block_m(ppe * E, k, E) == bm, (ppe, bm)
     assert ml.pick_block_m(0, 1, 8) == 16
