@@ -236,12 +236,8 @@ FwdLayout fwd_layout(const moe_lora_dims* d) {
 }
 
 // ---- tensor maps
-// promo: L2 sector promotion of the map's loads.  Maps whose rows are read whole use
-// 256-byte promotion; the LoRA expand reads 16 ranks (32 bytes) of each r_max-wide row
-// of Bt and of the S tiles, where promotion would fetch the unused ranks too.
 int encode(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims, const uint64_t* strides,
-           const uint32_t* box, CUtensorMapSwizzle sw, const char* what,
-           CUtensorMapL2promotion promo = CU_TENSOR_MAP_L2_PROMOTION_L2_256B) {
+           const uint32_t* box, CUtensorMapSwizzle sw, const char* what) {
   cuuint64_t gd[5];
   cuuint64_t gs[4];
   cuuint32_t bx[5], es[5];
@@ -252,7 +248,7 @@ int encode(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims, cons
   }
   for (int i = 0; i < rank - 1; ++i) gs[i] = strides[i];
   CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), gd, gs, bx, es,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, sw, promo,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(MOE_LORA_ECUDA, "cuTensorMapEncodeTiled(%s) failed with %d", what, (int)r);
   return MOE_LORA_OK;
@@ -495,18 +491,18 @@ int do_forward(const moe_lora_dims* d, const uint16_t* x, const float* topk_w, c
     {
       const uint64_t dm[4] = {R, I, 2, LE}, st[3] = {R * 2, I * R * 2, 2 * I * R * 2};
       const uint32_t bx[4] = {16, 128, 1, 1};
-      MOE_TRY(encode(&m_gu.lw, Bt_gu, 4, dm, st, bx, CU_TENSOR_MAP_SWIZZLE_32B, "Bt_gu", CU_TENSOR_MAP_L2_PROMOTION_NONE));
+      MOE_TRY(encode(&m_gu.lw, Bt_gu, 4, dm, st, bx, CU_TENSOR_MAP_SWIZZLE_32B, "Bt_gu"));
     }
     {
       const uint64_t dm[3] = {R, H, LE}, st[2] = {R * 2, H * R * 2};
       const uint32_t bx[3] = {16, 128, 1};
-      MOE_TRY(encode(&m_dn.lw, Bt_dn, 3, dm, st, bx, CU_TENSOR_MAP_SWIZZLE_32B, "Bt_dn", CU_TENSOR_MAP_L2_PROMOTION_NONE));
+      MOE_TRY(encode(&m_dn.lw, Bt_dn, 3, dm, st, bx, CU_TENSOR_MAP_SWIZZLE_32B, "Bt_dn"));
     }
     {
       const uint64_t dm[3] = {RP, (uint64_t)BT, nruns}, st[2] = {RP * 2, (uint64_t)BT * RP * 2};
       const uint32_t bx[3] = {16, tok_rows, 1};
-      MOE_TRY(encode(&m_gu.ls, sgu, 3, dm, st, bx, CU_TENSOR_MAP_SWIZZLE_32B, "S_gu", CU_TENSOR_MAP_L2_PROMOTION_NONE));
-      MOE_TRY(encode(&m_dn.ls, sdn, 3, dm, st, bx, CU_TENSOR_MAP_SWIZZLE_32B, "S_dn", CU_TENSOR_MAP_L2_PROMOTION_NONE));
+      MOE_TRY(encode(&m_gu.ls, sgu, 3, dm, st, bx, CU_TENSOR_MAP_SWIZZLE_32B, "S_gu"));
+      MOE_TRY(encode(&m_dn.ls, sdn, 3, dm, st, bx, CU_TENSOR_MAP_SWIZZLE_32B, "S_dn"));
     }
   } else {
     // No adapter runs exist, so these maps are never loaded through; keep them valid.
