@@ -119,8 +119,40 @@ def test_no_adapter_anywhere(ml, torch, oracle):
 
 def test_zero_adapters_L0(ml, torch, oracle):
     wl = W.custom(name="l0", T=48, H=256, I=256, E=4, k=2, L=0, ranks=(), lora_mode="none")
-    run_case(ml, torch, oracle, wl, block_m=16)
-    run_case(ml, torch, oracle, wl, block_m=128)
+    for bm in (16, 128, 256):
+        run_case(ml, torch, oracle, wl, block_m=bm)
+
+
+def test_token_order_gather(ml, torch, oracle):
+    """x larger than half the L2 (82 MB): the gather copies in token order in a second
+    launch.  Ragged T, several blocks per expert, adapters and no-adapter tokens;
+    sampled outputs against the oracle, the align whole."""
+    wl = W.custom(name="bigx", T=20011, H=2048, I=256, E=8, k=2, L=3, ranks=(16, 32, 8),
+                  lora_mode="uniform_with_none")
+    assert ml.plan(dims_of(wl, 0, ml))["launches_forward"] == 7   # gather + token-order copy + ...
+    for bm in (128, 256):
+        run_case(ml, torch, oracle, wl, block_m=bm, tokens=sample_tokens(wl.T, 48))
+
+
+def test_cta_pair_invalid_ids(ml, torch, oracle):
+    """256-row blocks (CTA pairs) with dropped pairs: stale pair records are rejected."""
+    wl = W.custom(name="bad256", T=700, H=256, I=384, E=3, k=2, L=3, ranks=(16, 16, 32), lora_mode="uniform_with_none")
+    logits, lora, x, w = inputs(wl)
+    ids, tw = oracle.route(logits, wl.k)
+    ids[3, 0] = -1
+    ids[600, 1] = wl.E
+    lora = lora.copy()
+    lora[7] = wl.L
+    d = dims_of(wl, 256, ml)
+    layer = ml.Layer(d, dev_weights(w, torch))
+    ml.align(d, to_dev(ids, torch), to_dev(lora, torch), layer.bufs, layer.ws_align)
+    ml.forward(d, to_dev(x, torch), to_dev(tw.astype(np.float32), torch), layer.bufs, layer.w, layer.out,
+               layer.ws_fwd, layer.status)
+    torch.cuda.synchronize()
+    assert int(layer.status.item()) == 0
+    assert_align_equal(align_to_numpy(layer.bufs), oracle.align(ids, lora, wl.E, wl.L, 256))
+    ref = oracle.forward(x, ids, tw.astype(np.float32), lora, w)
+    assert parity_error(layer.out.float().cpu().numpy(), ref)[0] <= TOL
 
 
 def test_all_tokens_one_expert(ml, torch, oracle):
