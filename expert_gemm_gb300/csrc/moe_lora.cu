@@ -14,6 +14,7 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <new>
 
 #include "common.cuh"
 
@@ -732,11 +733,16 @@ int moe_lora_forward(const moe_lora_dims* d, const uint16_t* x, const float* top
                     dev_status, static_cast<cudaStream_t>(stream), stage_events);
 }
 
-int moe_lora_layer_host(const moe_lora_dims* d, const float* logits_host, const int32_t* lora_ids_host,
-                        const uint16_t* x_host, const uint16_t* W_gu, const uint16_t* W_dn, const uint16_t* A_gu,
-                        const uint16_t* Bt_gu, const uint16_t* A_dn, const uint16_t* Bt_dn, uint16_t* out_host,
-                        void* workspace, size_t workspace_bytes, int64_t* dropped, void* stream) {
-  MOE_RESOLVE(d);
+}  // extern "C"
+
+namespace {
+// Enqueues the layer_host sequence on s without synchronising: copies in, route+align,
+// forward, out and (status, totals) back.  status_dst/totals_dst: host destinations.
+int layer_enqueue(const moe_lora_dims* d, const float* logits_host, const int32_t* lora_ids_host,
+                  const uint16_t* x_host, const uint16_t* W_gu, const uint16_t* W_dn, const uint16_t* A_gu,
+                  const uint16_t* Bt_gu, const uint16_t* A_dn, const uint16_t* Bt_dn, uint16_t* out_host,
+                  void* workspace, size_t workspace_bytes, int32_t* status_dst, int32_t* totals_dst,
+                  cudaStream_t s) {
   MOE_TRY(validate_dims(d));
   const LayerLayout l = layer_layout(d);
   MOE_TRY(check_ptr(workspace, "workspace", true));
@@ -747,7 +753,6 @@ int moe_lora_layer_host(const moe_lora_dims* d, const float* logits_host, const 
     MOE_TRY(check_ptr(x_host, "x_host", false));
     MOE_TRY(check_ptr(out_host, "out_host", false));
   }
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* b = static_cast<uint8_t*>(workspace);
   float* logits = reinterpret_cast<float*>(b + l.logits);
   int32_t* lora = reinterpret_cast<int32_t*>(b + l.lora);
@@ -770,13 +775,91 @@ int moe_lora_layer_host(const moe_lora_dims* d, const float* logits_host, const 
   }
   MOE_TRY(do_forward(d, x, w, &al, W_gu, W_dn, A_gu, Bt_gu, A_dn, Bt_dn, out, b + l.fwd, l.logits - l.fwd, status, s,
                       nullptr));
-  int32_t host_status = 0, tot[4] = {0, 0, 0, 0};
   if (T > 0) MOE_CUDA(cudaMemcpyAsync(out_host, out, T * d->H * 2, cudaMemcpyDeviceToHost, s));
-  MOE_CUDA(cudaMemcpyAsync(&host_status, status, 4, cudaMemcpyDeviceToHost, s));
-  MOE_CUDA(cudaMemcpyAsync(tot, al.totals, 16, cudaMemcpyDeviceToHost, s));
+  MOE_CUDA(cudaMemcpyAsync(status_dst, status, 4, cudaMemcpyDeviceToHost, s));
+  MOE_CUDA(cudaMemcpyAsync(totals_dst, al.totals, 16, cudaMemcpyDeviceToHost, s));
+  return MOE_LORA_OK;
+}
+}  // namespace
+
+struct moe_lora_graph {
+  cudaGraphExec_t exec = nullptr;
+  int32_t* status_host = nullptr;   // [0] device status, [4..7] align totals
+};
+
+extern "C" {
+
+int moe_lora_layer_host(const moe_lora_dims* d, const float* logits_host, const int32_t* lora_ids_host,
+                        const uint16_t* x_host, const uint16_t* W_gu, const uint16_t* W_dn, const uint16_t* A_gu,
+                        const uint16_t* Bt_gu, const uint16_t* A_dn, const uint16_t* Bt_dn, uint16_t* out_host,
+                        void* workspace, size_t workspace_bytes, int64_t* dropped, void* stream) {
+  MOE_RESOLVE(d);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t host_status = 0, tot[4] = {0, 0, 0, 0};
+  MOE_TRY(layer_enqueue(d, logits_host, lora_ids_host, x_host, W_gu, W_dn, A_gu, Bt_gu, A_dn, Bt_dn, out_host,
+                        workspace, workspace_bytes, &host_status, tot, s));
   MOE_CUDA(cudaStreamSynchronize(s));
   if (dropped) *dropped = tot[3];
   if (host_status != 0) return fail(MOE_LORA_EDEVICE, "device status 0x%x", host_status);
+  return MOE_LORA_OK;
+}
+
+int moe_lora_layer_graph_create(const moe_lora_dims* d, const float* logits_host, const int32_t* lora_ids_host,
+                                const uint16_t* x_host, const uint16_t* W_gu, const uint16_t* W_dn,
+                                const uint16_t* A_gu, const uint16_t* Bt_gu, const uint16_t* A_dn,
+                                const uint16_t* Bt_dn, uint16_t* out_host, int32_t* status_host, void* workspace,
+                                size_t workspace_bytes, void* stream, moe_lora_graph** graph) {
+  MOE_RESOLVE(d);
+  if (!graph) return fail(MOE_LORA_EINVAL, "graph is NULL");
+  *graph = nullptr;
+  MOE_TRY(check_ptr(status_host, "status_host", false));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (!s) return fail(MOE_LORA_EINVAL, "graph capture needs a non-default stream");
+  // one eager run: validation and the kernels' one-time set-up happen outside the capture
+  MOE_TRY(layer_enqueue(d, logits_host, lora_ids_host, x_host, W_gu, W_dn, A_gu, Bt_gu, A_dn, Bt_dn, out_host,
+                        workspace, workspace_bytes, status_host, status_host + 4, s));
+  MOE_CUDA(cudaStreamSynchronize(s));
+  if (status_host[0] != 0) return fail(MOE_LORA_EDEVICE, "device status 0x%x", status_host[0]);
+  cudaGraph_t g = nullptr;
+  MOE_CUDA(cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal));
+  const int st = layer_enqueue(d, logits_host, lora_ids_host, x_host, W_gu, W_dn, A_gu, Bt_gu, A_dn, Bt_dn, out_host,
+                               workspace, workspace_bytes, status_host, status_host + 4, s);
+  const cudaError_t ce = cudaStreamEndCapture(s, &g);
+  if (st != MOE_LORA_OK) {
+    if (g) cudaGraphDestroy(g);
+    return st;
+  }
+  if (ce != cudaSuccess) return cuda_fail(ce, "cudaStreamEndCapture");
+  cudaGraphExec_t exec = nullptr;
+  const cudaError_t ie = cudaGraphInstantiate(&exec, g, 0);
+  cudaGraphDestroy(g);
+  if (ie != cudaSuccess) return cuda_fail(ie, "cudaGraphInstantiate");
+  moe_lora_graph* h = new (std::nothrow) moe_lora_graph;
+  if (!h) {
+    cudaGraphExecDestroy(exec);
+    return fail(MOE_LORA_EINVAL, "out of host memory");
+  }
+  h->exec = exec;
+  h->status_host = status_host;
+  *graph = h;
+  return MOE_LORA_OK;
+}
+
+int moe_lora_layer_graph_run(moe_lora_graph* graph, void* stream, int64_t* dropped) {
+  if (!graph || !graph->exec) return fail(MOE_LORA_EINVAL, "graph is NULL");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  MOE_CUDA(cudaGraphLaunch(graph->exec, s));
+  MOE_CUDA(cudaStreamSynchronize(s));
+  if (dropped) *dropped = graph->status_host[4 + 3];
+  if (graph->status_host[0] != 0) return fail(MOE_LORA_EDEVICE, "device status 0x%x", graph->status_host[0]);
+  return MOE_LORA_OK;
+}
+
+int moe_lora_layer_graph_destroy(moe_lora_graph* graph) {
+  if (!graph) return MOE_LORA_OK;
+  cudaError_t e = graph->exec ? cudaGraphExecDestroy(graph->exec) : cudaSuccess;
+  delete graph;
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGraphExecDestroy");
   return MOE_LORA_OK;
 }
 

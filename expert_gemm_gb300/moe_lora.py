@@ -23,7 +23,8 @@ MAX_ADAPTERS, MAX_RANK, MAX_EXPERTS, MAX_TOPK = 256, 64, 1024, 32
 EXPORTS = ["moe_lora_align_capacity", "moe_lora_workspace_size", "moe_lora_pick_block_m", "moe_lora_route",
            "moe_lora_align", "moe_lora_forward", "moe_lora_layer_workspace_size", "moe_lora_layer_host",
            "moe_lora_status_string", "moe_lora_last_error", "moe_lora_version", "moe_lora_align_static",
-           "moe_lora_route_align", "moe_lora_plan_query"]
+           "moe_lora_route_align", "moe_lora_plan_query", "moe_lora_layer_graph_create",
+           "moe_lora_layer_graph_run", "moe_lora_layer_graph_destroy"]
 STATIC_SCRATCH_BYTES = 4 << 20
 
 
@@ -75,6 +76,10 @@ def load(path: str = LIB_PATH):
     lib.moe_lora_align_static.argtypes = [DP, vp, vp, AP, vp]
     lib.moe_lora_route_align.argtypes = [DP, vp, vp, vp, vp, AP, vp, sz, vp]
     lib.moe_lora_plan_query.argtypes = [DP, C.POINTER(Plan)]
+    lib.moe_lora_layer_graph_create.argtypes = [DP, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp,
+                                                C.POINTER(vp)]
+    lib.moe_lora_layer_graph_run.argtypes = [vp, vp, C.POINTER(i64)]
+    lib.moe_lora_layer_graph_destroy.argtypes = [vp]
     lib.moe_lora_forward.argtypes = [DP, vp, vp, AP, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp, vp]
     lib.moe_lora_layer_host.argtypes = [DP, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, C.POINTER(i64), vp]
     lib.moe_lora_status_string.restype = C.c_char_p
@@ -83,7 +88,8 @@ def load(path: str = LIB_PATH):
     lib.moe_lora_version.restype = C.c_int
     for name in ("moe_lora_align_capacity", "moe_lora_workspace_size", "moe_lora_layer_workspace_size",
                  "moe_lora_route", "moe_lora_align", "moe_lora_forward", "moe_lora_layer_host",
-                 "moe_lora_align_static", "moe_lora_route_align", "moe_lora_plan_query"):
+                 "moe_lora_align_static", "moe_lora_route_align", "moe_lora_plan_query",
+                 "moe_lora_layer_graph_create", "moe_lora_layer_graph_run", "moe_lora_layer_graph_destroy"):
         getattr(lib, name).restype = C.c_int
     _lib = lib
     return lib
@@ -241,6 +247,43 @@ def layer_host(d: LayerDims, logits_host, lora_ids_host, x_host, w: dict, out_ho
     return dropped.value
 
 
+class LayerGraph:
+    """moe_lora_layer_graph_*: the host-to-host layer captured once, replayed per step.
+
+    Host buffers must be pinned and stay put; each run() reads their current contents.
+    """
+
+    def __init__(self, d: LayerDims, logits_host, lora_ids_host, x_host, w: dict, out_host, workspace, stream):
+        import torch
+        self.status_host = torch.zeros(8, dtype=torch.int32).pin_memory()
+        self.stream = stream
+        self._keep = (logits_host, lora_ids_host, x_host, out_host, workspace, w)
+        h = C.c_void_p()
+        _check(load().moe_lora_layer_graph_create(
+            C.byref(d.c()), _ptr(logits_host), _ptr(lora_ids_host), _ptr(x_host), _ptr(w["W_gu"]), _ptr(w["W_dn"]),
+            _ptr(w.get("A_gu")), _ptr(w.get("Bt_gu")), _ptr(w.get("A_dn")), _ptr(w.get("Bt_dn")), _ptr(out_host),
+            _ptr(self.status_host), _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream),
+            C.byref(h)))
+        self.handle = h
+
+    def run(self) -> int:
+        """One step; returns the dropped-pair count."""
+        dropped = C.c_int64()
+        _check(load().moe_lora_layer_graph_run(self.handle, _stream(self.stream), C.byref(dropped)))
+        return dropped.value
+
+    def close(self):
+        if self.handle:
+            _check(load().moe_lora_layer_graph_destroy(self.handle))
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
 class Layer:
     """One MoE-LoRA layer with device-resident weights and preallocated scratch.
 
@@ -269,6 +312,13 @@ class Layer:
         forward(self.d, x, self.topk_w, self.bufs, self.w, self.out, self.ws_fwd, self.status, stream,
                 stage_events)
         return self.out
+
+    def graph_host(self, logits_host, lora_ids_host, x_host, out_host, stream) -> LayerGraph:
+        """The host-to-host layer as a replayable graph on `stream` (pinned host buffers)."""
+        import torch
+        if self._ws_layer is None:
+            self._ws_layer = torch.empty(layer_workspace_size(self.d), dtype=torch.uint8, device=self.device)
+        return LayerGraph(self.d, logits_host, lora_ids_host, x_host, self.w, out_host, self._ws_layer, stream)
 
     def step_host(self, logits_host, lora_ids_host, x_host, out_host, stream=None) -> int:
         import torch

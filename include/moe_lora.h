@@ -240,6 +240,36 @@ int moe_lora_layer_host(const moe_lora_dims *d, const float *logits_host,
                         int64_t *dropped, void *stream);
 
 /*
+ * The moe_lora_layer_host sequence (host->device copies, route, align, forward,
+ * device->host copies) captured once as a CUDA graph and replayed per step: one
+ * launch instead of three copies, the kernels and two copies issued from the CPU.
+ * The pages capture GPU operation sequences with CUDA graphs to cut kernel-launch
+ * and CPU overhead ([AWS] "Execution optimizations").
+ *   create: same arguments as moe_lora_layer_host, with every host buffer pinned
+ *           (cudaHostAlloc / cudaHostRegister) and status_host an extra pinned int32[8]
+ *           that each run fills with the device status word and the align totals.
+ *           Runs the layer once eagerly (validation, kernel set-up), then captures it
+ *           on `stream`.  *graph receives the handle.
+ *   run:    launches the graph on `stream` and synchronises it; the host buffers'
+ *           CURRENT contents are the step's inputs.  *dropped (may be NULL) receives
+ *           the dropped-pair count; returns MOE_LORA_EDEVICE if the device reported
+ *           a timeout.
+ *   destroy: releases the graph.  Buffers, weights and workspace stay the caller's;
+ *           none of them may move or be freed while the graph exists.
+ */
+typedef struct moe_lora_graph moe_lora_graph;
+int moe_lora_layer_graph_create(const moe_lora_dims *d, const float *logits_host,
+                                const int32_t *lora_ids_host, const uint16_t *x_host,
+                                const uint16_t *W_gu, const uint16_t *W_dn,
+                                const uint16_t *A_gu, const uint16_t *Bt_gu,
+                                const uint16_t *A_dn, const uint16_t *Bt_dn,
+                                uint16_t *out_host, int32_t *status_host,
+                                void *workspace, size_t workspace_bytes, void *stream,
+                                moe_lora_graph **graph);
+int moe_lora_layer_graph_run(moe_lora_graph *graph, void *stream, int64_t *dropped);
+int moe_lora_layer_graph_destroy(moe_lora_graph *graph);
+
+/*
  * moe_lora_align_static: moe_lora_align without a caller-supplied workspace.
  * The pages have no counterpart of this entry point.  It is for callers that cannot
  * allocate device memory when they call: a serving engine that has handed almost all

@@ -302,3 +302,34 @@ def test_layer_host_entry(ml, torch, oracle, name):
     ids, tw = oracle.route(logits, wl.k)
     ref = oracle.forward(x, ids, tw.astype(np.float32), lora, w)
     assert parity_error(y, ref)[0] <= TOL
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode", "sweep_T256"])
+def test_layer_graph_replay(ml, torch, oracle, name):
+    """moe_lora_layer_graph_*: the captured host-to-host layer gives moe_lora_layer_host's
+    bytes, and a replay after new inputs are written into the same pinned buffers
+    computes the new batch."""
+    wl = W.get(name)
+    logits, lora, x, w = inputs(wl)
+    layer = ml.Layer(dims_of(wl, 0, ml), dev_weights(w, torch))
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()   # noqa: E731
+    lg, lr, xh = pin(logits), pin(lora), pin(x.view(np.int16))
+    out_direct = torch.empty((wl.T, wl.H), dtype=torch.int16).pin_memory()
+    layer.step_host(lg, lr, xh, out_direct)
+    out_g = torch.empty((wl.T, wl.H), dtype=torch.int16).pin_memory()
+    stream = torch.cuda.Stream()
+    graph = layer.graph_host(lg, lr, xh, out_g, stream)
+    try:
+        assert graph.run() == 0
+        assert torch.equal(out_g, out_direct)
+        g = np.random.default_rng(11)
+        logits2 = g.standard_normal(logits.shape).astype(np.float32)
+        x2 = W.f32_to_bf16_bits(g.standard_normal(x.shape).astype(np.float32))
+        lg.copy_(torch.from_numpy(logits2))
+        xh.copy_(torch.from_numpy(x2.view(np.int16)))
+        assert graph.run() == 0
+        ids, tw = oracle.route(logits2, wl.k)
+        ref = oracle.forward(x2, ids, tw.astype(np.float32), lora, w)
+        assert parity_error(out_g.view(torch.bfloat16).float().numpy(), ref)[0] <= TOL
+    finally:
+        graph.close()
