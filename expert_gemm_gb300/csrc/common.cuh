@@ -67,6 +67,7 @@ struct GemmMaps {
   CUtensorMap tok;    // token rows in sorted order (x_sorted / h_sorted) 2D
   CUtensorMap lw;     // LoRA expand weights (Bt_gu 4D / Bt_dn 3D)
   CUtensorMap ls;     // S run tiles 3D
+  CUtensorMap out;    // CTA-pair gate_up / down: output rows (h_sorted / y, bf16) 2D, box {64, 32}
 };
 
 // Launchers (defined next to their kernels).

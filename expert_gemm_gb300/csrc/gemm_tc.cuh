@@ -65,6 +65,7 @@ struct GemmCfg {
   // fits beside a shrink CTA -- measured faster on the decode shapes; 32/64: 5)
   static constexpr int STAGES = MODE == kShrink ? 4
                                 : SWAP           ? (BT <= 16 ? 3 : 5)
+                                : CTA2           ? 5   // + 32 KB of output staging
                                                  : (192 * 1024) / STAGE_BYTES;
   // accumulators: non-swapped MT tiles of M=128 tokens x N; swapped NH tiles of 128 x BT
   static constexpr int NH = MODE == kShrink ? 1 : 2;
@@ -76,7 +77,12 @@ struct GemmCfg {
   static constexpr int TMEM_COLS =
       TMEM_NEED <= 32 ? 32 : TMEM_NEED <= 64 ? 64 : TMEM_NEED <= 128 ? 128 : TMEM_NEED <= 256 ? 256 : 512;
   static constexpr int SD = 4;                              // tile-id ring depth
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align slack*/ + 4096 /*barriers, tile ring*/;
+  // CTA pairs stage their bf16 output rows in shared memory and write them with TMA
+  // stores: per epilogue warp two buffers of 32 rows x 64 columns (4 KB each).
+  static constexpr bool TMA_STORE = CTA2;
+  static constexpr int OUT_BYTES = TMA_STORE ? 4 * 2 * 4096 : 0;
+  static constexpr int SMEM_BYTES =
+      STAGES * STAGE_BYTES + OUT_BYTES + 1024 /*align slack*/ + 4096 /*barriers, tile ring*/;
   static_assert(!SWAP || (BT == 16 || BT == 32 || BT == 64), "swapped tiles take 16/32/64 tokens");
   static_assert(SWAP || BT == 128 || BT == 256, "token-tiled blocks are 128 or 256 rows");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
@@ -134,7 +140,9 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&v);
 }
-__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
+// silu(z) = z / (1 + e^-z) with the fast approximate divide (a few ulp; the result is
+// rounded to bf16): the epilogue's instruction count competes with the MMA issuer.
+__device__ __forceinline__ float silu_f(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
 template <int MODE>
 __device__ __forceinline__ int live_tiles(const GemmParams& prm) {
@@ -229,6 +237,35 @@ __device__ __forceinline__ const Tile* sched_read(GemmBars* bars, int i, int32_t
   return &bars->tiles[slot];
 }
 
+// Output staging of the CTA-pair epilogues: epilogue warp q owns two 4 KB buffers of
+// 32 rows x 128 bytes (64 bf16 columns) in the 128-byte-swizzled layout of a TMA box
+// {64, 32}; lane i writes row i.  Before a buffer is reused, the store issued from it
+// two stores earlier must have read it.
+__device__ __forceinline__ uint8_t* stage_out_buffer(uint8_t* out_stage, int q, int lane, int n_out) {
+  if (n_out >= 2) {
+    if (lane == 0) bulk_wait_read<1>();
+    __syncwarp();
+  }
+  return out_stage + q * 8192 + (n_out & 1) * 4096;
+}
+// 16-byte chunks j and j + 1 of row `lane` (chunk j holds columns 8j .. 8j + 7).
+__device__ __forceinline__ void put_row_chunks(uint8_t* buf, int lane, int j, const uint32_t (&pk)[8]) {
+  uint8_t* row = buf + lane * 128;
+  *reinterpret_cast<uint4*>(row + ((j ^ (lane & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+  *reinterpret_cast<uint4*>(row + (((j + 1) ^ (lane & 7)) << 4)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+}
+// Makes the warp's staged rows visible to the async proxy and stores them at (col, row).
+__device__ __forceinline__ void store_out_chunk(const CUtensorMap* map, const uint8_t* buf, int lane, int col,
+                                                int row, int& n_out) {
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(map, buf, col, row);
+    bulk_commit();
+  }
+  ++n_out;
+}
+
 template <int MODE, bool SWAP, int BT>
 __global__ void __launch_bounds__(192, 1)
     moe_gemm_kernel(const __grid_constant__ GemmMaps maps, const __grid_constant__ GemmParams prm) {
@@ -254,7 +291,8 @@ __global__ void __launch_bounds__(192, 1)
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  GemmBars* bars = reinterpret_cast<GemmBars*>(smem + C::STAGES * C::STAGE_BYTES);
+  uint8_t* out_stage = smem + C::STAGES * C::STAGE_BYTES;   // 1024-aligned (C::OUT_BYTES)
+  GemmBars* bars = reinterpret_cast<GemmBars*>(out_stage + C::OUT_BYTES);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
@@ -536,6 +574,7 @@ __global__ void __launch_bounds__(192, 1)
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;          // TMEM lane quarter this warp may access
     const int m = q * 32 + lane;     // accumulator row (TMEM lane) of this thread
+    int n_out = 0;                   // TMA stores issued by this warp (CTA pairs)
     for (int i = 0;; ++i) {
       const Tile* tp = sched_read(bars, i, prm.status);
       if (!tp) break;
@@ -655,16 +694,32 @@ __global__ void __launch_bounds__(192, 1)
                   tmem_ld16(ta + 128 + c0 + 16 * q4, up[q4]);   // up features
                 }
                 tmem_ld_wait();
-                uint4* dst = reinterpret_cast<uint4*>(hrow + c0);
+                if constexpr (C::TMA_STORE) {
+                  uint8_t* buf = stage_out_buffer(out_stage, q, lane, n_out);
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                  uint32_t pk[8];
+                  for (int q4 = 0; q4 < 4; ++q4) {
+                    uint32_t pk[8];
 #pragma unroll
-                  for (int j = 0; j < 8; ++j)
-                    pk[j] = pack_bf16x2(silu_f(__uint_as_float(g[q4][2 * j])) * __uint_as_float(up[q4][2 * j]),
-                                        silu_f(__uint_as_float(g[q4][2 * j + 1])) * __uint_as_float(up[q4][2 * j + 1]));
-                  dst[2 * q4] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                  dst[2 * q4 + 1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                    for (int j = 0; j < 8; ++j)
+                      pk[j] = pack_bf16x2(silu_f(__uint_as_float(g[q4][2 * j])) * __uint_as_float(up[q4][2 * j]),
+                                          silu_f(__uint_as_float(g[q4][2 * j + 1])) *
+                                              __uint_as_float(up[q4][2 * j + 1]));
+                    put_row_chunks(buf, lane, 2 * q4, pk);
+                  }
+                  store_out_chunk(&maps.out, buf, lane, f0 + c0, row0 + mt * 128 + q * 32, n_out);
+                } else {
+                  uint4* dst = reinterpret_cast<uint4*>(hrow + c0);
+#pragma unroll
+                  for (int q4 = 0; q4 < 4; ++q4) {
+                    uint32_t pk[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                      pk[j] = pack_bf16x2(silu_f(__uint_as_float(g[q4][2 * j])) * __uint_as_float(up[q4][2 * j]),
+                                          silu_f(__uint_as_float(g[q4][2 * j + 1])) *
+                                              __uint_as_float(up[q4][2 * j + 1]));
+                    dst[2 * q4] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    dst[2 * q4 + 1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                  }
                 }
               }
             }
@@ -699,6 +754,24 @@ __global__ void __launch_bounds__(192, 1)
           uint16_t* y16 = static_cast<uint16_t*>(prm.y_out);
           float* y32 = static_cast<float*>(prm.y_out) + static_cast<size_t>(t.ks) * prm.part_rows * H;
           if constexpr (!SWAP) {
+            if constexpr (C::TMA_STORE) {
+              // 64 output features per TMA store; every row of the tile is written (a
+              // padding row's output is never read).  One TMEM wait per 16 columns.
+              for (int c0 = 0; c0 < 256; c0 += 64) {
+                if (f0 + c0 >= H) break;
+                uint8_t* buf = stage_out_buffer(out_stage, q, lane, n_out);
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                  tmem_ld16(tq + c0 + 16 * q4, v);
+                  tmem_ld_wait();
+                  uint32_t pk[8];
+#pragma unroll
+                  for (int j = 0; j < 8; ++j) pk[j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+                  put_row_chunks(buf, lane, 2 * q4, pk);
+                }
+                store_out_chunk(&maps.out, buf, lane, f0 + c0, row0 + q * 32, n_out);
+              }
+            } else
             for (int mt = 0; mt < C::MT; ++mt) {
               const int row = row0 + mt * 128 + m;
               const bool valid = prm.sorted_p[row] < prm.P;
@@ -759,6 +832,9 @@ __global__ void __launch_bounds__(192, 1)
     }
   }
 
+  if constexpr (C::TMA_STORE) {
+    if (warp >= 2 && lane == 0) bulk_wait_all();   // the epilogue's output stores have completed
+  }
   __syncwarp();   // lanes of every warp reconverge before the CTA barrier
   tc_fence_before_sync();
   __syncthreads();

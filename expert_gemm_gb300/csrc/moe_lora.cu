@@ -510,8 +510,22 @@ int do_forward(const moe_lora_dims* d, const uint16_t* x, const float* topk_w, c
     m_gu.lw = m_gu.ls = m_gu.w;
     m_dn.lw = m_dn.ls = m_dn.w;
   }
-  m_sgu.lw = m_sgu.ls = m_sgu.w;
-  m_sdn.lw = m_sdn.ls = m_sdn.w;
+  m_sgu.lw = m_sgu.ls = m_sgu.out = m_sgu.w;
+  m_sdn.lw = m_sdn.ls = m_sdn.out = m_sdn.w;
+  // output rows of the CTA-pair gate_up / down epilogues (TMA stores of 32 rows x 64 columns)
+  m_gu.out = m_gu.w;
+  m_dn.out = m_dn.w;
+  if (BT == 256) {
+    const uint32_t bx[2] = {64, 32};
+    {
+      const uint64_t dm[2] = {I, rows}, st[1] = {I * 2};
+      MOE_TRY(encode(&m_gu.out, hs, 2, dm, st, bx, CU_TENSOR_MAP_SWIZZLE_128B, "h_sorted (store)"));
+    }
+    if (l.ks_dn == 1) {
+      const uint64_t dm[2] = {H, rows}, st[1] = {H * 2};
+      MOE_TRY(encode(&m_dn.out, y, 2, dm, st, bx, CU_TENSOR_MAP_SWIZZLE_128B, "y (store)"));
+    }
+  }
 
   moe::GemmParams p{};
   p.block_expert = al->block_expert;

@@ -255,7 +255,7 @@ __global__ void __launch_bounds__(256) silu_rows_kernel(const float4* __restrict
       a.x += ga.x; a.y += ga.y; a.z += ga.z; a.w += ga.w;
       b.x += gb.x; b.y += gb.y; b.z += gb.z; b.w += gb.w;
     }
-    auto silu = [](float z) { return z / (1.0f + __expf(-z)); };
+    auto silu = [](float z) { return __fdividef(z, 1.0f + __expf(-z)); };
     h[i] = make_uint2(pack2(silu(a.x) * b.x, silu(a.y) * b.y), pack2(silu(a.z) * b.z, silu(a.w) * b.w));
   }
 }
