@@ -17,6 +17,9 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
                                                           int k, int P, uint4* __restrict__ xs,
                                                           int32_t* __restrict__ pair_row, int32_t* __restrict__ status,
                                                           int32_t* __restrict__ ctr, int n_ctr, bool copy_rows) {
+  // Launched as a programmatic dependent of whatever precedes the forward (the align):
+  // its launch overlaps that kernel's tail, its reads wait for it.
+  pdl_wait();
   pdl_trigger();   // the next kernel waits for this grid before reading what it writes
   const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t nthr = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -215,10 +218,21 @@ cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* sorted_p, const
   // When x is larger than half the 129 MB L2, its k re-reads in sorted-row order come
   // from DRAM: copy in token order then (x read once).  Otherwise one row-order pass.
   const bool token_order = gather_token_order(P / k, H);
-  gather_rows_kernel<<<static_cast<unsigned>(grid), rows_per_cta * 32, 0, s>>>(
-      reinterpret_cast<const uint4*>(x), sorted_p, totals, max_rows, H / 8, k, P, reinterpret_cast<uint4*>(x_sorted),
-      pair_row, status, ctr, n_ctr, !token_order);
-  cudaError_t err = cudaGetLastError();
+  cudaError_t err;
+  {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(rows_per_cta * 32, 1, 1);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    err = cudaLaunchKernelEx(&cfg, gather_rows_kernel, reinterpret_cast<const uint4*>(x), sorted_p, totals, max_rows,
+                             H / 8, k, P, reinterpret_cast<uint4*>(x_sorted), pair_row, status, ctr, n_ctr,
+                             !token_order);
+  }
   if (err != cudaSuccess || !token_order) return err;
   const int64_t T = P / k;
   cudaLaunchConfig_t cfg = {};
