@@ -337,7 +337,7 @@ def run_ours(args, rank, world, local_rank):
     ml.load()
     wl = workload_of(args)
     w = W.make_weights(wl, 0)                     # same weights on every replica, own batch per rank
-    wd = {n: _dev(torch, w[n]) for n in ("W_gu", "W_dn", "A_gu", "Bt_gu", "A_dn", "Bt_dn")}
+    wd = {n: _dev(torch, w[n]) for n in ("W_gu", "W_dn", "A_gu", "B_gu", "A_dn", "B_dn")}
     del w
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     bm = args.block_m or ml.pick_block_m(wl.T, wl.k, wl.E)

@@ -12,8 +12,8 @@ namespace moe {
 // Which stage of the layer one grouped-GEMM launch computes.
 enum GemmMode : int {
   kShrink = 0,   // S_run = X_block * A[a,e]^T       (gate_up_shrink / down_shrink)
-  kGateUp = 1,   // h = silu(gate) * up, gate/up = X W_gu[e]^T + S_run Bt_gu[a,e]^T (gate_up + expand)
-  kDown = 2,     // y[row] = h W_dn[e]^T + S_run Bt_dn[a,e]^T                      (down + expand)
+  kGateUp = 1,   // h = silu(gate) * up, gate/up = X W_gu[e]^T + S_run B_gu[a,e] (gate_up + expand)
+  kDown = 2,     // y[row] = h W_dn[e]^T + S_run B_dn[a,e]                      (down + expand)
 };
 
 constexpr int kKTile = 64;      // K elements per pipeline stage (one 128-byte swizzle row of bf16)
@@ -65,7 +65,7 @@ struct GemmParams {
 struct GemmMaps {
   CUtensorMap w;      // base weights (W_gu 4D / W_dn 3D / A 3D)
   CUtensorMap tok;    // token rows in sorted order (x_sorted / h_sorted) 2D
-  CUtensorMap lw;     // LoRA expand weights (Bt_gu 4D / Bt_dn 3D)
+  CUtensorMap lw;     // LoRA expand weights, rank-major (B_gu 5D / B_dn 4D)
   CUtensorMap ls;     // S run tiles 3D
   CUtensorMap out;    // CTA-pair gate_up / down: output rows (h_sorted / y, bf16) 2D, box {64, 32}
 };

@@ -2,13 +2,13 @@
 // fed by TMA, for the three GEMM-shaped steps of the MoE-LoRA layer:
 //
 //   kShrink : S_run = X_block * A[a,e]^T           LoRA shrink of gate_up or down
-//   kGateUp : g = X W_gu[e]^T (+ S_run Bt_gu[a,e]^T per adapter run), h = silu(g_gate) * g_up
-//   kDown   : d = H W_dn[e]^T (+ S_run Bt_dn[a,e]^T per adapter run), stored per sorted row
+//   kGateUp : g = X W_gu[e]^T (+ S_run B_gu[a,e] per adapter run), h = silu(g_gate) * g_up
+//   kDown   : d = H W_dn[e]^T (+ S_run B_dn[a,e] per adapter run), stored per sorted row
 //
 // The LoRA expand is not a separate kernel: every adapter run of a token block adds
 // ceil(rank/16) extra K-steps (packed BK/16 per pipeline stage) to the same TMEM
 // accumulator, with the run's S tile (rows outside the run are zero) as the
-// token-side operand and Bt[a,e] as the weight-side operand.  SiLU gating happens in
+// token-side operand and B[a,e] as the weight-side operand.  SiLU gating happens in
 // the epilogue that drains TMEM; the down epilogue stores each real row's output with
 // plain stores and a separate pass combines a token's k rows in a fixed order (no
 // atomics anywhere, so repeated calls give identical bytes).  This is the pages'
@@ -423,21 +423,20 @@ __global__ void __launch_bounds__(192, 1)
               const int c = lc;
               uint8_t* wc = wdst + j * (C::WROWS * 32);
               uint8_t* tc = tdst + j * (C::TROWS * 32);
+              // weight side: 16 rank rows of B (rank-major) as 64-column atoms; one box
+              // holds the tile's columns (gate_up: gate then up), a pair CTA's half
               if constexpr (C::CTA2) {
                 const int rk = static_cast<int>(rank);
                 if constexpr (MODE == kGateUp)
-                  tma_load_4d_pair(wc, &maps.lw, fb_pair, c * kRankChunk, t.f0, rk, ae);
+                  tma_load_5d_pair(wc, &maps.lw, fb_pair, 0, c * kRankChunk, t.f0 / 64, rk, ae);
                 else
-                  tma_load_3d_pair(wc, &maps.lw, fb_pair, c * kRankChunk, t.f0 + 128 * rk, ae);
+                  tma_load_4d_pair(wc, &maps.lw, fb_pair, 0, c * kRankChunk, (t.f0 + 128 * rk) / 64, ae);
                 tma_load_3d_pair(tc, &maps.ls, fb_pair, c * kRankChunk, 128 * rk, run);
               } else {
-                if constexpr (MODE == kGateUp) {
-                  tma_load_4d(wc, &maps.lw, fb, c * kRankChunk, t.f0, 0, ae);
-                  tma_load_4d(wc + 128 * 32, &maps.lw, fb, c * kRankChunk, t.f0, 1, ae);
-                } else {
-                  tma_load_3d(wc, &maps.lw, fb, c * kRankChunk, t.f0, ae);
-                  tma_load_3d(wc + 128 * 32, &maps.lw, fb, c * kRankChunk, t.f0 + 128, ae);
-                }
+                if constexpr (MODE == kGateUp)
+                  tma_load_5d(wc, &maps.lw, fb, 0, c * kRankChunk, t.f0 / 64, 0, ae);
+                else
+                  tma_load_4d(wc, &maps.lw, fb, 0, c * kRankChunk, t.f0 / 64, ae);
                 tma_load_3d(tc, &maps.ls, fb, c * kRankChunk, 0, run);
               }
               if (++lc == tl.nch[lr]) {
@@ -485,10 +484,11 @@ __global__ void __launch_bounds__(192, 1)
         else tc_commit(bar);
       };
       constexpr int kM = C::CTA2 ? 256 : 128;
-      // stage-0 descriptors: base K-steps (128/64-byte swizzle rows), LoRA K-steps (32-byte)
+      // stage-0 descriptors: base K-steps (128/64-byte swizzle rows); LoRA K-steps: S
+      // K-major in 32-byte rows, B MN-major (64-column atoms of 16 rank rows, 2 KB apart)
       const uint32_t sbase = smem_u32(smem);
       const uint64_t dW = smem_desc(sbase, C::SBO, C::SW), dT = smem_desc(sbase + C::W_BYTES, C::SBO, C::SW);
-      const uint64_t dWl = smem_desc(sbase, 256, kSw32), dTl = smem_desc(sbase + C::W_BYTES, 256, kSw32);
+      const uint64_t dWl = smem_desc_mn128(sbase, 2048), dTl = smem_desc(sbase + C::W_BYTES, 256, kSw32);
       int st = 0;          // stage of the next K-step (continues across tiles)
       uint32_t sph = 0;    // its phase parity
       for (int i = 0;; ++i) {
@@ -510,7 +510,8 @@ __global__ void __launch_bounds__(192, 1)
         // instruction descriptors of this tile's base and LoRA K-steps
         const uint32_t id_base = SWAP ? idesc_bf16_f32(128, BT)
                                       : idesc_bf16_f32(kM, MODE == kShrink ? t.snch * kRankChunk : 256);
-        constexpr uint32_t id_lora = SWAP ? idesc_bf16_f32(128, BT) : idesc_bf16_f32(kM, 256);
+        constexpr uint32_t id_lora =
+            SWAP ? (idesc_bf16_f32(128, BT) | kIdescAMn) : (idesc_bf16_f32(kM, 256) | kIdescBMn);
         uint32_t acc = 0;
         bool ok = true;
         // The hot loop issues from one thread: descriptors are the stage-0 ones plus
@@ -541,7 +542,7 @@ __global__ void __launch_bounds__(192, 1)
               acc = 1;
             }
           } else if constexpr (C::kLora) {
-            // up to CPS rank chunks, of one or several runs (each chunk: its own S and Bt)
+            // up to CPS rank chunks, of one or several runs (each chunk: its own S and B)
             const int left = t.snch - (it - t.nk) * C::CPS;
             const int nc = left < C::CPS ? left : C::CPS;
             for (int c = 0; c < nc; ++c) {

@@ -4,9 +4,9 @@
 // Launch sequence of moe_lora_forward (all on the caller's stream):
 //   gather    x rows into sorted (expert, adapter, pair) order; zero padding rows
 //   shrink    S_gu per adapter run = x_block A_gu[a,e]^T          (tcgen05)
-//   gate_up   h = silu(gate) * up, gate/up = x W_gu[e]^T + S_gu Bt_gu[a,e]^T (tcgen05)
+//   gate_up   h = silu(gate) * up, gate/up = x W_gu[e]^T + S_gu B_gu[a,e]   (tcgen05)
 //   shrink    S_dn per adapter run = h_block A_dn[a,e]^T          (tcgen05)
-//   down      y[row] = h W_dn[e]^T + S_dn Bt_dn[a,e]^T              (tcgen05)
+//   down      y[row] = h W_dn[e]^T + S_dn B_dn[a,e]                (tcgen05)
 //   combine   out[t] = bf16(sum_j w[t,j] y[row of (t,j)]), fixed order
 #include <cudaTypedefs.h>
 
@@ -400,8 +400,8 @@ int do_route_align(const moe_lora_dims* d, const float* logits, const int32_t* l
 }
 
 int do_forward(const moe_lora_dims* d, const uint16_t* x, const float* topk_w, const moe_lora_align_buf* al,
-               const uint16_t* W_gu, const uint16_t* W_dn, const uint16_t* A_gu, const uint16_t* Bt_gu,
-               const uint16_t* A_dn, const uint16_t* Bt_dn, uint16_t* out, void* ws, size_t ws_bytes,
+               const uint16_t* W_gu, const uint16_t* W_dn, const uint16_t* A_gu, const uint16_t* B_gu,
+               const uint16_t* A_dn, const uint16_t* B_dn, uint16_t* out, void* ws, size_t ws_bytes,
                int32_t* dev_status, cudaStream_t s, void* const* ev) {
   MOE_RESOLVE(d);
   MOE_TRY(validate_dims(d));
@@ -422,9 +422,9 @@ int do_forward(const moe_lora_dims* d, const uint16_t* x, const float* topk_w, c
   MOE_TRY(check_ptr(ws, "workspace", true));
   if (d->L > 0) {
     MOE_TRY(check_ptr(A_gu, "A_gu", true));
-    MOE_TRY(check_ptr(Bt_gu, "Bt_gu", true));
+    MOE_TRY(check_ptr(B_gu, "B_gu", true));
     MOE_TRY(check_ptr(A_dn, "A_dn", true));
-    MOE_TRY(check_ptr(Bt_dn, "Bt_dn", true));
+    MOE_TRY(check_ptr(B_dn, "B_dn", true));
   }
   if (ws_bytes < l.bytes) return fail(MOE_LORA_EWORKSPACE, "forward workspace %zu < %zu bytes", ws_bytes, l.bytes);
   MOE_TRY(check_device());
@@ -489,15 +489,20 @@ int do_forward(const moe_lora_dims* d, const uint16_t* x, const float* topk_w, c
       const uint32_t bx[3] = {64, 16, 1};
       MOE_TRY(encode(&m_sdn.w, A_dn, 3, dm, st, bx, CU_TENSOR_MAP_SWIZZLE_128B, "A_dn"));
     }
+    // B, rank-major: one box is 16 rank rows of the tile's weight columns, landing as
+    // 64-column atoms of 16 rows x 128 bytes (the MN-major 128-byte-swizzle operand
+    // layout).  Dims: 64 columns, rank, 64-column atom, [gate|up,] adapter x expert.
+    // Columns past I (or H) fall outside the atom dimension and read as zero.
+    const uint32_t atoms = BT == 256 ? 2u : 4u;   // CTA pairs load their 128 columns each
     {
-      const uint64_t dm[4] = {R, I, 2, LE}, st[3] = {R * 2, I * R * 2, 2 * I * R * 2};
-      const uint32_t bx[4] = {16, 128, 1, 1};
-      MOE_TRY(encode(&m_gu.lw, Bt_gu, 4, dm, st, bx, CU_TENSOR_MAP_SWIZZLE_32B, "Bt_gu"));
+      const uint64_t dm[5] = {64, R, I / 64, 2, LE}, st[4] = {2 * I * 2, 128, I * 2, R * 2 * I * 2};
+      const uint32_t bx[5] = {64, 16, 2, atoms / 2, 1};
+      MOE_TRY(encode(&m_gu.lw, B_gu, 5, dm, st, bx, CU_TENSOR_MAP_SWIZZLE_128B, "B_gu"));
     }
     {
-      const uint64_t dm[3] = {R, H, LE}, st[2] = {R * 2, H * R * 2};
-      const uint32_t bx[3] = {16, 128, 1};
-      MOE_TRY(encode(&m_dn.lw, Bt_dn, 3, dm, st, bx, CU_TENSOR_MAP_SWIZZLE_32B, "Bt_dn"));
+      const uint64_t dm[4] = {64, R, H / 64, LE}, st[3] = {H * 2, 128, R * H * 2};
+      const uint32_t bx[4] = {64, 16, atoms, 1};
+      MOE_TRY(encode(&m_dn.lw, B_dn, 4, dm, st, bx, CU_TENSOR_MAP_SWIZZLE_128B, "B_dn"));
     }
     {
       const uint64_t dm[3] = {RP, (uint64_t)BT, nruns}, st[2] = {RP * 2, (uint64_t)BT * RP * 2};
@@ -645,7 +650,7 @@ LayerLayout layer_layout(const moe_lora_dims* d) {
 
 extern "C" {
 
-int moe_lora_version(void) { return 200; }
+int moe_lora_version(void) { return 300; }
 
 const char* moe_lora_status_string(int status) {
   switch (status) {
@@ -740,10 +745,10 @@ int moe_lora_route_align(const moe_lora_dims* d, const float* logits, const int3
 
 int moe_lora_forward(const moe_lora_dims* d, const uint16_t* x, const float* topk_w,
                      const moe_lora_align_buf* aligned, const uint16_t* W_gu, const uint16_t* W_dn,
-                     const uint16_t* A_gu, const uint16_t* Bt_gu, const uint16_t* A_dn, const uint16_t* Bt_dn,
+                     const uint16_t* A_gu, const uint16_t* B_gu, const uint16_t* A_dn, const uint16_t* B_dn,
                      uint16_t* out, void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream,
                      void* const* stage_events) {
-  return do_forward(d, x, topk_w, aligned, W_gu, W_dn, A_gu, Bt_gu, A_dn, Bt_dn, out, workspace, workspace_bytes,
+  return do_forward(d, x, topk_w, aligned, W_gu, W_dn, A_gu, B_gu, A_dn, B_dn, out, workspace, workspace_bytes,
                     dev_status, static_cast<cudaStream_t>(stream), stage_events);
 }
 
@@ -754,7 +759,7 @@ namespace {
 // forward, out and (status, totals) back.  status_dst/totals_dst: host destinations.
 int layer_enqueue(const moe_lora_dims* d, const float* logits_host, const int32_t* lora_ids_host,
                   const uint16_t* x_host, const uint16_t* W_gu, const uint16_t* W_dn, const uint16_t* A_gu,
-                  const uint16_t* Bt_gu, const uint16_t* A_dn, const uint16_t* Bt_dn, uint16_t* out_host,
+                  const uint16_t* B_gu, const uint16_t* A_dn, const uint16_t* B_dn, uint16_t* out_host,
                   void* workspace, size_t workspace_bytes, int32_t* status_dst, int32_t* totals_dst,
                   cudaStream_t s) {
   MOE_TRY(validate_dims(d));
@@ -787,7 +792,7 @@ int layer_enqueue(const moe_lora_dims* d, const float* logits_host, const int32_
   } else {
     MOE_TRY(do_align(d, ids, lora, &al, b + l.align, l.fwd - l.align, s));
   }
-  MOE_TRY(do_forward(d, x, w, &al, W_gu, W_dn, A_gu, Bt_gu, A_dn, Bt_dn, out, b + l.fwd, l.logits - l.fwd, status, s,
+  MOE_TRY(do_forward(d, x, w, &al, W_gu, W_dn, A_gu, B_gu, A_dn, B_dn, out, b + l.fwd, l.logits - l.fwd, status, s,
                       nullptr));
   if (T > 0) MOE_CUDA(cudaMemcpyAsync(out_host, out, T * d->H * 2, cudaMemcpyDeviceToHost, s));
   MOE_CUDA(cudaMemcpyAsync(status_dst, status, 4, cudaMemcpyDeviceToHost, s));
@@ -805,12 +810,12 @@ extern "C" {
 
 int moe_lora_layer_host(const moe_lora_dims* d, const float* logits_host, const int32_t* lora_ids_host,
                         const uint16_t* x_host, const uint16_t* W_gu, const uint16_t* W_dn, const uint16_t* A_gu,
-                        const uint16_t* Bt_gu, const uint16_t* A_dn, const uint16_t* Bt_dn, uint16_t* out_host,
+                        const uint16_t* B_gu, const uint16_t* A_dn, const uint16_t* B_dn, uint16_t* out_host,
                         void* workspace, size_t workspace_bytes, int64_t* dropped, void* stream) {
   MOE_RESOLVE(d);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int32_t host_status = 0, tot[4] = {0, 0, 0, 0};
-  MOE_TRY(layer_enqueue(d, logits_host, lora_ids_host, x_host, W_gu, W_dn, A_gu, Bt_gu, A_dn, Bt_dn, out_host,
+  MOE_TRY(layer_enqueue(d, logits_host, lora_ids_host, x_host, W_gu, W_dn, A_gu, B_gu, A_dn, B_dn, out_host,
                         workspace, workspace_bytes, &host_status, tot, s));
   MOE_CUDA(cudaStreamSynchronize(s));
   if (dropped) *dropped = tot[3];
@@ -820,8 +825,8 @@ int moe_lora_layer_host(const moe_lora_dims* d, const float* logits_host, const 
 
 int moe_lora_layer_graph_create(const moe_lora_dims* d, const float* logits_host, const int32_t* lora_ids_host,
                                 const uint16_t* x_host, const uint16_t* W_gu, const uint16_t* W_dn,
-                                const uint16_t* A_gu, const uint16_t* Bt_gu, const uint16_t* A_dn,
-                                const uint16_t* Bt_dn, uint16_t* out_host, int32_t* status_host, void* workspace,
+                                const uint16_t* A_gu, const uint16_t* B_gu, const uint16_t* A_dn,
+                                const uint16_t* B_dn, uint16_t* out_host, int32_t* status_host, void* workspace,
                                 size_t workspace_bytes, void* stream, moe_lora_graph** graph) {
   MOE_RESOLVE(d);
   if (!graph) return fail(MOE_LORA_EINVAL, "graph is NULL");
@@ -830,13 +835,13 @@ int moe_lora_layer_graph_create(const moe_lora_dims* d, const float* logits_host
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (!s) return fail(MOE_LORA_EINVAL, "graph capture needs a non-default stream");
   // one eager run: validation and the kernels' one-time set-up happen outside the capture
-  MOE_TRY(layer_enqueue(d, logits_host, lora_ids_host, x_host, W_gu, W_dn, A_gu, Bt_gu, A_dn, Bt_dn, out_host,
+  MOE_TRY(layer_enqueue(d, logits_host, lora_ids_host, x_host, W_gu, W_dn, A_gu, B_gu, A_dn, B_dn, out_host,
                         workspace, workspace_bytes, status_host, status_host + 4, s));
   MOE_CUDA(cudaStreamSynchronize(s));
   if (status_host[0] != 0) return fail(MOE_LORA_EDEVICE, "device status 0x%x", status_host[0]);
   cudaGraph_t g = nullptr;
   MOE_CUDA(cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal));
-  const int st = layer_enqueue(d, logits_host, lora_ids_host, x_host, W_gu, W_dn, A_gu, Bt_gu, A_dn, Bt_dn, out_host,
+  const int st = layer_enqueue(d, logits_host, lora_ids_host, x_host, W_gu, W_dn, A_gu, B_gu, A_dn, B_dn, out_host,
                                workspace, workspace_bytes, status_host, status_host + 4, s);
   const cudaError_t ce = cudaStreamEndCapture(s, &g);
   if (st != MOE_LORA_OK) {

@@ -153,6 +153,15 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* m, uin
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_5d(void* dst, const CUtensorMap* m, uint64_t* bar, int c0, int c1,
+                                            int c2, int c3, int c4) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
+      : "memory");
+}
+
 // TMA loads of a CTA pair: the data lands in this CTA's shared memory, the completion
 // is signalled on a barrier that may belong to either CTA of the pair (a
 // shared::cluster address from mapa_shared).
@@ -177,6 +186,15 @@ __device__ __forceinline__ void tma_load_4d_pair(void* dst, const CUtensorMap* m
       "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_5d_pair(void* dst, const CUtensorMap* m, uint32_t bar, int c0, int c1,
+                                                 int c2, int c3, int c4) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
       : "memory");
 }
 
@@ -244,6 +262,22 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t sbo, uint
   return d;
 }
 constexpr uint32_t kSw128 = 2, kSw64 = 4, kSw32 = 6;
+// Shared-memory matrix descriptor of an MN-major operand in the 128-byte swizzle: the
+// tile is stored as 64-element MN atoms, each atom its K rows of 128 bytes (K rows
+// contiguous, 8-row groups 1024 bytes apart); `atom_stride` bytes between the atoms.
+// Leading offset = stride between MN atoms, stride offset = stride between 8-row K
+// groups (checked on GB300 with one MMA against a host product).
+__device__ __forceinline__ uint64_t smem_desc_mn128(uint32_t saddr, uint32_t atom_stride) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>((atom_stride >> 4) & 0x3FFFu) << 16;   // leading offset: MN atoms
+  d |= static_cast<uint64_t>(1024u >> 4) << 32;                     // stride offset: 8-row K groups
+  d |= static_cast<uint64_t>(1u) << 46;
+  d |= static_cast<uint64_t>(kSw128) << 61;
+  return d;
+}
+// Instruction-descriptor bits marking operand A or B as MN-major.
+constexpr uint32_t kIdescAMn = 1u << 15, kIdescBMn = 1u << 16;
 
 // Instruction descriptor of tcgen05.mma.kind::f16: bf16 x bf16 -> fp32, both
 // operands K-major, shape M x N (K = 16 per instruction).

@@ -222,7 +222,7 @@ STAGES = ("gather", "shrink_gu", "gate_up", "shrink_dn", "down", "combine")
 
 def forward(d: LayerDims, x, topk_w, bufs: dict, w: dict, out, workspace, dev_status, stream=None,
             stage_events=None):
-    """w: device tensors W_gu, W_dn, A_gu, Bt_gu, A_dn, Bt_dn (bf16 or int16 bit patterns).
+    """w: device tensors W_gu, W_dn, A_gu, B_gu, A_dn, B_dn (bf16 or int16 bit patterns).
 
     stage_events: None, or NUM_STAGES + 1 torch.cuda.Event recorded at the stage boundaries.
     """
@@ -230,8 +230,8 @@ def forward(d: LayerDims, x, topk_w, bufs: dict, w: dict, out, workspace, dev_st
     if stage_events is not None:
         ev = (C.c_void_p * len(stage_events))(*[e.cuda_event for e in stage_events])
     _check(load().moe_lora_forward(C.byref(d.c()), _ptr(x), _ptr(topk_w), C.byref(_abuf(bufs)),
-                                   _ptr(w["W_gu"]), _ptr(w["W_dn"]), _ptr(w.get("A_gu")), _ptr(w.get("Bt_gu")),
-                                   _ptr(w.get("A_dn")), _ptr(w.get("Bt_dn")), _ptr(out), _ptr(workspace),
+                                   _ptr(w["W_gu"]), _ptr(w["W_dn"]), _ptr(w.get("A_gu")), _ptr(w.get("B_gu")),
+                                   _ptr(w.get("A_dn")), _ptr(w.get("B_dn")), _ptr(out), _ptr(workspace),
                                    workspace.numel() * workspace.element_size(), _ptr(dev_status),
                                    _stream(stream), ev))
 
@@ -240,8 +240,8 @@ def layer_host(d: LayerDims, logits_host, lora_ids_host, x_host, w: dict, out_ho
     """Whole layer from host buffers (pinned recommended) to a host output; returns dropped pairs."""
     dropped = C.c_int64()
     _check(load().moe_lora_layer_host(C.byref(d.c()), _ptr(logits_host), _ptr(lora_ids_host), _ptr(x_host),
-                                      _ptr(w["W_gu"]), _ptr(w["W_dn"]), _ptr(w.get("A_gu")), _ptr(w.get("Bt_gu")),
-                                      _ptr(w.get("A_dn")), _ptr(w.get("Bt_dn")), _ptr(out_host), _ptr(workspace),
+                                      _ptr(w["W_gu"]), _ptr(w["W_dn"]), _ptr(w.get("A_gu")), _ptr(w.get("B_gu")),
+                                      _ptr(w.get("A_dn")), _ptr(w.get("B_dn")), _ptr(out_host), _ptr(workspace),
                                       workspace.numel() * workspace.element_size(), C.byref(dropped),
                                       _stream(stream)))
     return dropped.value
@@ -261,7 +261,7 @@ class LayerGraph:
         h = C.c_void_p()
         _check(load().moe_lora_layer_graph_create(
             C.byref(d.c()), _ptr(logits_host), _ptr(lora_ids_host), _ptr(x_host), _ptr(w["W_gu"]), _ptr(w["W_dn"]),
-            _ptr(w.get("A_gu")), _ptr(w.get("Bt_gu")), _ptr(w.get("A_dn")), _ptr(w.get("Bt_dn")), _ptr(out_host),
+            _ptr(w.get("A_gu")), _ptr(w.get("B_gu")), _ptr(w.get("A_dn")), _ptr(w.get("B_dn")), _ptr(out_host),
             _ptr(self.status_host), _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream),
             C.byref(h)))
         self.handle = h

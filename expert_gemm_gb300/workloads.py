@@ -34,9 +34,9 @@ reduction dimension is contiguous):
   W_gu  [E, 2I, H]   rows [0, I) are the gate projection, rows [I, 2I) the up projection
   W_dn  [E, H, I]
   A_gu  [L, E, r_max, H]   LoRA shrink of gate_up (rows >= rank(a) are zero)
-  Bt_gu [L, E, 2I, r_max]  LoRA expand of gate_up, stored transposed (cols >= rank(a) zero)
+  B_gu  [L, E, r_max, 2I]  LoRA expand of gate_up, the r x 2I matrix B of XAB (rows >= rank(a) zero)
   A_dn  [L, E, r_max, I]
-  Bt_dn [L, E, H, r_max]
+  B_dn  [L, E, r_max, H]
 Mixed ranks: adapter a has rank 16 when a is even and 64 when a is odd.
 
 Determinism: each tensor, and each slice of it along its leading dimension,
@@ -203,19 +203,16 @@ def make_weights(wl: Workload, seed: int = 0) -> dict:
     ranks = np.asarray(wl.ranks, dtype=np.int32)
     s = wl.w_std
 
-    def zero_rows(i, v):      # v: [E, R, K] for adapter i -> rows >= rank are zero
+    def zero_rows(i, v):      # v: [E, R, K or N] for adapter i -> rows >= rank are zero
         v[:, ranks[i]:, :] = 0
-
-    def zero_cols(i, v):      # v: [E, N, R] for adapter i -> cols >= rank are zero
-        v[:, :, ranks[i]:] = 0
 
     w = {
         "W_gu": _normal_bf16(seed, _WGU, (E, 2 * I, H), s),
         "W_dn": _normal_bf16(seed, _WDN, (E, H, I), s),
         "A_gu": _normal_bf16(seed, _AGU, (L, E, R, H), s, zero_rows),
-        "Bt_gu": _normal_bf16(seed, _BGU, (L, E, 2 * I, R), s, zero_cols),
+        "B_gu": _normal_bf16(seed, _BGU, (L, E, R, 2 * I), s, zero_rows),
         "A_dn": _normal_bf16(seed, _ADN, (L, E, R, I), s, zero_rows),
-        "Bt_dn": _normal_bf16(seed, _BDN, (L, E, H, R), s, zero_cols),
+        "B_dn": _normal_bf16(seed, _BDN, (L, E, R, H), s, zero_rows),
         "ranks": ranks,
     }
     return w

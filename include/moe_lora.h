@@ -16,9 +16,9 @@
  * projections ([ZH] "增強重點摘要"), i.e. four extra ops per expert:
  * gate_up_shrink, gate_up_expand, down_shrink, down_expand ([KO] "Amazon 전용 튜닝").
  * For a pair (token t, expert e) with adapter a and rank r = ranks[a]:
- *     g = W_gu[e] x_t + Bt_gu[a,e][:, :r] (A_gu[a,e][:r, :] x_t)          (2I)
+ *     g = W_gu[e] x_t + B_gu[a,e][:r, :]^T (A_gu[a,e][:r, :] x_t)         (2I)
  *     h = silu(g[0:I]) * g[I:2I]                                        (I)
- *     d = W_dn[e] h   + Bt_dn[a,e][:, :r] (A_dn[a,e][:r, :] h)            (H)
+ *     d = W_dn[e] h   + B_dn[a,e][:r, :]^T (A_dn[a,e][:r, :] h)           (H)
  *     out_t = sum_j w_{t,j} d_{t,j}
  * where the weights w are the softmax over the E router logits, kept for the k
  * largest and renormalised; the router and the aggregation of expert outputs are
@@ -86,7 +86,7 @@ typedef struct moe_lora_dims {
     int32_t E;        /* experts, 1..MOE_LORA_MAX_EXPERTS                               */
     int32_t k;        /* experts per token, 1..min(E, MOE_LORA_MAX_TOPK)                */
     int32_t L;        /* adapters, 0..MOE_LORA_MAX_ADAPTERS                             */
-    int32_t r_max;    /* storage rank: rows of A, columns of Bt; multiple of 8, <= 64   */
+    int32_t r_max;    /* storage rank: rows of A and of B; multiple of 8, <= 64         */
     int32_t block_m;  /* rows per align block: 16, 32, 64 (weight-streaming kernels)    */
                       /* or 128, 256 (token-tiled kernels); 0 = the tile table's choice */
                       /* for (T, k, E) (moe_lora_pick_block_m, moe_lora_plan_query)     */
@@ -199,9 +199,12 @@ int moe_lora_route_align(const moe_lora_dims *d, const float *logits, const int3
  *   W_gu    [E][2I][H]        bf16; rows [0,I) gate, rows [I,2I) up
  *   W_dn    [E][H][I]         bf16
  *   A_gu    [L][E][r_max][H]  bf16; rows >= ranks[a] must be zero
- *   Bt_gu   [L][E][2I][r_max] bf16 (B of gate_up, transposed); cols >= ranks[a] zero
+ *   B_gu    [L][E][r_max][2I] bf16, the r x 2I matrix B of XAB for gate_up (columns
+ *                             [0,I) gate, [I,2I) up); rows >= ranks[a] zero
  *   A_dn    [L][E][r_max][I]  bf16; rows >= ranks[a] zero
- *   Bt_dn   [L][E][H][r_max]  bf16; cols >= ranks[a] zero
+ *   B_dn    [L][E][r_max][H]  bf16; rows >= ranks[a] zero
+ *   (A and B rank-major: an adapter's rank-r slice is its first r rows, read as r
+ *   contiguous rows, so a low-rank adapter in a wide bank costs only its own bytes.)
  *   out     [T][H]            bf16, device, out: fully overwritten
  *   workspace  device scratch of at least forward_bytes
  *   dev_status one int32, device: cleared by the call, then receives MOE_LORA_DEV_* bits
@@ -216,8 +219,8 @@ int moe_lora_route_align(const moe_lora_dims *d, const float *logits, const int3
 int moe_lora_forward(const moe_lora_dims *d, const uint16_t *x, const float *topk_w,
                      const moe_lora_align_buf *aligned,
                      const uint16_t *W_gu, const uint16_t *W_dn,
-                     const uint16_t *A_gu, const uint16_t *Bt_gu,
-                     const uint16_t *A_dn, const uint16_t *Bt_dn,
+                     const uint16_t *A_gu, const uint16_t *B_gu,
+                     const uint16_t *A_dn, const uint16_t *B_dn,
                      uint16_t *out, void *workspace, size_t workspace_bytes,
                      int32_t *dev_status, void *stream, void *const *stage_events);
 
@@ -234,8 +237,8 @@ int moe_lora_layer_workspace_size(const moe_lora_dims *d, size_t *bytes);
 int moe_lora_layer_host(const moe_lora_dims *d, const float *logits_host,
                         const int32_t *lora_ids_host, const uint16_t *x_host,
                         const uint16_t *W_gu, const uint16_t *W_dn,
-                        const uint16_t *A_gu, const uint16_t *Bt_gu,
-                        const uint16_t *A_dn, const uint16_t *Bt_dn,
+                        const uint16_t *A_gu, const uint16_t *B_gu,
+                        const uint16_t *A_dn, const uint16_t *B_dn,
                         uint16_t *out_host, void *workspace, size_t workspace_bytes,
                         int64_t *dropped, void *stream);
 
@@ -261,8 +264,8 @@ typedef struct moe_lora_graph moe_lora_graph;
 int moe_lora_layer_graph_create(const moe_lora_dims *d, const float *logits_host,
                                 const int32_t *lora_ids_host, const uint16_t *x_host,
                                 const uint16_t *W_gu, const uint16_t *W_dn,
-                                const uint16_t *A_gu, const uint16_t *Bt_gu,
-                                const uint16_t *A_dn, const uint16_t *Bt_dn,
+                                const uint16_t *A_gu, const uint16_t *B_gu,
+                                const uint16_t *A_dn, const uint16_t *B_dn,
                                 uint16_t *out_host, int32_t *status_host,
                                 void *workspace, size_t workspace_bytes, void *stream,
                                 moe_lora_graph **graph);

@@ -213,6 +213,19 @@ int oracle_align(int64_t T, int32_t E, int32_t k, int32_t L, int32_t BM,
 
 static double silu(double z) { return z / (1.0 + exp(-z)); }
 
+/* y[n] = sum_{c < rows} M[c][n] * v[c] for n < cols, M row-major bf16 with row pitch
+ * `pitch` (v times the first `rows` rows of M). */
+static void vecmat_bf16(const uint16_t *M, int64_t rows, int64_t cols, int64_t pitch,
+                        const double *v, double *y)
+{
+    for (int64_t n = 0; n < cols; ++n) y[n] = 0.0;
+    for (int64_t c = 0; c < rows; ++c) {
+        const uint16_t *m = M + c * pitch;
+        const double vc = v[c];
+        for (int64_t n = 0; n < cols; ++n) y[n] += bf16_to_double(m[n]) * vc;
+    }
+}
+
 /* y[n] = sum_c M[n][c] * v[c] for n < rows, M row-major bf16 with row pitch `pitch`. */
 static void matvec_bf16(const uint16_t *M, int64_t rows, int64_t cols, int64_t pitch,
                         const double *v, double *y)
@@ -231,10 +244,10 @@ static void matvec_bf16(const uint16_t *M, int64_t rows, int64_t cols, int64_t p
  *   out_t = sum over valid pairs (t, j) of w_{t,j} * d_{t,j}, where with e = topk_ids[t][j],
  *   a = lora_ids[t], r = ranks[a]:
  *     g   = W_gu[e] x_t                                   (2I)
- *     g  += Bt_gu[a][e][:, 0:r] (A_gu[a][e][0:r, :] x_t)  if a >= 0   (gate_up shrink, expand)
+ *     g  += (A_gu[a][e][0:r, :] x_t) B_gu[a][e][0:r, :]   if a >= 0   (gate_up shrink, expand)
  *     h_i = silu(g_i) * g_{I+i}                           (I)
  *     d   = W_dn[e] h                                     (H)
- *     d  += Bt_dn[a][e][:, 0:r] (A_dn[a][e][0:r, :] h)    if a >= 0   (down shrink, expand)
+ *     d  += (A_dn[a][e][0:r, :] h) B_dn[a][e][0:r, :]     if a >= 0   (down shrink, expand)
  * Tokens without a valid pair get out_t = 0.  *n_dropped counts invalid pairs seen.
  */
 void oracle_forward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t k, int32_t L,
@@ -242,8 +255,8 @@ void oracle_forward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t k, int32
                     const uint16_t *x, const int32_t *topk_ids, const float *topk_w,
                     const int32_t *lora_ids,
                     const uint16_t *W_gu, const uint16_t *W_dn,
-                    const uint16_t *A_gu, const uint16_t *Bt_gu,
-                    const uint16_t *A_dn, const uint16_t *Bt_dn,
+                    const uint16_t *A_gu, const uint16_t *B_gu,
+                    const uint16_t *A_dn, const uint16_t *B_dn,
                     const int64_t *tokens, int64_t n_tokens,
                     double *out, int64_t *n_dropped)
 {
@@ -276,8 +289,8 @@ void oracle_forward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t k, int32
                     const int64_t ae = (int64_t)a * E + e;
                     /* gate_up shrink: s = A x */
                     matvec_bf16(A_gu + ae * r_max * H, r, H, H, xt, s);
-                    /* gate_up expand: g += B^T s */
-                    matvec_bf16(Bt_gu + ae * 2 * I * r_max, 2 * (int64_t)I, r, r_max, s, u);
+                    /* gate_up expand: g += s B (B: r_max rows of 2I) */
+                    vecmat_bf16(B_gu + ae * r_max * 2 * I, r, 2 * (int64_t)I, 2 * (int64_t)I, s, u);
                     for (int32_t n = 0; n < 2 * I; ++n) g[n] += u[n];
                 }
                 for (int32_t c = 0; c < I; ++c) h[c] = silu(g[c]) * g[I + c];
@@ -288,7 +301,7 @@ void oracle_forward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t k, int32
                     const int32_t r = ranks[a];
                     const int64_t ae = (int64_t)a * E + e;
                     matvec_bf16(A_dn + ae * r_max * I, r, I, I, h, s);          /* down shrink */
-                    matvec_bf16(Bt_dn + ae * H * r_max, H, r, r_max, s, u);      /* down expand */
+                    vecmat_bf16(B_dn + ae * r_max * H, r, H, H, s, u);          /* down expand */
                     for (int32_t n = 0; n < H; ++n) d[n] += u[n];
                 }
                 /* weighted combine over the k experts */

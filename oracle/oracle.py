@@ -120,7 +120,7 @@ class Oracle:
         I = I2 // 2
         L, _, R, _ = w["A_gu"].shape
         ranks = np.ascontiguousarray(w["ranks"], dtype=np.int32)
-        arrs = [np.ascontiguousarray(w[n], dtype=np.uint16) for n in ("W_gu", "W_dn", "A_gu", "Bt_gu", "A_dn", "Bt_dn")]
+        arrs = [np.ascontiguousarray(w[n], dtype=np.uint16) for n in ("W_gu", "W_dn", "A_gu", "B_gu", "A_dn", "B_dn")]
         if tokens is None:
             tok_p, n_out = None, T
         else:

@@ -51,7 +51,7 @@ def dev_weights(w: dict, torch):
     if key not in _dev_cache:
         _dev_cache.clear()
         torch.cuda.empty_cache()
-        _dev_cache[key] = {n: to_dev(w[n], torch) for n in ("W_gu", "W_dn", "A_gu", "Bt_gu", "A_dn", "Bt_dn")}
+        _dev_cache[key] = {n: to_dev(w[n], torch) for n in ("W_gu", "W_dn", "A_gu", "B_gu", "A_dn", "B_dn")}
     return _dev_cache[key]
 
 

@@ -99,10 +99,10 @@ def moe_base_batched(x_bits, topk_ids, topk_w, W_gu_bits, W_dn_bits):
 
 
 def moe_merged(x_bits, topk_ids, topk_w, lora_ids, w):
-    """MoE with each adapter merged into its expert's weights: W' = W + B^T[:, :r] A[:r, :]."""
+    """MoE with each adapter merged into its expert's weights: W' = W + B[:r, :]^T A[:r, :]."""
     X = f64(x_bits)
     Wg, Wd = f64(w["W_gu"]), f64(w["W_dn"])
-    Ag, Bg, Ad, Bd = f64(w["A_gu"]), f64(w["Bt_gu"]), f64(w["A_dn"]), f64(w["Bt_dn"])
+    Ag, Bg, Ad, Bd = f64(w["A_gu"]), f64(w["B_gu"]), f64(w["A_dn"]), f64(w["B_dn"])
     ranks = w["ranks"]
     E, I2, H = Wg.shape
     I = I2 // 2
@@ -117,8 +117,8 @@ def moe_merged(x_bits, topk_ids, topk_w, lora_ids, w):
             Mg, Md = Wg[e], Wd[e]
             if a >= 0:
                 r = int(ranks[a])
-                Mg = Mg + Bg[a, e][:, :r] @ Ag[a, e][:r, :]
-                Md = Md + Bd[a, e][:, :r] @ Ad[a, e][:r, :]
+                Mg = Mg + Bg[a, e][:r, :].T @ Ag[a, e][:r, :]
+                Md = Md + Bd[a, e][:r, :].T @ Ad[a, e][:r, :]
             g = Mg @ X[t]
             d = Md @ (silu(g[:I]) * g[I:])
             out[t] += float(topk_w[t, j]) * d

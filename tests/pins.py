@@ -137,8 +137,8 @@ def pin_forward_zero_B(o):
     ids, w = o.route(d["logits"], wl.k)
     w = w.astype(np.float32)
     wz = dict(d)
-    wz["Bt_gu"] = np.zeros_like(d["Bt_gu"])
-    wz["Bt_dn"] = np.zeros_like(d["Bt_dn"])
+    wz["B_gu"] = np.zeros_like(d["B_gu"])
+    wz["B_dn"] = np.zeros_like(d["B_dn"])
     a = o.forward(d["x"], ids, w, d["lora_ids"], wz)
     b = o.forward(d["x"], ids, w, np.full(wl.T, -1, np.int32), d)
     assert np.array_equal(a, b)
@@ -201,7 +201,7 @@ def pin_forward_rank_padding_unread(o):
     ref = o.forward(d["x"], ids, w, d["lora_ids"], d)
     g = np.random.default_rng(9)
     dd = dict(d)
-    for name, axis in (("A_gu", 2), ("A_dn", 2), ("Bt_gu", 3), ("Bt_dn", 3)):
+    for name, axis in (("A_gu", 2), ("A_dn", 2), ("B_gu", 2), ("B_dn", 2)):
         arr = d[name].copy()
         for a, r in enumerate(d["ranks"]):
             sl = [a, slice(None), slice(None), slice(None)]
@@ -223,7 +223,7 @@ def pin_forward_golden(o):
     doc = json.load(open(os.path.join(GOLDEN, "hand_layer.json")))
     cm = doc["common"]
     bits = lambda v: f32_to_bf16_bits(np.array(v, dtype=np.float32))   # noqa: E731
-    wts = {n: bits(cm[n]) for n in ("W_gu", "W_dn", "A_gu", "Bt_gu", "A_dn", "Bt_dn")}
+    wts = {n: bits(cm[n]) for n in ("W_gu", "W_dn", "A_gu", "B_gu", "A_dn", "B_dn")}
     wts["ranks"] = np.array(cm["ranks"], dtype=np.int32)
     for c in doc["cases"]:
         logits = np.array(c["logits"], dtype=np.float32)

@@ -21,8 +21,10 @@ MUTANTS = [
      "for (int32_t n = 0; n < 2 * I; ++n) g[n] += 0.0 * u[n];"),
     ("down_expand_dropped", "for (int32_t n = 0; n < H; ++n) d[n] += u[n];",
      "for (int32_t n = 0; n < H; ++n) d[n] += 0.0 * u[n];"),
-    ("expand_pitch_wrong", "matvec_bf16(Bt_dn + ae * H * r_max, H, r, r_max, s, u);",
-     "matvec_bf16(Bt_dn + ae * H * r_max, H, r, r, s, u);"),
+    ("expand_adapter_stride_wrong", "vecmat_bf16(B_dn + ae * r_max * H, r, H, H, s, u);",
+     "vecmat_bf16(B_dn + ae * r * H, r, H, H, s, u);"),
+    ("expand_transposed", "vecmat_bf16(B_gu + ae * r_max * 2 * I, r, 2 * (int64_t)I, 2 * (int64_t)I, s, u);",
+     "matvec_bf16(B_gu + ae * r_max * 2 * I, 2 * (int64_t)I, r, r_max, s, u);"),
     ("shrink_reads_x_in_down", "matvec_bf16(A_dn + ae * r_max * I, r, I, I, h, s);",
      "matvec_bf16(A_dn + ae * r_max * I, r, I, I, xt, s);"),
     ("combine_weight_ignored", "o[c] += w * d[c];", "o[c] += d[c];"),
