@@ -127,7 +127,7 @@ def workload_of(args) -> W.Workload:
 
 # -------------------------------------------------------------- our arm -----
 
-KERNEL_SOURCES = ("gemm_tc.cuh", "ptx.cuh", "common.cuh", "gemm_tc.cu")
+KERNEL_SOURCES = ("gemm_tc.cuh", "ptx.cuh", "common.cuh", "gemm_tc.cu", "moe_lora.cu")   # kernels and their tensor maps
 
 
 def kernel_source_hash() -> str:

@@ -68,6 +68,8 @@ struct GemmMaps {
   CUtensorMap lw;     // LoRA expand weights, rank-major (B_gu 5D / B_dn 4D)
   CUtensorMap ls;     // S run tiles 3D
   CUtensorMap out;    // CTA-pair gate_up / down: output rows (h_sorted / y, bf16) 2D, box {64, 32}
+  CUtensorMap w_rank[3];   // kShrink: A with boxes of 32, 48 and 64 rank rows (w: 16), so a
+                           //   stage loads its adapter's ranks with one TMA
 };
 
 // Launchers (defined next to their kernels).

@@ -56,14 +56,17 @@ struct GemmCfg {
   static constexpr uint32_t SW = BK == 64 ? kSw128 : kSw64;
   static constexpr uint32_t SBO = 8 * ROWB;           // bytes between 8-row core groups
   static constexpr int CPS = BK / kRankChunk;         // LoRA rank chunks per stage
-  // weight-side rows staged per K-tile
-  static constexpr int WROWS = MODE == kShrink ? (SWAP ? 128 : 64) : (CTA2 ? 128 : 256);
+  // weight-side rows staged per K-tile (a shrink's A: rank <= 64 rows, so the weight-
+  // streaming shrink issues M = 64 MMAs over them)
+  static constexpr int WROWS = MODE == kShrink ? 64 : (CTA2 ? 128 : 256);
+  static constexpr int WM = SWAP ? (MODE == kShrink ? 64 : 128) : 0;   // MMA M of weight-streaming tiles
   static constexpr int W_BYTES = WROWS * ROWB;
   static constexpr int T_BYTES = TROWS * ROWB;
   static constexpr int STAGE_BYTES = W_BYTES + T_BYTES;
   // (16-token weight-streaming tiles: 3 stages, so two CTAs share an SM and a GEMM CTA
   // fits beside a shrink CTA -- measured faster on the decode shapes; 32/64: 5)
-  static constexpr int STAGES = MODE == kShrink ? 4
+  // (weight-streaming shrink: 10-16 KB stages, 8 deep, 6 for 64-token tiles)
+  static constexpr int STAGES = MODE == kShrink ? (SWAP ? (BT <= 32 ? 8 : 6) : 4)
                                 : SWAP           ? (BT <= 16 ? 3 : 5)
                                 : CTA2           ? 5   // + 32 KB of output staging
                                                  : (192 * 1024) / STAGE_BYTES;
@@ -331,6 +334,8 @@ __global__ void __launch_bounds__(192, 1)
     if (lane == 0) {
       tma_prefetch_desc(&maps.w);
       tma_prefetch_desc(&maps.tok);
+      if constexpr (MODE == kShrink)
+        for (int j = 0; j < 3; ++j) tma_prefetch_desc(&maps.w_rank[j]);
       if constexpr (C::kLora) {
         tma_prefetch_desc(&maps.lw);
         tma_prefetch_desc(&maps.ls);
@@ -396,10 +401,11 @@ __global__ void __launch_bounds__(192, 1)
               tma_load_3d(wdst, &maps.w, fb, k0, t.f0, t.e);
               tma_load_3d(wdst + 128 * C::ROWB, &maps.w, fb, k0, t.f0 + 128, t.e);
             } else {
+              // the adapter's rank rows in one box: the producer thread's issue loop, not
+              // the bytes, paces the shrink's stages
               const int ae = t.sa * prm.E + t.e;
               mbar_arrive_expect_tx(fb, t.snch * kRankChunk * C::ROWB + C::T_BYTES);
-              for (int c = 0; c < t.snch; ++c)
-                tma_load_3d(wdst + c * kRankChunk * C::ROWB, &maps.w, fb, k0, c * kRankChunk, ae);
+              tma_load_3d(wdst, t.snch <= 1 ? &maps.w : &maps.w_rank[t.snch - 2], fb, k0, 0, ae);
             }
             tma_load_2d(tdst, &maps.tok, fb, k0, t.row0);
           } else if constexpr (C::kLora) {
@@ -508,7 +514,7 @@ __global__ void __launch_bounds__(192, 1)
         tc_fence_after_sync();
         const uint32_t acc_base = tmem + ab * C::ACC_COLS;
         // instruction descriptors of this tile's base and LoRA K-steps
-        const uint32_t id_base = SWAP ? idesc_bf16_f32(128, BT)
+        const uint32_t id_base = SWAP ? idesc_bf16_f32(C::WM, BT)
                                       : idesc_bf16_f32(kM, MODE == kShrink ? t.snch * kRankChunk : 256);
         constexpr uint32_t id_lora =
             SWAP ? (idesc_bf16_f32(128, BT) | kIdescAMn) : (idesc_bf16_f32(kM, 256) | kIdescBMn);
@@ -601,6 +607,9 @@ __global__ void __launch_bounds__(192, 1)
           const int end = prm.runs[4 * t.srun + 3] - row0;
           const int r_a = prm.ranks[t.sa];
           uint16_t* srun = prm.s_out + static_cast<size_t>(t.srun) * BT * prm.r_pad;
+          // weight-streaming (M = 64 accumulator): rank row mr sits in lane mr % 16 of
+          // TMEM lane quarter mr / 16
+          const int mr = lane < 16 ? 16 * q + lane : (1 << 30);
           if constexpr (!SWAP) {
             // row mt*128 + m of the token block; columns are ranks
             for (int mt = 0; mt < C::MT; ++mt) {
@@ -628,35 +637,35 @@ __global__ void __launch_bounds__(192, 1)
               }
             }
           } else if (prm.ksplit == 1) {
-            // row m is rank index m; columns are the BT tokens of the block
+            // rank row mr; columns are the BT tokens of the block
             for (int n0 = 0; n0 < BT; n0 += 16) {
               tmem_ld16(tq + n0, v);
               tmem_ld_wait();
-              if (m < prm.r_pad) {
+              if (mr < prm.r_pad) {
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                   const int n = n0 + j;
-                  const float val = (n >= beg && n < end && m < r_a) ? __uint_as_float(v[j]) : 0.f;
+                  const float val = (n >= beg && n < end && mr < r_a) ? __uint_as_float(v[j]) : 0.f;
                   __nv_bfloat16 hv = __float2bfloat16_rn(val);
-                  srun[static_cast<size_t>(n) * prm.r_pad + m] = *reinterpret_cast<uint16_t*>(&hv);
+                  srun[static_cast<size_t>(n) * prm.r_pad + mr] = *reinterpret_cast<uint16_t*>(&hv);
                 }
               }
             }
           } else {
-            // K split: each epilogue warp owns 32 rank rows.  It stores this split's
+            // K split: each epilogue warp owns 16 rank rows.  It stores this split's
             // fp32 partial S for them, then counts itself in on a per-(run, warp)
             // arrival counter; the warp that completes the count (no waiting) sums
             // all splits' partials and writes those rows of the bf16 S tile.
             // Partials: [split][run][BT][r_pad]; counters: [run][4].
-            if (q * 32 < prm.r_pad) {
+            if (q * 16 < prm.r_pad) {
               const size_t part = (static_cast<size_t>(t.ks) * prm.max_runs + t.srun) * BT * prm.r_pad;
               for (int n0 = 0; n0 < BT; n0 += 16) {
                 tmem_ld16(tq + n0, v);
                 tmem_ld_wait();
-                if (m < prm.r_pad) {
+                if (mr < prm.r_pad) {
 #pragma unroll
                   for (int j = 0; j < 16; ++j)
-                    prm.s_part[part + static_cast<size_t>(n0 + j) * prm.r_pad + m] = __uint_as_float(v[j]);
+                    prm.s_part[part + static_cast<size_t>(n0 + j) * prm.r_pad + mr] = __uint_as_float(v[j]);
                 }
               }
               __threadfence();
@@ -666,15 +675,15 @@ __global__ void __launch_bounds__(192, 1)
               last = __shfl_sync(0xffffffffu, last, 0);
               if (last) {
                 __threadfence();
-                if (m < prm.r_pad) {
+                if (mr < prm.r_pad) {
                   for (int n = 0; n < BT; ++n) {
                     float sum = 0.f;
                     for (int sp = 0; sp < prm.ksplit; ++sp)
                       sum += __ldcg(prm.s_part + (static_cast<size_t>(sp) * prm.max_runs + t.srun) * BT * prm.r_pad +
-                                    static_cast<size_t>(n) * prm.r_pad + m);
-                    const float val = (n >= beg && n < end && m < r_a) ? sum : 0.f;
+                                    static_cast<size_t>(n) * prm.r_pad + mr);
+                    const float val = (n >= beg && n < end && mr < r_a) ? sum : 0.f;
                     __nv_bfloat16 hv = __float2bfloat16_rn(val);
-                    srun[static_cast<size_t>(n) * prm.r_pad + m] = *reinterpret_cast<uint16_t*>(&hv);
+                    srun[static_cast<size_t>(n) * prm.r_pad + mr] = *reinterpret_cast<uint16_t*>(&hv);
                   }
                 }
               }

@@ -479,15 +479,22 @@ int do_forward(const moe_lora_dims* d, const uint16_t* x, const float* topk_w, c
     MOE_TRY(encode(&m_sdn.tok, hs, 2, dm, st, bxs, swz(bk_sh), "h_sorted"));
   }
   if (d->L > 0) {
-    {
-      const uint64_t dm[3] = {H, R, LE}, st[2] = {H * 2, R * H * 2};
-      const uint32_t bx[3] = {64, 16, 1};
-      MOE_TRY(encode(&m_sgu.w, A_gu, 3, dm, st, bx, CU_TENSOR_MAP_SWIZZLE_128B, "A_gu"));
-    }
-    {
-      const uint64_t dm[3] = {I, R, LE}, st[2] = {I * 2, R * I * 2};
-      const uint32_t bx[3] = {64, 16, 1};
-      MOE_TRY(encode(&m_sdn.w, A_dn, 3, dm, st, bx, CU_TENSOR_MAP_SWIZZLE_128B, "A_dn"));
+    // A: one map per rank class, boxes of 16, 32, 48, 64 rows (a stage loads an
+    // adapter's ranks in one TMA; rows past r_max read as zero)
+    for (int c = 0; c < 4; ++c) {
+      const uint32_t rows = 16u * (uint32_t)(c + 1);
+      {
+        const uint64_t dm[3] = {H, R, LE}, st[2] = {H * 2, R * H * 2};
+        const uint32_t bx[3] = {64, rows, 1};
+        MOE_TRY(encode(c == 0 ? &m_sgu.w : &m_sgu.w_rank[c - 1], A_gu, 3, dm, st, bx, CU_TENSOR_MAP_SWIZZLE_128B,
+                       "A_gu"));
+      }
+      {
+        const uint64_t dm[3] = {I, R, LE}, st[2] = {I * 2, R * I * 2};
+        const uint32_t bx[3] = {64, rows, 1};
+        MOE_TRY(encode(c == 0 ? &m_sdn.w : &m_sdn.w_rank[c - 1], A_dn, 3, dm, st, bx, CU_TENSOR_MAP_SWIZZLE_128B,
+                       "A_dn"));
+      }
     }
     // B, rank-major: one box is 16 rank rows of the tile's weight columns, landing as
     // 64-column atoms of 16 rows x 128 bytes (the MN-major 128-byte-swizzle operand
