@@ -165,6 +165,17 @@ def test_all_tokens_one_expert(ml, torch, oracle):
         run_case(ml, torch, oracle, wl, block_m=bm, logits=logits)
 
 
+@pytest.mark.parametrize("block_m", [16, 64, 128, 256])
+def test_ranks_off_the_chunk_grid(ml, torch, oracle, block_m):
+    """Ranks 40, 24, 48, 8 in a rank-48 bank: A boxes of 48 and 32 rows, rank chunks
+    whose last rows are the bank's zero padding, B rows past r_max read as zero; with
+    ragged feature tiles (I = 320, H = 448) in every tile orientation."""
+    wl = W.custom(name="rk48", T=160, H=448, I=320, E=4, k=2, L=4, ranks=(40, 24, 48, 8),
+                  lora_mode="uniform_with_none")
+    assert wl.r_max == 48
+    run_case(ml, torch, oracle, wl, block_m=block_m)
+
+
 def test_single_token(ml, torch, oracle):
     wl = W.custom(name="one", T=1, H=512, I=256, E=16, k=4, L=2, ranks=(16, 16), lora_mode="uniform")
     for bm in (16, 128):
