@@ -34,6 +34,27 @@ __device__ __forceinline__ int lower_bound_u32(const uint32_t* a, int lo, int hi
   return lo;
 }
 
+// Ascending bitonic sort of n (a power of two) keys in shared memory, all threads of
+// the CTA; ends with a barrier.
+__device__ void bitonic_sort(uint32_t* keys, int n) {
+  for (int size = 2; size <= n; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      __syncthreads();
+      for (int i = threadIdx.x; i < n / 2; i += blockDim.x) {
+        const int lo = 2 * i - (i & (stride - 1));
+        const int hi = lo + stride;
+        const bool asc = (lo & size) == 0;
+        const uint32_t x = keys[lo], y = keys[hi];
+        if ((x > y) == asc) {
+          keys[lo] = y;
+          keys[hi] = x;
+        }
+      }
+    }
+  }
+  __syncthreads();
+}
+
 // Phase 1 for one chunk: keys of its pairs sorted in keys[] (shared), per-bucket
 // counts of the chunk and its invalid-pair count written to global scratch.  ids: the
 // expert ids [P] (global, or shared when the same CTA has just routed them).
@@ -61,23 +82,7 @@ __device__ void chunk_phase(const AlignLaunch& a, const int32_t* ids, uint32_t* 
     keys[i] = key;
   }
   if (inval) atomicAdd(&s_invalid, inval);
-  // bitonic sort, ascending
-  for (int size = 2; size <= CH; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      __syncthreads();
-      for (int i = threadIdx.x; i < CH / 2; i += blockDim.x) {
-        const int lo = 2 * i - (i & (stride - 1));
-        const int hi = lo + stride;
-        const bool asc = (lo & size) == 0;
-        const uint32_t x = keys[lo], y = keys[hi];
-        if ((x > y) == asc) {
-          keys[lo] = y;
-          keys[hi] = x;
-        }
-      }
-    }
-  }
-  __syncthreads();
+  bitonic_sort(keys, CH);
   for (int i = threadIdx.x; i < CH; i += blockDim.x) {
     const uint32_t key = keys[i];
     if (store_keys) a.chunk_keys[p0 + i] = key;
@@ -260,15 +265,127 @@ __global__ void __launch_bounds__(1024) align_scatter_kernel(AlignLaunch a) {
   scatter_phase(a, keys, blockIdx.x);
 }
 
-// All three phases in one CTA, for batches that fit one chunk: the sorted keys stay
-// in shared memory and two launches disappear from the decode path.
+// Batches that fit one chunk (P <= 4096) in one CTA.  After the sort the whole layout
+// comes from the sorted keys in shared memory, with work proportional to the pairs,
+// experts and blocks rather than to the E * (L+1) buckets, and no scratch round trips
+// through global memory (the decode front end is latency, not bandwidth).
+//
+// small_keys: the keys of the P pairs sorted in keys[CH]; returns the invalid-pair count.
+__device__ int small_keys(const AlignLaunch& a, const int32_t* ids, uint32_t* keys) {
+  __shared__ int32_t s_invalid;
+  const int CH = 1 << a.ch_log2;
+  const int LB = a.L + 1;
+  if (threadIdx.x == 0) s_invalid = 0;
+  __syncthreads();
+  int inval = 0;
+  for (int i = threadIdx.x; i < CH; i += blockDim.x) {
+    uint32_t key = kInvalidKey;
+    if (i < a.P) {
+      const int e = ids[i];
+      const int ad = a.lora_ids[i / a.k];
+      if (e >= 0 && e < a.E && ad >= -1 && ad < a.L)
+        key = (static_cast<uint32_t>(e * LB + ad + 1) << a.ch_log2) | static_cast<uint32_t>(i);
+      else
+        ++inval;
+    }
+    keys[i] = key;
+  }
+  if (inval) atomicAdd(&s_invalid, inval);
+  bitonic_sort(keys, CH);
+  return s_invalid;
+}
+
+// small_layout: the align outputs from the nv valid sorted keys (keys[0, nv), invalid
+// keys sort last).  s_runblk: shared scratch of nv ints (block of each run).
+__device__ void small_layout(const AlignLaunch& a, const uint32_t* keys, int n_invalid, int32_t* s_runblk) {
+  __shared__ int32_t s_cnt[MOE_LORA_MAX_EXPERTS];      // pairs per expert
+  __shared__ int32_t s_first[MOE_LORA_MAX_EXPERTS];    // sorted position of its first pair
+  __shared__ int32_t s_begin[MOE_LORA_MAX_EXPERTS + 1];  // padded first row
+  __shared__ int32_t s_warp[32];
+  const int tid = threadIdx.x, nt = blockDim.x;
+  const int LB = a.L + 1, BM = a.BM, lg = a.ch_log2;
+  const int nv = static_cast<int>(a.P) - n_invalid;
+  const moe_lora_align_buf& o = a.out;
+  for (int e = tid; e < a.E; e += nt) s_cnt[e] = 0;
+  __syncthreads();
+  for (int i = tid; i < nv; i += nt) {
+    const int e = static_cast<int>(keys[i] >> lg) / LB;
+    if (i == 0 || static_cast<int>(keys[i - 1] >> lg) / LB != e) s_first[e] = i;
+    atomicAdd(&s_cnt[e], 1);
+  }
+  __syncthreads();
+  // each expert padded to a multiple of BM rows; experts without pairs get none
+  const int rows = block_exclusive_scan(
+      a.E, [&](int e) { return (s_cnt[e] + BM - 1) / BM * BM; },
+      [&](int e, int pre) {
+        s_begin[e] = pre;
+        o.expert_begin[e] = pre;
+      },
+      s_warp);
+  if (tid == 0) {
+    s_begin[a.E] = rows;
+    o.expert_begin[a.E] = rows;
+  }
+  __syncthreads();
+  // sorted pair i: bucket, adapter, row; a run (one adapter >= 0 inside one block)
+  // starts where the bucket changes or a block begins, and ends before the next start
+  auto bucket = [&](int i) { return static_cast<int>(keys[i] >> lg); };
+  auto row_of = [&](int i) {
+    const int e = bucket(i) / LB;
+    return s_begin[e] + (i - s_first[e]);
+  };
+  auto starts = [&](int i) -> int {
+    if (bucket(i) % LB == 0) return 0;   // adapter -1: no run
+    return i == 0 || bucket(i - 1) != bucket(i) || row_of(i) % BM == 0;
+  };
+  const int nruns = block_exclusive_scan(
+      nv, starts,
+      [&](int i, int pre) {
+        const int r = row_of(i), b = bucket(i), ad = b % LB - 1;
+        o.sorted_p[r] = static_cast<int32_t>(keys[i] & ((1u << lg) - 1u));
+        if (ad < 0) return;
+        const bool st = starts(i);
+        const int run = pre + (st ? 1 : 0) - 1;
+        int32_t* q = o.runs + 4 * static_cast<int64_t>(run);
+        if (st) {
+          q[0] = r / BM;
+          q[1] = ad;
+          q[2] = r;
+          s_runblk[run] = r / BM;
+        }
+        if (i == nv - 1 || bucket(i + 1) != b || row_of(i + 1) % BM == 0) q[3] = r + 1;
+      },
+      s_warp);
+  // padding sentinels and block experts
+  for (int e = tid; e < a.E; e += nt) {
+    for (int r = s_begin[e] + s_cnt[e]; r < s_begin[e + 1]; ++r) o.sorted_p[r] = static_cast<int32_t>(a.P);
+    for (int blk = s_begin[e] / BM; blk < s_begin[e + 1] / BM; ++blk) o.block_expert[blk] = e;
+  }
+  if (tid == 0) {
+    o.totals[0] = rows;
+    o.totals[1] = rows / BM;
+    o.totals[2] = nruns;
+    o.totals[3] = n_invalid;
+  }
+  __syncthreads();
+  // first run of each block (runs are in block order)
+  const int nblocks = rows / BM;
+  for (int blk = tid; blk <= nblocks; blk += nt) {
+    int lo = 0, hi = nruns;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (s_runblk[mid] < blk) lo = mid + 1;
+      else hi = mid;
+    }
+    o.block_runs[blk] = lo;
+  }
+}
+
 __global__ void __launch_bounds__(1024) align_small_kernel(AlignLaunch a) {
   extern __shared__ uint32_t keys[];
-  chunk_phase(a, a.topk_ids, keys, 0, false);
-  __syncthreads();
-  scan_phase(a);
-  __syncthreads();
-  scatter_phase(a, keys, 0);
+  int32_t* s_runblk = reinterpret_cast<int32_t*>(keys + (1 << a.ch_log2));
+  const int inval = small_keys(a, a.topk_ids, keys);
+  small_layout(a, keys, inval, s_runblk);
 }
 
 // Route and align in one CTA (one chunk): each warp routes tokens into shared memory,
@@ -285,11 +402,8 @@ __global__ void __launch_bounds__(1024) route_align_small_kernel(AlignLaunch a, 
     route_token(logits + static_cast<int64_t>(t) * a.E, a.E, a.k, lane, s_ids + t * a.k, topk_w + t * a.k);
   __syncthreads();
   for (int p = threadIdx.x; p < a.P; p += blockDim.x) topk_ids[p] = s_ids[p];
-  chunk_phase(a, s_ids, keys, 0, false);
-  __syncthreads();
-  scan_phase(a);
-  __syncthreads();
-  scatter_phase(a, keys, 0);
+  const int inval = small_keys(a, s_ids, keys);   // ends with a barrier: s_ids is free again
+  small_layout(a, keys, inval, s_ids);
 }
 
 }  // namespace
@@ -299,7 +413,7 @@ cudaError_t launch_align(const AlignLaunch& a, cudaStream_t s) {
   const int threads = CH < 1024 ? CH : 1024;
   const size_t smem = static_cast<size_t>(CH) * sizeof(uint32_t);
   if (a.nchunks == 1) {
-    align_small_kernel<<<1, 1024, smem, s>>>(a);
+    align_small_kernel<<<1, 1024, smem + static_cast<size_t>(a.P) * sizeof(int32_t), s>>>(a);
     return cudaGetLastError();
   }
   if (a.nchunks > 0) {

@@ -376,12 +376,21 @@ int do_align(const moe_lora_dims* d, const int32_t* topk_ids, const int32_t* lor
 
 // Route then align.  Batches of one align chunk (T*k <= 4096) take a single launch;
 // larger ones the route kernel and the align kernels.
+// Route and align share one single-CTA launch only for a few tokens: in one CTA the
+// router costs ~400 issue cycles per token (measured: 3 us at T = 16, 57 us at T = 256
+// with E = 128, k = 8), while the route kernel gives every token its own warp across
+// the GPU.  Larger one-chunk batches take the route kernel, then the one-CTA align.
+constexpr int64_t kFusedRouteTokens = 32;
+bool fused_route_align(const moe_lora_dims* d, const AlignLayout& l) {
+  return l.nchunks == 1 && d->T <= kFusedRouteTokens;
+}
+
 int do_route_align(const moe_lora_dims* d, const float* logits, const int32_t* lora_ids, int32_t* topk_ids,
                    float* topk_w, const moe_lora_align_buf* out, void* ws, size_t ws_bytes, cudaStream_t s) {
   MOE_RESOLVE(d);
   MOE_TRY(validate_dims(d));
   const AlignLayout l = align_layout(d);
-  if (l.nchunks != 1) {
+  if (!fused_route_align(d, l)) {
     MOE_TRY(do_route(logits, d->T, d->E, d->k, topk_ids, topk_w, s));
     return do_align(d, topk_ids, lora_ids, out, ws, ws_bytes, s);
   }
@@ -698,7 +707,8 @@ int moe_lora_plan_query(const moe_lora_dims* d, moe_lora_plan* out) {
     if (!moe::gemm_stage_shape(modes[g], d->block_m, &p.k_tile[g], &p.stages[g]))
       return fail(MOE_LORA_EUNSUPPORTED, "no GEMM compiled for block_m = %d", d->block_m);
   const int64_t P = d->T * d->k;
-  p.launches_route_align = (P > 0 && P <= 4096) ? 1 : (P == 0 ? 1 : 4);
+  const AlignLayout al = align_layout(d);
+  p.launches_route_align = P == 0 ? 1 : fused_route_align(d, al) ? 1 : al.nchunks == 1 ? 2 : 4;
   // gather (+ its token-order copy when x outgrows L2), shrinks, gate_up (+ SiLU pass
   // after a K split), down, combine
   p.launches_forward =

@@ -14,19 +14,29 @@
 
 namespace moe {
 
-// Lane i owns experts i, i+32, ... (E <= 1024 -> 32 per lane).  Lane 0 writes the k
+// Lane i owns experts i, i+32, ... (SLOTS per lane, E <= 32 * SLOTS), read into
+// registers once; the k selection passes then run on registers.  Lane 0 writes the k
 // ids and weights of the token to ids[0..k) and wts[0..k) (any address space).
-__device__ __forceinline__ void route_token(const float* __restrict__ l, int E, int k, int lane, int32_t* ids,
-                                            float* wts) {
+template <int SLOTS>
+__device__ __forceinline__ void route_token_n(const float* __restrict__ l, int E, int k, int lane, int32_t* ids,
+                                              float* wts) {
+  float lv[SLOTS];
+#pragma unroll
+  for (int s = 0; s < SLOTS; ++s) {
+    const int ex = lane + 32 * s;
+    lv[s] = ex < E ? l[ex] : 0.f;
+  }
   uint32_t taken = 0;   // bit s: expert lane + 32*s already chosen
   float vals[MOE_LORA_MAX_TOPK];
   int chosen[MOE_LORA_MAX_TOPK];
   for (int j = 0; j < k; ++j) {
     float bv = -INFINITY;
     int bi = 0x7fffffff;
-    for (int s = 0, ex = lane; ex < E; ++s, ex += 32) {
-      if (taken & (1u << s)) continue;
-      const float v = l[ex];
+#pragma unroll
+    for (int s = 0; s < SLOTS; ++s) {
+      const int ex = lane + 32 * s;
+      if (ex >= E || (taken & (1u << s))) continue;
+      const float v = lv[s];
       if (bi == 0x7fffffff || v > bv || (v == bv && ex < bi)) {
         bv = v;
         bi = ex;
@@ -55,6 +65,16 @@ __device__ __forceinline__ void route_token(const float* __restrict__ l, int E, 
       wts[j] = expf(vals[j] - mx) * inv;
     }
   }
+}
+
+// route_token_n with the fewest register slots that hold E experts (warp-uniform E).
+__device__ __forceinline__ void route_token(const float* __restrict__ l, int E, int k, int lane, int32_t* ids,
+                                            float* wts) {
+  if (E <= 32) route_token_n<1>(l, E, k, lane, ids, wts);
+  else if (E <= 64) route_token_n<2>(l, E, k, lane, ids, wts);
+  else if (E <= 128) route_token_n<4>(l, E, k, lane, ids, wts);
+  else if (E <= 256) route_token_n<8>(l, E, k, lane, ids, wts);
+  else route_token_n<(MOE_LORA_MAX_EXPERTS + 31) / 32>(l, E, k, lane, ids, wts);
 }
 
 }  // namespace moe

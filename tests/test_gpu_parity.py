@@ -176,6 +176,17 @@ def test_ranks_off_the_chunk_grid(ml, torch, oracle, block_m):
     run_case(ml, torch, oracle, wl, block_m=block_m)
 
 
+@pytest.mark.parametrize("T,k", [(512, 8), (4097, 1)])
+def test_align_one_chunk_boundary(ml, torch, oracle, T, k):
+    """P = 4096 pairs, the largest batch the one-CTA align takes (layout from the sorted
+    keys in shared memory), and P = 4097, the smallest the chunked align takes; many
+    experts and Zipf adapters with 10% none, bit-exact against the oracle."""
+    wl = W.custom(name=f"edge{T}x{k}", T=T, H=128, I=128, E=64, k=k, L=32, ranks=(16,) * 32,
+                  lora_mode="zipf_with_none", bias_std=0.5, none_frac=0.1)
+    for bm in (16, 128):
+        run_case(ml, torch, oracle, wl, block_m=bm)
+
+
 def test_single_token(ml, torch, oracle):
     wl = W.custom(name="one", T=1, H=512, I=256, E=16, k=4, L=2, ranks=(16, 16), lora_mode="uniform")
     for bm in (16, 128):

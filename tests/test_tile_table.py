@@ -69,6 +69,17 @@ def test_decode_plan():
     assert p["launches_forward"] == 6      # gather, 2 shrinks, gate_up, down, combine
 
 
+def test_route_align_launches():
+    """Route and align fuse into one single-CTA launch only for a few tokens (T <= 32 and
+    one sort chunk); larger one-chunk batches launch the route kernel, then the one-CTA
+    align; more than 4096 pairs take the chunked align (route + chunk/scan/scatter)."""
+    assert ml.plan(dims(W.get("decode"), 0))["launches_route_align"] == 1      # T = 16
+    assert ml.plan(dims(W.get("sweep_T16"), 0))["launches_route_align"] == 1   # T = 16, 128 pairs
+    assert ml.plan(dims(W.get("sweep_T256"), 0))["launches_route_align"] == 2  # 2048 pairs
+    assert ml.plan(dims(W.get("tiny"), 0))["launches_route_align"] == 2        # T = 64
+    assert ml.plan(dims(W.get("sweep_T4096"), 0))["launches_route_align"] == 4
+
+
 def test_prefill_plan():
     p = ml.plan(dims(W.get("prefill"), 0))
     assert p["block_m"] == 256 and not p["weight_streaming"]
