@@ -305,16 +305,20 @@ int gate_up_ksplit(const moe_lora_dims* d, const Caps& cap) {
 }
 // The weight-streaming shrink splits K only for long reductions whose runs cannot fill
 // the SMs -- a run's tile otherwise walks all of K alone.  Measured: splitting short
-// reductions only adds per-tile overhead and keeps the SMs from the next kernel.
-// About one tile per SM, each split at least 16 K-tiles.
+// reductions only adds per-tile overhead and keeps the SMs from the next kernel
+// (decode: 57 runs of 45 K-tiles; a single token's 8 runs of 32 K-tiles: 67 -> 70 us
+// split 4 ways).  About one tile per SM, each split at least 16 K-tiles, or 8 when the
+// runs are a handful (at most one per 8 SMs; dense_decode: 0.197 -> 0.193 ms).
 int shrink_ksplit(const moe_lora_dims* d, const Caps& cap, int K) {
   const TileClass& tc = kTileTable[block_row(d->block_m)];
   const int64_t nk = K / 64;
+  const bool few = cap.runs > 0 && cap.runs * 8 <= kPlanSMs;
   if (d->block_m >= 128 || d->L == 0 || cap.runs <= 0 || tc.shrink_min_ktiles <= 0 || nk < tc.shrink_min_ktiles ||
       cap.runs >= kPlanSMs)
     return 1;
   int64_t ks = ((int64_t)kPlanSMs + cap.runs - 1) / cap.runs;
-  const int64_t ks_max = nk / 16 < tc.shrink_max_splits ? nk / 16 : tc.shrink_max_splits;
+  const int64_t per = few ? 8 : 16;
+  const int64_t ks_max = nk / per < tc.shrink_max_splits ? nk / per : tc.shrink_max_splits;
   if (ks > ks_max) ks = ks_max;
   return ks < 1 ? 1 : (int)ks;
 }

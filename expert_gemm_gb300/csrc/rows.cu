@@ -177,7 +177,9 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const void* __
                                                                   int H8, int ns, uint4* __restrict__ out) {
   __shared__ int32_t s_row[kCombineThreads / 32][MOE_LORA_MAX_TOPK];
   __shared__ float s_w[kCombineThreads / 32][MOE_LORA_MAX_TOPK];
-  pdl_wait();   // the down GEMM's rows are complete
+  // The pair lookups read what the gather, align and route wrote: those finished before
+  // the down GEMM could start (each kernel of the chain lets its dependent launch only
+  // after its own wait), so only the expert rows below wait for the down GEMM.
   const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
   const int64_t gw = static_cast<int64_t>(blockIdx.x) * (kCombineThreads / 32) + wib;
   if (gw >= T * ns) return;
@@ -199,6 +201,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const void* __
     s_w[wib][slot] = w;
   }
   __syncwarp();
+  pdl_wait();   // the down GEMM's rows are complete
   const int n = __popc(valid);
   const int per = (H8 + ns - 1) / ns;
   const int c_end = min(H8, (slab + 1) * per);
