@@ -18,7 +18,7 @@ ROOT = os.path.dirname(PKG)
 OBJ = os.path.join(ROOT, "_build", "obj")
 LIB = os.path.join(PKG, "libmoe_lora.so")
 
-SOURCES = ["moe_lora.cu", "route.cu", "align.cu", "rows.cu", "gemm_tc.cu"]
+SOURCES = ["moe_lora.cu", "route.cu", "align.cu", "rows.cu", "shrink_rows.cu", "gemm_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", os.path.join(ROOT, "include")]

@@ -116,6 +116,23 @@ cudaError_t launch_combine(const void* y, int ksplit, int64_t part_rows, const i
 // g being the sum of the ksplit partial buffers [ksplit][part_rows][2I] in split order.
 cudaError_t launch_silu_rows(const float* g_part, int ksplit, int64_t part_rows, const int32_t* totals,
                              int64_t max_rows, int I, uint16_t* h, bool pdl, cudaStream_t s);
+// LoRA shrink of short runs on CUDA cores (weight-streaming blocks, block_m <= 64):
+// one CTA per (run, kShrinkSlice-wide K slice); fp32 slice partials added in slice
+// order by the CTA that completes the run's count (s_cnt[4 * run], zero at launch).
+constexpr int kShrinkSlice = 256;
+struct ShrinkRowsLaunch {
+  const uint16_t* xs;           // token rows in sorted order [rows][K]
+  const uint16_t* A;            // [L*E][r_max][K]
+  const int32_t* runs;          // [runs][4] {block, adapter, begin, end}
+  const int32_t* block_expert;  // [blocks]
+  const int32_t* totals;        // {rows, blocks, runs, dropped}
+  float* s_part;                // [slices][max_runs][block_m][r_pad] fp32
+  int32_t* s_cnt;               // [max_runs][4]
+  uint16_t* s_out;              // [runs][block_m][r_pad] bf16
+  int32_t K, E, r_max, r_pad, block_m, slices, max_runs;
+  int32_t ranks[MOE_LORA_MAX_ADAPTERS];
+};
+cudaError_t launch_shrink_rows(const ShrinkRowsLaunch& a, int64_t max_runs, bool pdl, cudaStream_t s);
 // pdl: launch with programmatic stream serialisation (may overlap the previous kernel).
 cudaError_t launch_gemm(int mode, int bt, const GemmMaps& maps, const GemmParams& prm, int64_t max_blocks,
                         int64_t max_runs, bool pdl, cudaStream_t s);

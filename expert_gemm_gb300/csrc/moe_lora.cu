@@ -116,13 +116,14 @@ struct TileClass {
   int dn_tiles_per_cta;   // weight-streaming down: the same
   int shrink_min_ktiles;  // weight-streaming shrink: split K only from this many 64-wide K-tiles
   int shrink_max_splits;
+  int shrink_cores;       // 1: the shrinks run on CUDA cores (short runs, split over K), else tcgen05
 };
 constexpr TileClass kTileTable[] = {
-    {-1.0, 16, 2, 6, 64, 8},    // up to 10 pairs per expert (decode batches)
-    {10.0, 32, 2, 6, 64, 8},    // 10 .. 24
-    {24.0, 64, 2, 6, 64, 8},    // 24 .. 95
-    {95.0, 128, 1, 1, 0, 1},    // 95 .. 2047: token-tiled, compute-bound, no K split
-    {2047.0, 256, 1, 1, 0, 1},  // more than 2047: 256-token blocks on CTA pairs
+    {-1.0, 16, 2, 6, 64, 8, 1},    // up to 10 pairs per expert (decode batches)
+    {10.0, 32, 2, 6, 64, 8, 1},    // 10 .. 24
+    {24.0, 64, 2, 6, 64, 8, 1},    // 24 .. 95
+    {95.0, 128, 1, 1, 0, 1, 0},    // 95 .. 2047: token-tiled, compute-bound, no K split
+    {2047.0, 256, 1, 1, 0, 1, 0},  // more than 2047: 256-token blocks on CTA pairs
 };
 constexpr int kTableRows = sizeof(kTileTable) / sizeof(kTileTable[0]);
 
@@ -207,6 +208,25 @@ struct FwdLayout {
 };
 constexpr int kNumGemmCounters = 4;   // tile counters: shrink_gu, gate_up, shrink_dn, down
 constexpr int kPlanSMs = 152;         // SM count the K-split heuristics plan for (GB300)
+// Whether the shrinks run on CUDA cores (shrink_rows) rather than as tcgen05 tiles, and
+// over how many K slices.  The tensor-core shrink is a chain of dependent TMA round
+// trips per run; behind a long base-weight stream (the GEMM after it starts streaming
+// at once) it is hidden, and a CUDA-core shrink only takes SMs from that stream
+// (measured: decode 0.285 -> 0.299 ms, dense_decode 0.193 -> 0.201 ms).  When the
+// stream is short -- gate_up's weights of at most min(E, T*k) experts under ~128 MB --
+// and the runs are a handful (at most one per 8 SMs: a single token's experts), the
+// shrink is the critical path and a run's tile chain is long; split over K on CUDA
+// cores it is shorter (one token over 128 experts: 65 -> 61 us).  With tens of short
+// runs the tensor-core tiles already spread over the SMs (the 64-token test layer:
+// 46 us against 48 on CUDA cores).
+constexpr double kShrinkCoresMaxStreamBytes = 128.0 * 1024 * 1024;
+bool shrink_on_cores(const moe_lora_dims* d, const Caps& cap) {
+  if (d->L <= 0 || d->block_m >= 128 || kTileTable[block_row(d->block_m)].shrink_cores == 0) return false;
+  if (cap.runs <= 0 || cap.runs * 8 > kPlanSMs) return false;
+  const double experts = (double)(d->T * d->k < d->E ? d->T * d->k : d->E);
+  return experts * 2.0 * d->I * d->H * 2.0 <= kShrinkCoresMaxStreamBytes;
+}
+int shrink_slices(int K) { return (K + moe::kShrinkSlice - 1) / moe::kShrinkSlice; }
 int shrink_ksplit(const moe_lora_dims* d, const Caps& cap, int K);
 int gate_up_ksplit(const moe_lora_dims* d, const Caps& cap);
 int down_ksplit(const moe_lora_dims* d, const Caps& cap);
@@ -229,8 +249,9 @@ FwdLayout fwd_layout(const moe_lora_dims* d) {
   l.gpart = off; off += l.ks_gu > 1 ? up256((size_t)l.ks_gu * c.rows * 2 * d->I * 4) : 0;
   // fp32 partial S of K-split shrinks, and their per-(run, warp) arrival counters
   const size_t s_part = (size_t)c.runs * d->block_m * r_pad_of(d) * 4;
-  l.pgu = off; off += up256((size_t)shrink_ksplit(d, c, d->H) * s_part);
-  l.pdn = off; off += up256((size_t)shrink_ksplit(d, c, d->I) * s_part);
+  const bool cores = shrink_on_cores(d, c);
+  l.pgu = off; off += up256((size_t)(cores ? shrink_slices(d->H) : shrink_ksplit(d, c, d->H)) * s_part);
+  l.pdn = off; off += up256((size_t)(cores ? shrink_slices(d->I) : shrink_ksplit(d, c, d->I)) * s_part);
   l.n_ctr = kNumGemmCounters + 2 * 4 * (int)c.runs;
   l.bytes = off;
   return l;
@@ -583,6 +604,29 @@ int do_forward(const moe_lora_dims* d, const uint16_t* x, const float* topk_w, c
                                    l.n_ctr, s));
   MOE_CUDA(mark(1 + MOE_LORA_STAGE_GATHER));
 
+  const bool cores = shrink_on_cores(d, cap);
+  // the shrink on CUDA cores: same inputs, same S tiles
+  auto shrink_rows = [&](const uint16_t* rows_in, const uint16_t* A, int K, uint16_t* s_out, size_t part_off,
+                         int32_t* cnt) -> cudaError_t {
+    moe::ShrinkRowsLaunch r{};
+    r.xs = rows_in;
+    r.A = A;
+    r.runs = al->runs;
+    r.block_expert = al->block_expert;
+    r.totals = al->totals;
+    r.s_part = reinterpret_cast<float*>(base + part_off);
+    r.s_cnt = cnt;
+    r.s_out = s_out;
+    r.K = K;
+    r.E = d->E;
+    r.r_max = d->r_max;
+    r.r_pad = (int32_t)RP;
+    r.block_m = BT;
+    r.slices = shrink_slices(K);
+    r.max_runs = (int32_t)cap.runs;
+    for (int a = 0; a < d->L; ++a) r.ranks[a] = d->ranks[a];
+    return moe::launch_shrink_rows(r, cap.runs, true, s);
+  };
   if (lora) {
     moe::GemmParams q = p;
     q.K = d->H;
@@ -591,7 +635,8 @@ int do_forward(const moe_lora_dims* d, const uint16_t* x, const float* topk_w, c
     q.ksplit = shrink_ksplit(d, cap, d->H);
     q.s_part = reinterpret_cast<float*>(base + l.pgu);
     q.s_cnt = ctr + kNumGemmCounters;
-    MOE_CUDA(moe::launch_gemm(moe::kShrink, BT, m_sgu, q, cap.blocks, cap.runs, true, s));
+    if (cores) MOE_CUDA(shrink_rows(xs, A_gu, d->H, sgu, l.pgu, q.s_cnt));
+    else MOE_CUDA(moe::launch_gemm(moe::kShrink, BT, m_sgu, q, cap.blocks, cap.runs, true, s));
   }
   MOE_CUDA(mark(1 + MOE_LORA_STAGE_SHRINK_GU));
   {
@@ -616,7 +661,8 @@ int do_forward(const moe_lora_dims* d, const uint16_t* x, const float* topk_w, c
     q.ksplit = shrink_ksplit(d, cap, d->I);
     q.s_part = reinterpret_cast<float*>(base + l.pdn);
     q.s_cnt = ctr + kNumGemmCounters + 4 * cap.runs;
-    MOE_CUDA(moe::launch_gemm(moe::kShrink, BT, m_sdn, q, cap.blocks, cap.runs, true, s));
+    if (cores) MOE_CUDA(shrink_rows(hs, A_dn, d->I, sdn, l.pdn, q.s_cnt));
+    else MOE_CUDA(moe::launch_gemm(moe::kShrink, BT, m_sdn, q, cap.blocks, cap.runs, true, s));
   }
   MOE_CUDA(mark(1 + MOE_LORA_STAGE_SHRINK_DN));
   {
@@ -702,14 +748,20 @@ int moe_lora_plan_query(const moe_lora_dims* d, moe_lora_plan* out) {
   p.table_row = block_row(d->block_m);
   p.weight_streaming = d->block_m < 128;
   const bool lora = d->L > 0;
-  p.ksplit[0] = lora ? shrink_ksplit(d, cap, d->H) : 0;
+  const bool cores = shrink_on_cores(d, cap);
+  p.shrink_on_cores = cores ? 1 : 0;
+  p.ksplit[0] = lora ? (cores ? shrink_slices(d->H) : shrink_ksplit(d, cap, d->H)) : 0;
   p.ksplit[1] = l.ks_gu;
-  p.ksplit[2] = lora ? shrink_ksplit(d, cap, d->I) : 0;
+  p.ksplit[2] = lora ? (cores ? shrink_slices(d->I) : shrink_ksplit(d, cap, d->I)) : 0;
   p.ksplit[3] = l.ks_dn;
   const int modes[4] = {moe::kShrink, moe::kGateUp, moe::kShrink, moe::kDown};
   for (int g = 0; g < 4; ++g)
     if (!moe::gemm_stage_shape(modes[g], d->block_m, &p.k_tile[g], &p.stages[g]))
       return fail(MOE_LORA_EUNSUPPORTED, "no GEMM compiled for block_m = %d", d->block_m);
+  if (cores) {   // one K slice per CTA, no pipeline
+    p.k_tile[0] = p.k_tile[2] = moe::kShrinkSlice;
+    p.stages[0] = p.stages[2] = 1;
+  }
   const int64_t P = d->T * d->k;
   const AlignLayout al = align_layout(d);
   p.launches_route_align = P == 0 ? 1 : fused_route_align(d, al) ? 1 : al.nchunks == 1 ? 2 : 4;

@@ -41,7 +41,8 @@ class AlignBuf(C.Structure):
 class Plan(C.Structure):
     _fields_ = [("block_m", C.c_int32), ("table_row", C.c_int32), ("weight_streaming", C.c_int32),
                 ("ksplit", C.c_int32 * 4), ("k_tile", C.c_int32 * 4), ("stages", C.c_int32 * 4),
-                ("launches_route_align", C.c_int32), ("launches_forward", C.c_int32)]
+                ("launches_route_align", C.c_int32), ("launches_forward", C.c_int32),
+                ("shrink_on_cores", C.c_int32)]
 
 
 GEMMS = ("shrink_gu", "gate_up", "shrink_dn", "down")
@@ -153,7 +154,7 @@ def plan(d: LayerDims) -> dict:
     return {"block_m": p.block_m, "table_row": p.table_row, "weight_streaming": bool(p.weight_streaming),
             "ksplit": dict(zip(GEMMS, p.ksplit)), "k_tile": dict(zip(GEMMS, p.k_tile)),
             "stages": dict(zip(GEMMS, p.stages)), "launches_route_align": p.launches_route_align,
-            "launches_forward": p.launches_forward}
+            "launches_forward": p.launches_forward, "shrink_on_cores": bool(p.shrink_on_cores)}
 
 
 def align_capacity(d: LayerDims):

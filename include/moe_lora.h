@@ -145,6 +145,9 @@ typedef struct moe_lora_plan {
     int32_t stages[4];            /* pipeline stages in shared memory                       */
     int32_t launches_route_align; /* kernel launches of one moe_lora_route_align           */
     int32_t launches_forward;     /* kernel launches of one moe_lora_forward               */
+    int32_t shrink_on_cores;      /* 1: the LoRA shrinks run on CUDA cores, split over K in
+                                     ksplit[0]/ksplit[2] slices of k_tile elements (short
+                                     adapter runs); 0: tcgen05 tiles                        */
 } moe_lora_plan;
 
 /* Fills *out for dims d (host only: no device call).  Returns a status. */

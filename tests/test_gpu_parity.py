@@ -85,9 +85,12 @@ def test_down_split_k(ml, torch, oracle, block_m):
 
 
 def test_shrink_split_k(ml, torch, oracle):
-    """A long reduction (I = 8192) over few adapter runs: the weight-streaming down shrink
-    splits K; the last split of each run sums the fp32 partials."""
+    """A long reduction (I = 8192) over few adapter runs: the down shrink splits K (here on
+    CUDA cores, 32 slices of 256; the tensor-core split runs in the dense_decode layer);
+    the CTA that completes a run adds its fp32 partials in slice order."""
     wl = W.custom(name="shsplit", T=6, H=256, I=8192, E=2, k=1, L=3, ranks=(16, 64, 32), lora_mode="uniform")
+    d = dims_of(wl, 16, ml)
+    assert ml.plan(d)["shrink_on_cores"] and ml.plan(d)["ksplit"]["shrink_dn"] == 32
     run_case(ml, torch, oracle, wl, block_m=16)
 
 
@@ -106,8 +109,12 @@ def test_dense_multi_lora(ml, torch, oracle, block_m):
 
 
 def test_dense_decode_config(ml, torch, oracle):
-    """The dense 32B-class MLP at decode size (H=5120, I=25600), every output element."""
-    run_case(ml, torch, oracle, W.get("dense_decode"))
+    """The dense 32B-class MLP at decode size (H=5120, I=25600), every output element; its
+    shrinks are tcgen05 tiles split over K (fp32 partials summed by the last split)."""
+    wl = W.get("dense_decode")
+    p = ml.plan(dims_of(wl, ml.pick_block_m(wl.T, wl.k, wl.E), ml))
+    assert not p["shrink_on_cores"] and p["ksplit"]["shrink_gu"] > 1 and p["ksplit"]["shrink_dn"] > 1
+    run_case(ml, torch, oracle, wl)
 
 
 # -------------------------------------------------------------- edge cases --
@@ -185,6 +192,21 @@ def test_align_one_chunk_boundary(ml, torch, oracle, T, k):
                   lora_mode="zipf_with_none", bias_std=0.5, none_frac=0.1)
     for bm in (16, 128):
         run_case(ml, torch, oracle, wl, block_m=bm)
+
+
+@pytest.mark.parametrize("block_m", [16, 32, 64])
+def test_shrink_paths_every_weight_streaming_block(ml, torch, oracle, block_m):
+    """Both shrinks on every weight-streaming block size.  A handful of runs over a short
+    weight stream takes the CUDA-core shrink: runs of several rows, ranks 40 and 8, K
+    slices cut ragged (H = 2880 = 11 x 256 + 64, I = 320).  A layer whose gate_up weights
+    stream for longer (4 experts of 2 x 4096 x 4096) takes the tcgen05 shrink tiles
+    (sampled tokens)."""
+    few = W.custom(name="fewruns", T=6, H=2880, I=320, E=3, k=2, L=2, ranks=(40, 8), lora_mode="uniform")
+    assert ml.plan(dims_of(few, block_m, ml))["shrink_on_cores"]
+    run_case(ml, torch, oracle, few, block_m=block_m)
+    big = W.custom(name="bigw", T=200, H=4096, I=4096, E=4, k=1, L=3, ranks=(16, 64, 32), lora_mode="uniform_with_none")
+    assert not ml.plan(dims_of(big, block_m, ml))["shrink_on_cores"]
+    run_case(ml, torch, oracle, big, block_m=block_m, tokens=sample_tokens(big.T, 40))
 
 
 def test_single_token(ml, torch, oracle):

@@ -80,6 +80,18 @@ def test_route_align_launches():
     assert ml.plan(dims(W.get("sweep_T4096"), 0))["launches_route_align"] == 4
 
 
+def test_shrink_on_cores_only_for_a_handful_of_runs_over_a_short_stream():
+    """A single token over 128 experts (8 runs, 50 MB of gate_up weights): the shrinks run
+    on CUDA cores in 256-wide K slices (H = 2048: 8, I = 768: 3).  Decode, the 64-token
+    layer and dense_decode keep tcgen05 shrink tiles (long weight streams or tens of
+    runs)."""
+    p = ml.plan(dims(W.get("sweep_T1"), 0))
+    assert p["shrink_on_cores"] and p["ksplit"]["shrink_gu"] == 8 and p["ksplit"]["shrink_dn"] == 3
+    assert p["k_tile"]["shrink_gu"] == 256
+    for name in ("decode", "tiny", "dense_decode", "sweep_T16"):
+        assert not ml.plan(dims(W.get(name), 0))["shrink_on_cores"], name
+
+
 def test_prefill_plan():
     p = ml.plan(dims(W.get("prefill"), 0))
     assert p["block_m"] == 256 and not p["weight_streaming"]
