@@ -301,6 +301,50 @@ def test_route_align_matches_separate_calls(ml, torch, name):
     assert_align_equal(a1, a0)
 
 
+@pytest.mark.parametrize("T,k", [(4, 2), (16, 2), (11, 3), (16, 4), (13, 5)])
+def test_align_small_batch_sizes(ml, torch, oracle, T, k):
+    """P = 8, 32, 33, 64, 65 pairs (32-, 64- and 128-key sort chunks of the one-CTA align):
+    bit-exact against the oracle with invalid expert and adapter ids dropped; the fused
+    route+align (T <= 32) gives the same bytes as route then align."""
+    wl = W.custom(name=f"w{T}x{k}", T=T, H=128, I=128, E=8, k=k, L=3, ranks=(16, 8, 32),
+                  lora_mode="uniform_with_none")
+    logits, lora, _, _ = inputs(wl)
+    for bm in (16, 128):
+        d = dims_of(wl, bm, ml)
+        a_bytes, _ = ml.workspace_size(d)
+        ids, _ = oracle.route(logits, wl.k)
+        ids = ids.copy()
+        bad_lora = lora.copy()
+        ids[0, 0] = -1
+        ids[T - 1, k - 1] = wl.E
+        bad_lora[T // 2] = wl.L
+        bufs = ml.alloc_align(d)
+        ws = torch.empty(max(a_bytes, 256), dtype=torch.int8, device="cuda")
+        ml.align(d, to_dev(ids, torch), to_dev(bad_lora, torch), bufs, ws)
+        torch.cuda.synchronize()
+        al = align_to_numpy(bufs)
+        assert_align_equal(al, oracle.align(ids, bad_lora, wl.E, wl.L, bm))
+        assert al["num_dropped"] >= 2
+        # fused route + align against the separate calls
+        lg, lr = to_dev(logits, torch), to_dev(lora, torch)
+        res = []
+        for fused in (False, True):
+            b2 = ml.alloc_align(d)
+            w2 = torch.empty(max(a_bytes, 256), dtype=torch.uint8, device="cuda")
+            i2 = torch.full((wl.T, wl.k), -9, dtype=torch.int32, device="cuda")
+            t2 = torch.full((wl.T, wl.k), -9.0, dtype=torch.float32, device="cuda")
+            if fused:
+                ml.route_align(d, lg, lr, i2, t2, b2, w2)
+            else:
+                ml.route(lg, wl.k, i2, t2)
+                ml.align(d, i2, lr, b2, w2)
+            torch.cuda.synchronize()
+            res.append((i2.cpu().numpy(), align_to_numpy(b2)))
+        assert np.array_equal(res[0][0], res[1][0])
+        assert_align_equal(res[1][1], res[0][1])
+        assert_align_equal(res[0][1], oracle.align(oracle.route(logits, wl.k)[0], lora, wl.E, wl.L, bm))
+
+
 def test_empty_batch(ml, torch):
     wl = W.get("tiny")
     _, _, _, w = inputs(wl)
