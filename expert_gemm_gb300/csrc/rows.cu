@@ -168,13 +168,11 @@ __device__ __forceinline__ void combine_cols(const void* __restrict__ y, int ksp
 // the GEMM finished first.
 constexpr int kCombineThreads = 256;
 template <bool SPLIT>
-__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const void* __restrict__ y, int ksplit,
-                                                                  int64_t part_rows,
-                                                                  const int32_t* __restrict__ pair_row,
-                                                                  const int32_t* __restrict__ sorted_p,
-                                                                  const int32_t* __restrict__ totals,
-                                                                  const float* __restrict__ topk_w, int64_t T, int k,
-                                                                  int H8, int ns, uint4* __restrict__ out) {
+__device__ __forceinline__ void combine_body(const void* __restrict__ y, int ksplit, int64_t part_rows,
+                                             const int32_t* __restrict__ pair_row,
+                                             const int32_t* __restrict__ sorted_p,
+                                             const int32_t* __restrict__ totals, const float* __restrict__ topk_w,
+                                             int64_t T, int k, int H8, int ns, uint4* __restrict__ out) {
   __shared__ int32_t s_row[kCombineThreads / 32][MOE_LORA_MAX_TOPK];
   __shared__ float s_w[kCombineThreads / 32][MOE_LORA_MAX_TOPK];
   // The pair lookups read what the gather, align and route wrote: those finished before
@@ -208,6 +206,24 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const void* __
   // (one column group per step: two per step, more loads in flight, measured slower)
   for (int c = slab * per + lane; c < c_end; c += 32)
     combine_cols<SPLIT, 1>(y, ksplit, part_rows, H8, s_row[wib], s_w[wib], n, c, t, out);
+}
+
+// Over bf16 rows: at most 40 registers a thread, so 6 CTAs (48 warps) share an SM.
+// Each warp has only its token's few row loads in flight, so the loads in flight per
+// SM, i.e. the resident warps, set the combine's bandwidth (prefill 179 -> 122 us
+// against 4 CTAs at 57 registers; 8 CTAs spill).
+__global__ void __launch_bounds__(kCombineThreads, 6)
+    combine_rows_kernel(const void* __restrict__ y, int ksplit, int64_t part_rows, const int32_t* __restrict__ pair_row,
+                        const int32_t* __restrict__ sorted_p, const int32_t* __restrict__ totals,
+                        const float* __restrict__ topk_w, int64_t T, int k, int H8, int ns, uint4* __restrict__ out) {
+  combine_body<false>(y, ksplit, part_rows, pair_row, sorted_p, totals, topk_w, T, k, H8, ns, out);
+}
+// Over fp32 K-split partials (their sums need more registers; capped, it would spill).
+__global__ void __launch_bounds__(kCombineThreads)
+    combine_parts_kernel(const void* __restrict__ y, int ksplit, int64_t part_rows, const int32_t* __restrict__ pair_row,
+                         const int32_t* __restrict__ sorted_p, const int32_t* __restrict__ totals,
+                         const float* __restrict__ topk_w, int64_t T, int k, int H8, int ns, uint4* __restrict__ out) {
+  combine_body<true>(y, ksplit, part_rows, pair_row, sorted_p, totals, topk_w, T, k, H8, ns, out);
 }
 
 }  // namespace
@@ -322,9 +338,9 @@ cudaError_t launch_combine(const void* y, int ksplit, int64_t part_rows, const i
   uint4* o = reinterpret_cast<uint4*>(out);
   const int nsi = static_cast<int>(ns);
   if (ksplit > 1)
-    return cudaLaunchKernelEx(&cfg, combine_kernel<true>, y, ksplit, part_rows, pair_row, sorted_p, totals, topk_w, T,
+    return cudaLaunchKernelEx(&cfg, combine_parts_kernel, y, ksplit, part_rows, pair_row, sorted_p, totals, topk_w, T,
                               k, H8, nsi, o);
-  return cudaLaunchKernelEx(&cfg, combine_kernel<false>, y, ksplit, part_rows, pair_row, sorted_p, totals, topk_w, T,
+  return cudaLaunchKernelEx(&cfg, combine_rows_kernel, y, ksplit, part_rows, pair_row, sorted_p, totals, topk_w, T,
                             k, H8, nsi, o);
 }
 
