@@ -68,7 +68,7 @@ struct GemmCfg {
   // (weight-streaming shrink: 10-16 KB stages, 8 deep, 6 for 64-token tiles)
   static constexpr int STAGES = MODE == kShrink ? (SWAP ? (BT <= 32 ? 8 : 6) : 4)
                                 : SWAP           ? (BT <= 16 ? 3 : 5)
-                                : CTA2           ? 5   // + 32 KB of output staging
+                                : CTA2           ? 6   // + 16 KB of output staging
                                                  : (192 * 1024) / STAGE_BYTES;
   // accumulators: non-swapped MT tiles of M=128 tokens x N; swapped NH tiles of 128 x BT
   static constexpr int NH = MODE == kShrink ? 1 : 2;
@@ -81,9 +81,11 @@ struct GemmCfg {
       TMEM_NEED <= 32 ? 32 : TMEM_NEED <= 64 ? 64 : TMEM_NEED <= 128 ? 128 : TMEM_NEED <= 256 ? 256 : 512;
   static constexpr int SD = 4;                              // tile-id ring depth
   // CTA pairs stage their bf16 output rows in shared memory and write them with TMA
-  // stores: per epilogue warp two buffers of 32 rows x 64 columns (4 KB each).
+  // stores: per epilogue warp one buffer of 32 rows x 64 columns (4 KB).  (A second
+  // buffer per warp costs a pipeline stage: 5 stages with two, 6 with one; the sixth
+  // stage is worth more -- prefill 3.81 -> 3.76 ms.)
   static constexpr bool TMA_STORE = CTA2;
-  static constexpr int OUT_BYTES = TMA_STORE ? 4 * 2 * 4096 : 0;
+  static constexpr int OUT_BYTES = TMA_STORE ? 4 * 4096 : 0;
   static constexpr int SMEM_BYTES =
       STAGES * STAGE_BYTES + OUT_BYTES + 1024 /*align slack*/ + 4096 /*barriers, tile ring*/;
   static_assert(!SWAP || (BT == 16 || BT == 32 || BT == 64), "swapped tiles take 16/32/64 tokens");
@@ -240,16 +242,16 @@ __device__ __forceinline__ const Tile* sched_read(GemmBars* bars, int i, int32_t
   return &bars->tiles[slot];
 }
 
-// Output staging of the CTA-pair epilogues: epilogue warp q owns two 4 KB buffers of
+// Output staging of the CTA-pair epilogues: epilogue warp q owns one 4 KB buffer of
 // 32 rows x 128 bytes (64 bf16 columns) in the 128-byte-swizzled layout of a TMA box
-// {64, 32}; lane i writes row i.  Before a buffer is reused, the store issued from it
-// two stores earlier must have read it.
+// {64, 32}; lane i writes row i.  Before the buffer is reused, the store issued from
+// it must have read it.
 __device__ __forceinline__ uint8_t* stage_out_buffer(uint8_t* out_stage, int q, int lane, int n_out) {
-  if (n_out >= 2) {
-    if (lane == 0) bulk_wait_read<1>();
+  if (n_out >= 1) {
+    if (lane == 0) bulk_wait_read<0>();   // the previous store has read the buffer
     __syncwarp();
   }
-  return out_stage + q * 8192 + (n_out & 1) * 4096;
+  return out_stage + q * 4096;
 }
 // 16-byte chunks j and j + 1 of row `lane` (chunk j holds columns 8j .. 8j + 7).
 __device__ __forceinline__ void put_row_chunks(uint8_t* buf, int lane, int j, const uint32_t (&pk)[8]) {

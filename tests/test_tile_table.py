@@ -95,7 +95,7 @@ def test_shrink_on_cores_only_for_a_handful_of_runs_over_a_short_stream():
 def test_prefill_plan():
     p = ml.plan(dims(W.get("prefill"), 0))
     assert p["block_m"] == 256 and not p["weight_streaming"]
-    assert p["stages"]["gate_up"] == 5 and p["stages"]["down"] == 5   # 32 KB stages of a CTA pair + output staging
+    assert p["stages"]["gate_up"] == 6 and p["stages"]["down"] == 6   # 32 KB stages of a CTA pair + 16 KB output staging
     assert p["ksplit"] == {"shrink_gu": 1, "gate_up": 1, "shrink_dn": 1, "down": 1}
     assert p["launches_route_align"] == 4  # 102400 pairs: route, then chunk/scan/scatter
     assert p["launches_forward"] == 7      # the gather copies in token order: a second launch
