@@ -345,6 +345,36 @@ def test_align_small_batch_sizes(ml, torch, oracle, T, k):
         assert_align_equal(res[0][1], oracle.align(oracle.route(logits, wl.k)[0], lora, wl.E, wl.L, bm))
 
 
+@pytest.mark.parametrize("E", [200, 1000])
+def test_route_many_experts(ml, torch, oracle, E):
+    """The router's wider register paths (E > 128: 8 and 32 logits per lane): ids bit-exact
+    and weights within 2e-6 of the oracle through the fused one-CTA route+align (T = 20)
+    and the route kernel (T = 300, and the separate calls), the align from them
+    bit-exact."""
+    for T in (20, 300):
+        wl = W.custom(name=f"re{E}x{T}", T=T, H=64, I=64, E=E, k=8, L=2, ranks=(16, 16),
+                      lora_mode="uniform_with_none")
+        logits, lora = W.make_routing(wl, 0)
+        d = dims_of(wl, 16, ml)
+        a_bytes, _ = ml.workspace_size(d)
+        ids_o, w_o = oracle.route(logits, wl.k)
+        lg, lr = to_dev(logits, torch), to_dev(lora, torch)
+        for fused in (False, True):
+            bufs = ml.alloc_align(d)
+            ws = torch.empty(max(a_bytes, 256), dtype=torch.uint8, device="cuda")
+            ids = torch.full((T, wl.k), -9, dtype=torch.int32, device="cuda")
+            tw = torch.full((T, wl.k), -9.0, dtype=torch.float32, device="cuda")
+            if fused:
+                ml.route_align(d, lg, lr, ids, tw, bufs, ws)
+            else:
+                ml.route(lg, wl.k, ids, tw)
+                ml.align(d, ids, lr, bufs, ws)
+            torch.cuda.synchronize()
+            assert np.array_equal(ids.cpu().numpy(), ids_o), (E, T, fused)
+            assert np.allclose(tw.cpu().numpy(), w_o, rtol=0, atol=2e-6), (E, T, fused)
+            assert_align_equal(align_to_numpy(bufs), oracle.align(ids_o, lora, E, wl.L, 16))
+
+
 def test_empty_batch(ml, torch):
     wl = W.get("tiny")
     _, _, _, w = inputs(wl)
