@@ -395,10 +395,13 @@ def run_ours(args, rank, world, local_rank):
 
 # --------------------------------------------------------- oracle timings ---
 
-def oracle_sample_rate(wl: W.Workload, n_tokens: int, budget_s: float, seed: int = 0):
-    """Oracle (route + align + fp64 forward) on the first n_tokens tokens, repeated for ~budget_s."""
+def oracle_sample_rate(wl: W.Workload, n_tokens: int, budget_s: float, seed: int = 0, threads: int = 0):
+    """Oracle (route + align + fp64 forward) on the first n_tokens tokens, repeated for ~budget_s.
+
+    threads > 0 caps the oracle's OpenMP threads for this sample (0: one per processor)."""
     from oracle import Oracle
     o = Oracle()
+    o.set_threads(threads)
     logits, lora = W.make_routing(wl, seed)
     x = W.make_activations(wl, seed)
     w = W.make_weights(wl, seed)
@@ -414,6 +417,7 @@ def oracle_sample_rate(wl: W.Workload, n_tokens: int, budget_s: float, seed: int
         el = time.perf_counter() - t0
         if el >= budget_s:
             break
+    o.set_threads(0)
     return n * reps / el, n, reps, el
 
 
@@ -423,6 +427,40 @@ def cores_used():
     except Exception:
         n = os.cpu_count() or 1
     return int(os.environ.get("OMP_NUM_THREADS", n))
+
+
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), or None."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return None
+
+
+def cpu_baseline(wl, budget_s):
+    """The oracle on all host cores and on one, over the same bounded token sample.
+
+    The oracle's forward is parallel over tokens, so the threads it uses are at most the
+    sample's token count."""
+    n = min(wl.T, 16)
+    v, n, reps, el = oracle_sample_rate(wl, n, budget_s)
+    v1, _, reps1, el1 = oracle_sample_rate(wl, n, budget_s / 3, threads=1)
+    return {"value": v, "unit": "tokens/s", "cores": min(cores_used(), n), "kind": "oracle",
+            "sample": f"first {n} of {wl.T} tokens, {reps} passes in {el:.1f} s (route + align + fp64 forward)",
+            "one_core": {"value": v1, "unit": "tokens/s", "cores": 1,
+                         "sample": f"the same {n} tokens, {reps1} passes in {el1:.1f} s"},
+            "host_cores": cores_used(), "cpu_model": cpu_model()}
 
 
 def run_reference(args):
@@ -456,8 +494,9 @@ def run_reference(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded normals, bf16)",
             "impl": "reference",
             "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k, "L": wl.L},
-            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores_used(), "kind": "oracle",
-                             "sample": f"first {n} of {wl.T} tokens per step (route + align + fp64 forward)"},
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": min(cores_used(), n), "kind": "oracle",
+                             "sample": f"first {n} of {wl.T} tokens per step (route + align + fp64 forward)",
+                             "host_cores": cores_used(), "cpu_model": cpu_model()},
             "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
@@ -494,11 +533,7 @@ def main():
     res = run_ours(args, rank, world, local_rank)
     if rank == 0:
         if world == 1 and args.cpu_baseline_s > 0:
-            wl = workload_of(args)
-            v, n, reps, el = oracle_sample_rate(wl, min(wl.T, 16), args.cpu_baseline_s)
-            res["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": cores_used(), "kind": "oracle",
-                                   "sample": f"first {n} of {wl.T} tokens, {reps} passes in {el:.1f} s "
-                                             f"(route + align + fp64 forward)"}
+            res["cpu_baseline"] = cpu_baseline(workload_of(args), args.cpu_baseline_s)
         print(json.dumps(res), flush=True)
     if world > 1:
         import torch

@@ -40,9 +40,19 @@
  * hand-computed cases, merged-weight runs).  Nothing here is "parity unpinned".
  */
 #include <math.h>
+#include <omp.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+
+/* Threads of the parallel regions that later calls from this host thread start
+ * (n <= 0: one per processor).  Returns the count now in force.  Timing only; the
+ * results do not depend on it. */
+int32_t oracle_set_threads(int32_t n)
+{
+    omp_set_num_threads(n > 0 ? n : omp_get_num_procs());
+    return omp_get_max_threads();
+}
 
 /* bf16 bit pattern -> double (exact). */
 static double bf16_to_double(uint16_t b)

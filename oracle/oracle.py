@@ -52,6 +52,8 @@ def load(path: str | None = None):
     lib.oracle_forward.argtypes = [C.c_int64] + [C.c_int32] * 6 + [I32P, U16P, I32P, F32P, I32P] + \
         [U16P] * 6 + [I64P, C.c_int64, F64P, I64P]
     lib.oracle_forward.restype = None
+    lib.oracle_set_threads.argtypes = [C.c_int32]
+    lib.oracle_set_threads.restype = C.c_int32
     if path is None:
         _lib = lib
     return lib
@@ -62,6 +64,10 @@ class Oracle:
 
     def __init__(self, path: str | None = None):
         self.lib = load(path)
+
+    def set_threads(self, n: int) -> int:
+        """OpenMP threads of later calls from this thread (n <= 0: one per processor)."""
+        return int(self.lib.oracle_set_threads(int(n)))
 
     def route(self, logits: np.ndarray, k: int):
         logits = np.ascontiguousarray(logits, dtype=np.float32)
