@@ -148,14 +148,23 @@ __device__ void scan_phase(const AlignLaunch& a) {
   const int tid = threadIdx.x, nt = blockDim.x;
   const moe_lora_align_buf& o = a.out;
 
+  // The loops below read kBatch values before writing any: loads and stores go to
+  // global scratch through the same struct, so the compiler would otherwise wait for
+  // each load in turn.
+  constexpr int kBatch = 8;
   // 1. bucket totals; counts[c][b] becomes the offset of chunk c inside bucket b
   for (int b = tid; b < NB; b += nt) {
     int run = 0;
-    for (int c = 0; c < a.nchunks; ++c) {
-      const int64_t ix = static_cast<int64_t>(c) * NB + b;
-      const int v = a.counts[ix];
-      a.counts[ix] = run;
-      run += v;
+    for (int c0 = 0; c0 < a.nchunks; c0 += kBatch) {
+      int v[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u)
+        v[u] = c0 + u < a.nchunks ? a.counts[static_cast<int64_t>(c0 + u) * NB + b] : 0;
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        if (c0 + u < a.nchunks) a.counts[static_cast<int64_t>(c0 + u) * NB + b] = run;
+        run += v[u];
+      }
     }
     a.bucket_total[b] = run;
   }
@@ -163,7 +172,13 @@ __device__ void scan_phase(const AlignLaunch& a) {
   // 2. pairs per expert
   for (int e = tid; e < a.E; e += nt) {
     int n = 0;
-    for (int j = 0; j < LB; ++j) n += a.bucket_total[e * LB + j];
+    for (int j0 = 0; j0 < LB; j0 += kBatch) {
+      int v[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) v[u] = j0 + u < LB ? a.bucket_total[e * LB + j0 + u] : 0;
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) n += v[u];
+    }
     a.expert_n[e] = n;
   }
   __syncthreads();
@@ -179,9 +194,15 @@ __device__ void scan_phase(const AlignLaunch& a) {
   // 4. bucket starts: expert start + earlier adapters of the same expert
   for (int e = tid; e < a.E; e += nt) {
     int base = o.expert_begin[e];
-    for (int j = 0; j < LB; ++j) {
-      a.bucket_base[e * LB + j] = base;
-      base += a.bucket_total[e * LB + j];
+    for (int j0 = 0; j0 < LB; j0 += kBatch) {
+      int v[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) v[u] = j0 + u < LB ? a.bucket_total[e * LB + j0 + u] : 0;
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        if (j0 + u < LB) a.bucket_base[e * LB + j0 + u] = base;
+        base += v[u];
+      }
     }
   }
   __syncthreads();
