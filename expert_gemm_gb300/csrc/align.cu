@@ -34,24 +34,74 @@ __device__ __forceinline__ int lower_bound_u32(const uint32_t* a, int lo, int hi
   return lo;
 }
 
-// Ascending bitonic sort of n (a power of two) keys in shared memory, all threads of
-// the CTA; ends with a barrier.
+// Compare-exchange of a pair held by one thread: ascending unless desc.
+__device__ __forceinline__ void cmp_swap(uint32_t& x, uint32_t& y, bool desc) {
+  if ((x > y) != desc) {
+    const uint32_t t = x;
+    x = y;
+    y = t;
+  }
+}
+
+// Ascending bitonic sort of n (a power of two, n <= 4 * blockDim.x) keys in shared
+// memory, all threads of the CTA; ends with a barrier.  Thread t holds keys
+// [4t, 4t + 4) in registers.  Compare-exchanges at distance 1 and 2 stay inside the
+// thread, distances 4..64 go between the lanes of a warp by shuffles, and only
+// distances of 128 and more pass through shared memory (15 barrier stages for 4096
+// keys instead of 78).  Every thread runs every stage, so the shuffles see full warps.
 __device__ void bitonic_sort(uint32_t* keys, int n) {
+  const int t = threadIdx.x;
+  const int i0 = 4 * t;   // first key of this thread
+  uint32_t v[4];
+  __syncthreads();        // the keys every thread wrote
+#pragma unroll
+  for (int q = 0; q < 4; ++q) v[q] = i0 + q < n ? keys[i0 + q] : 0xFFFFFFFFu;
   for (int size = 2; size <= n; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      __syncthreads();
-      for (int i = threadIdx.x; i < n / 2; i += blockDim.x) {
-        const int lo = 2 * i - (i & (stride - 1));
-        const int hi = lo + stride;
-        const bool asc = (lo & size) == 0;
-        const uint32_t x = keys[lo], y = keys[hi];
-        if ((x > y) == asc) {
-          keys[lo] = y;
-          keys[hi] = x;
+    int s = size >> 1;
+    if (s >= 128) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (i0 + q < n) keys[i0 + q] = v[q];
+      for (; s >= 128; s >>= 1) {
+        __syncthreads();
+        for (int i = t; i < n / 2; i += blockDim.x) {
+          const int lo = 2 * i - (i & (s - 1));
+          const int hi = lo + s;
+          uint32_t x = keys[lo], y = keys[hi];
+          cmp_swap(x, y, (lo & size) != 0);
+          keys[lo] = x;
+          keys[hi] = y;
         }
       }
+      __syncthreads();
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (i0 + q < n) v[q] = keys[i0 + q];
     }
+    // distances 4..64: the partner of key i0 + q is key q of lane ^ (s / 4)
+    for (; s >= 4; s >>= 1) {
+      const bool desc = (i0 & size) != 0, upper = (i0 & s) != 0;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t p = __shfl_xor_sync(0xffffffffu, v[q], s >> 2);
+        // the lower key of an ascending pair keeps the smaller one, and so on
+        v[q] = (upper != desc) ? (v[q] > p ? v[q] : p) : (v[q] < p ? v[q] : p);
+      }
+    }
+    // distances 2 and 1 (size 2 has only distance 1; there bit 1 of the key index
+    // decides the direction)
+    if (s == 2) {
+      const bool desc = (i0 & size) != 0;
+      cmp_swap(v[0], v[2], desc);
+      cmp_swap(v[1], v[3], desc);
+      s = 1;
+    }
+    cmp_swap(v[0], v[1], (i0 & size) != 0);
+    cmp_swap(v[2], v[3], ((i0 + 2) & size) != 0);
   }
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    if (i0 + q < n) keys[i0 + q] = v[q];
   __syncthreads();
 }
 
