@@ -11,7 +11,8 @@
 //
 // A stable counting sort in three launches:
 //   1. chunk:   each CTA sorts its chunk of pair keys (bucket << log2(CH) | local index)
-//               with a bitonic network in shared memory and writes per-bucket counts;
+//               with a bitonic network (registers and warp shuffles for short
+//               distances, shared memory for long ones) and writes per-bucket counts;
 //   2. scan:    one CTA turns counts into per-(chunk, bucket) offsets, expert starts
 //               (padded), bucket starts, runs, block experts, padding sentinels;
 //   3. scatter: each CTA places its pairs; rank inside the chunk = index - first index
