@@ -125,6 +125,14 @@ def workload_of(args) -> W.Workload:
     return wl
 
 
+def workload_config(wl: W.Workload, world: int) -> dict:
+    """The config keys both arms report for a workload."""
+    return {"workload": f"{wl.name}: T={wl.T} H={wl.H} I={wl.I} E={wl.E} top-{wl.k} L={wl.L} "
+                        f"ranks={sorted(set(wl.ranks))}", "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E,
+            "k": wl.k, "L": wl.L, "global_batch": world * wl.T,
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+
+
 # -------------------------------------------------------------- our arm -----
 
 KERNEL_SOURCES = ("gemm_tc.cuh", "ptx.cuh", "common.cuh", "gemm_tc.cu", "moe_lora.cu")   # kernels and their tensor maps
@@ -349,10 +357,7 @@ def run_ours(args, rank, world, local_rank):
         "metric": METRIC, "value": job_throughput(wl.T, world, m["ms"]), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": m["ms"], "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded normals, bf16)",
-        "config": {"workload": f"{wl.name}: T={wl.T} H={wl.H} I={wl.I} E={wl.E} top-{wl.k} L={wl.L} "
-                               f"ranks={sorted(set(wl.ranks))}", "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E,
-                   "k": wl.k, "L": wl.L, "block_m": bm, "global_batch": world * wl.T,
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        "config": {**workload_config(wl, world), "block_m": bm,
                    "l2": "flushed between timed steps (256 MiB write)"},
         "roofline": roof,
         "layer_roofline": layer,
@@ -493,7 +498,7 @@ def run_reference(args):
             "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded normals, bf16)",
             "impl": "reference",
-            "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k, "L": wl.L},
+            "config": workload_config(wl, args.gpus),
             "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": min(cores_used(), n), "kind": "oracle",
                              "sample": f"first {n} of {wl.T} tokens per step (route + align + fp64 forward)",
                              "host_cores": cores_used(), "cpu_model": cpu_model()},
