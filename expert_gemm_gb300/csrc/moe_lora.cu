@@ -967,23 +967,60 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 std::mutex g_static_mu;
-void* g_static_ptr[kMaxDevices] = {};
+struct StaticScratchEntry {
+  void* ptr = nullptr;
+  unsigned long long ctx_id = 0;   // driver id of the context the address belongs to
+};
+StaticScratchEntry g_static[kMaxDevices];
 
-// Device address of g_static_scratch on the current device, looked up once per
-// device.  (In host code the array's name is only a host-side stand-in.)
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+PFN_cuCtxGetId_v12000 g_ctx_id = nullptr;
+std::once_flag g_ctx_once;
+
+// Unique id of the calling thread's current context (0 if there is none yet).  A
+// context created after a cudaDeviceReset, or another context on the same device,
+// loads the module anew and the array may sit elsewhere, so the cache is keyed on it.
+unsigned long long current_ctx_id() {
+  std::call_once(g_ctx_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+    fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(fn);
+  });
+  if (!g_ctx_current || !g_ctx_id) return 0;
+  CUcontext ctx = nullptr;
+  if (g_ctx_current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+  unsigned long long id = 0;
+  if (g_ctx_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// Device address of g_static_scratch in the current device's current context.  (In
+// host code the array's name is only a host-side stand-in.)  The address is looked up
+// once per (device, context): the first call on a device, and the first call after
+// its context was replaced, do the look-up.
 int static_scratch(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   if (dev < 0 || dev >= kMaxDevices) return fail(MOE_LORA_EUNSUPPORTED, "device ordinal %d >= %d", dev, kMaxDevices);
   std::lock_guard<std::mutex> lock(g_static_mu);
-  if (!g_static_ptr[dev]) {
+  StaticScratchEntry& ent = g_static[dev];
+  const unsigned long long id = current_ctx_id();
+  if (!ent.ptr || id == 0 || id != ent.ctx_id) {
     void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_static_scratch);
+    e = cudaGetSymbolAddress(&p, g_static_scratch);   // creates the context if needed
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
-    g_static_ptr[dev] = p;
+    if (!p) return fail(MOE_LORA_ECUDA, "cudaGetSymbolAddress(static scratch) returned NULL");
+    ent.ptr = p;
+    ent.ctx_id = current_ctx_id();
   }
-  *out = g_static_ptr[dev];
+  *out = ent.ptr;
   return MOE_LORA_OK;
 }
 

@@ -287,7 +287,8 @@ int moe_lora_layer_graph_destroy(moe_lora_graph *graph);
  * scratch (align_bytes of moe_lora_workspace_size) is larger are rejected with
  * MOE_LORA_EWORKSPACE before anything is enqueued.
  *   - The first call on a device looks up the array's device address (once per
- *     device, with that device current); make that first call before any stream
+ *     device, with that device current; again after the device's context was
+ *     replaced, e.g. by cudaDeviceReset); make that first call before any stream
  *     capture.
  *   - All calls on a device share the one array: calls that overlap on the GPU
  *     (other streams, other host threads) race on it, so serialise them.

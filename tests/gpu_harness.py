@@ -76,10 +76,3 @@ def assert_align_equal(got: dict, ref: dict):
         a, b = np.asarray(got[k]).reshape(-1), np.asarray(ref[k]).reshape(-1)
         assert a.shape == b.shape and np.array_equal(a, b), k
 
-
-def sample_tokens(T: int, n: int, seed: int = 1):
-    if T <= n:
-        return np.arange(T, dtype=np.int64)
-    g = np.random.default_rng(seed)
-    s = set(g.choice(T, n, replace=False).tolist()) | {0, T - 1}
-    return np.array(sorted(s), dtype=np.int64)

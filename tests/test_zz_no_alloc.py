@@ -40,34 +40,52 @@ def test_static_scratch_size_is_enforced(ml):
     assert ei.value.status == ml.EWORKSPACE
 
 
+def _route(ml, torch, wl, seed):
+    logits, lora = W.make_routing(wl, seed)
+    lg = torch.from_numpy(logits).cuda()
+    lr = torch.from_numpy(lora).cuda()
+    ids = torch.empty((wl.T, wl.k), dtype=torch.int32, device="cuda")
+    tw = torch.empty((wl.T, wl.k), dtype=torch.float32, device="cuda")
+    ml.route(lg, wl.k, ids, tw)
+    return ids, lr
+
+
+def _compare(ml, torch, wl, d, ids, lr):
+    ref = ml.alloc_align(d)
+    got = ml.alloc_align(d)
+    for t in got.values():
+        t.fill_(-7)
+    a_bytes, _ = ml.workspace_size(d)
+    ws = torch.empty(a_bytes, dtype=torch.uint8, device="cuda")
+    ml.align(d, ids, lr, ref, ws)
+    ml.align_static(d, ids, lr, got)
+    torch.cuda.synchronize()
+    tot = ref["totals"].cpu().tolist()
+    assert got["totals"].cpu().tolist() == tot
+    rows, nb, nr, _ = tot
+    for name, n in (("sorted_p", rows), ("block_expert", nb), ("block_runs", nb + 1), ("runs", nr),
+                    ("expert_begin", wl.E + 1)):
+        assert torch.equal(got[name][:n].cpu(), ref[name][:n].cpu()), (wl.name, name)
+
+
 @pytest.mark.gpu
 def test_align_static_matches_align_twice(ml):
-    """Two calls in a row, different routings: bit-identical to moe_lora_align."""
+    """Two calls in a row on each layer, a different routing each time: bit-identical to
+    moe_lora_align.  decode and sweep_T256 (at most 4096 pairs) take the one-CTA align;
+    sweep_T4096 (32,768 pairs over 128 x 65 buckets) and wide (8,192 pairs) take the
+    chunked align, whose sort keys, per-chunk bucket counts and bucket bases live in
+    the static array, so the second call runs over the first call's leftovers."""
     import torch
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
-    cases = [(W.get("decode"), 0), (W.get("sweep_T256"), 3)]
-    for wl, seed in cases:
-        logits, lora = W.make_routing(wl, seed)
+    for name in ("decode", "sweep_T256", "sweep_T4096", "wide"):
+        wl = W.get(name)
         bm = ml.pick_block_m(wl.T, wl.k, wl.E)
         d = _dims(ml, wl, bm)
-        lg = torch.from_numpy(logits).cuda()
-        lr = torch.from_numpy(lora).cuda()
-        ids = torch.empty((wl.T, wl.k), dtype=torch.int32, device="cuda")
-        tw = torch.empty((wl.T, wl.k), dtype=torch.float32, device="cuda")
-        ml.route(lg, wl.k, ids, tw)
-        ref = ml.alloc_align(d)
-        got = ml.alloc_align(d)
-        for t in got.values():
-            t.fill_(-7)
         a_bytes, _ = ml.workspace_size(d)
-        ws = torch.empty(a_bytes, dtype=torch.uint8, device="cuda")
-        ml.align(d, ids, lr, ref, ws)
-        ml.align_static(d, ids, lr, got)
-        torch.cuda.synchronize()
-        tot = ref["totals"].cpu().tolist()
-        assert got["totals"].cpu().tolist() == tot
-        rows, nb, nr, _ = tot
-        for name, n in (("sorted_p", rows), ("block_expert", nb), ("block_runs", nb + 1), ("runs", nr),
-                        ("expert_begin", wl.E + 1)):
-            assert torch.equal(got[name][:n].cpu(), ref[name][:n].cpu()), (wl.name, name)
+        assert a_bytes <= ml.STATIC_SCRATCH_BYTES
+        if name in ("sweep_T4096", "wide"):
+            assert wl.T * wl.k > 4096          # more than one sort chunk
+        for seed in (0, 3):
+            ids, lr = _route(ml, torch, wl, seed)
+            _compare(ml, torch, wl, d, ids, lr)
