@@ -48,6 +48,8 @@ struct GemmParams {
   int32_t max_runs;
   uint16_t* s_out;              // kShrink: [runs][BT][r_pad] (bf16), rows outside the run zero
   int32_t* status;              // device status word (MOE_LORA_DEV_* bits)
+  uint64_t acc_wait_ns;         // limit of the single-CTA epilogue's accumulator wait (test hook;
+                                //   the default limit otherwise)
   int32_t K;                    // reduction length of the base GEMM (H or I)
   int32_t n_feat;               // output features (I for kGateUp, H for kDown)
   int32_t E;

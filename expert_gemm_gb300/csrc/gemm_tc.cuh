@@ -595,7 +595,8 @@ __global__ void __launch_bounds__(192, 1)
       }
       const int ab = i % C::NBUF;
       const uint32_t fph = (i / C::NBUF) & 1;
-      const bool got = C::CTA2 ? mbar_wait_cluster(&bars->acc_full[ab], fph) : mbar_wait(&bars->acc_full[ab], fph);
+      const bool got = C::CTA2 ? mbar_wait_cluster(&bars->acc_full[ab], fph)
+                               : mbar_wait_for(&bars->acc_full[ab], fph, prm.acc_wait_ns);
       if (!got) record_timeout(bars, prm.status);
       tc_fence_after_sync();
       const bool ok = got && !aborted(bars);

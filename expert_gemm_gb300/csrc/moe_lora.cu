@@ -10,6 +10,7 @@
 //   combine   out[t] = bf16(sum_j w[t,j] y[row of (t,j)]), fixed order
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -17,10 +18,14 @@
 #include <new>
 
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace {
 
 thread_local char g_err[512] = "";
+
+// Test hook: limit of the gate_up epilogue's accumulator wait (0 = the default limit).
+std::atomic<uint64_t> g_acc_wait_ns{0};
 
 int fail(int status, const char* fmt, ...) {
   va_list ap;
@@ -582,6 +587,7 @@ int do_forward(const moe_lora_dims* d, const uint16_t* x, const float* topk_w, c
   p.sorted_p = al->sorted_p;
   p.part_rows = cap.rows;
   p.status = dev_status;
+  p.acc_wait_ns = moe::kWaitTimeoutNs;
   p.E = d->E;
   p.k = d->k;
   p.P = (int32_t)(d->T * d->k);
@@ -647,6 +653,8 @@ int do_forward(const moe_lora_dims* d, const uint16_t* x, const float* topk_w, c
     q.lora_after_pdl = lora;
     q.tile_ctr = ctr + 1;
     q.n_ft = (d->I + 127) / 128;
+    const uint64_t lim = g_acc_wait_ns.load(std::memory_order_relaxed);
+    if (lim != 0 && lim < moe::kWaitTimeoutNs) q.acc_wait_ns = lim;
     q.ksplit = ks_gu;
     q.g_part = gpart;
     MOE_CUDA(moe::launch_gemm(moe::kGateUp, BT, m_gu, q, cap.blocks, cap.runs, true, s));
@@ -716,7 +724,12 @@ LayerLayout layer_layout(const moe_lora_dims* d) {
 
 extern "C" {
 
-int moe_lora_version(void) { return 300; }
+int moe_lora_version(void) { return 301; }
+
+int moe_lora_debug_set_acc_wait_ns(uint64_t ns) {
+  g_acc_wait_ns.store(ns, std::memory_order_relaxed);
+  return MOE_LORA_OK;
+}
 
 const char* moe_lora_status_string(int status) {
   switch (status) {

@@ -70,6 +70,20 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   return false;
 }
 
+// mbar_wait with a caller-given wall-clock limit.  At or above the default limit it is
+// mbar_wait; below it the clock is read on every iteration, so a short limit (a test's)
+// gives up within a few polls.
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  if (limit_ns >= kWaitTimeoutNs) return mbar_wait(bar, parity);
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1; it < kWaitMaxIters; ++it) {
+    if (global_timer_ns() - t0 > limit_ns) return false;
+    if (mbar_try_wait(bar, parity)) return true;
+  }
+  return false;
+}
+
 // ------------------------------------------------------- CTA pairs (clusters of 2)
 // A pair of CTAs in one cluster runs one 2-SM tcgen05 MMA.  Shared-memory addresses
 // of the peer are shared::cluster addresses obtained with mapa.

@@ -24,7 +24,7 @@ EXPORTS = ["moe_lora_align_capacity", "moe_lora_workspace_size", "moe_lora_pick_
            "moe_lora_align", "moe_lora_forward", "moe_lora_layer_workspace_size", "moe_lora_layer_host",
            "moe_lora_status_string", "moe_lora_last_error", "moe_lora_version", "moe_lora_align_static",
            "moe_lora_route_align", "moe_lora_plan_query", "moe_lora_layer_graph_create",
-           "moe_lora_layer_graph_run", "moe_lora_layer_graph_destroy"]
+           "moe_lora_layer_graph_run", "moe_lora_layer_graph_destroy", "moe_lora_debug_set_acc_wait_ns"]
 STATIC_SCRATCH_BYTES = 4 << 20
 
 
@@ -83,6 +83,8 @@ def load(path: str = LIB_PATH):
     lib.moe_lora_layer_graph_destroy.argtypes = [vp]
     lib.moe_lora_forward.argtypes = [DP, vp, vp, AP, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp, vp]
     lib.moe_lora_layer_host.argtypes = [DP, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, C.POINTER(i64), vp]
+    lib.moe_lora_debug_set_acc_wait_ns.argtypes = [C.c_uint64]
+    lib.moe_lora_debug_set_acc_wait_ns.restype = C.c_int
     lib.moe_lora_status_string.restype = C.c_char_p
     lib.moe_lora_status_string.argtypes = [C.c_int]
     lib.moe_lora_last_error.restype = C.c_char_p
@@ -141,6 +143,12 @@ class LayerDims:
 
 def version() -> int:
     return load().moe_lora_version()
+
+
+def debug_set_acc_wait_ns(ns: int):
+    """Test hook: limit (ns) of the gate_up epilogue's accumulator wait in later forward
+    calls (single-CTA kernels); 0 restores the default.  See moe_lora.h."""
+    _check(load().moe_lora_debug_set_acc_wait_ns(int(ns)))
 
 
 def pick_block_m(T: int, k: int, E: int) -> int:

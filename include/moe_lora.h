@@ -301,6 +301,24 @@ int moe_lora_align_static(const moe_lora_dims *d, const int32_t *topk_ids, const
                           const moe_lora_align_buf *out, void *stream);
 
 /* ------------------------------------------------------------ diagnostics -- */
+
+/*
+ * Test hook for the failure path; the pages have no counterpart.  Every pipeline wait
+ * in the GEMM kernels is bounded (2 s) and reports expiry through dev_status rather
+ * than trapping.  This call sets, for the moe_lora_forward calls that follow in this
+ * process, the wall-clock limit in nanoseconds of ONE of those waits: the gate_up
+ * epilogue's wait for its accumulator, in the single-CTA kernels (block_m <= 128; the
+ * CTA-pair kernels of 256-row blocks keep the default).  0 restores the default.  A
+ * limit shorter than the accumulator takes makes that wait give up: the call sets
+ * MOE_LORA_DEV_TIMEOUT in dev_status (moe_lora_layer_host and the graph run return
+ * MOE_LORA_EDEVICE), the gate_up kernel winds down -- its in-flight copies and MMAs
+ * drained, its TMEM freed, the MMA thread giving up its own wait after the default
+ * limit -- and the call's output is invalid; the later kernels of the call still run.
+ * The next call with the default limit computes normally.  Process-wide; always
+ * returns MOE_LORA_OK.
+ */
+int moe_lora_debug_set_acc_wait_ns(uint64_t ns);
+
 const char *moe_lora_status_string(int status);
 const char *moe_lora_last_error(void);   /* detail of this thread's last failure */
 int moe_lora_version(void);              /* MAJOR*10000 + MINOR*100 + PATCH       */

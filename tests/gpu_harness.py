@@ -76,3 +76,43 @@ def assert_align_equal(got: dict, ref: dict):
         a, b = np.asarray(got[k]).reshape(-1), np.asarray(ref[k]).reshape(-1)
         assert a.shape == b.shape and np.array_equal(a, b), k
 
+
+# ------------------------------------------------------------------ guards --
+# compute-sanitizer is not available here, so out-of-bounds writes are caught with
+# canary bytes: each output and scratch buffer of a call is a slice of a larger
+# allocation whose head and tail hold a fixed pattern, checked after the call.
+GUARD_BYTES = 4096        # keeps every slice 4 KB-aligned (TMA wants 16 bytes)
+GUARD_PATTERN = 0xA5
+
+
+class Guarded:
+    """Device buffers carved out of canary-padded allocations."""
+
+    def __init__(self, torch):
+        self.torch = torch
+        self.bufs = []
+
+    def empty(self, shape, dtype):
+        torch = self.torch
+        n = int(np.prod(shape)) * torch.empty(0, dtype=dtype).element_size()
+        raw = torch.full((n + 2 * GUARD_BYTES,), GUARD_PATTERN, dtype=torch.uint8, device="cuda")
+        self.bufs.append((raw, n))
+        return raw[GUARD_BYTES:GUARD_BYTES + n].view(dtype).view(shape)
+
+    def guard_layer(self, layer):
+        """Swaps a Layer's output, align arrays and workspaces for guarded ones."""
+        layer.out = self.empty(tuple(layer.out.shape), layer.out.dtype)
+        layer.ws_align = self.empty(tuple(layer.ws_align.shape), layer.ws_align.dtype)
+        layer.ws_fwd = self.empty(tuple(layer.ws_fwd.shape), layer.ws_fwd.dtype)
+        layer.bufs = {k: self.empty(tuple(v.shape), v.dtype) for k, v in layer.bufs.items()}
+        layer.topk_ids = self.empty(tuple(layer.topk_ids.shape), layer.topk_ids.dtype)
+        layer.topk_w = self.empty(tuple(layer.topk_w.shape), layer.topk_w.dtype)
+        return layer
+
+    def check(self):
+        for raw, n in self.bufs:
+            head = raw[:GUARD_BYTES]
+            tail = raw[GUARD_BYTES + n:]
+            assert bool((head == GUARD_PATTERN).all()), f"canary before a {n}-byte buffer overwritten"
+            assert bool((tail == GUARD_PATTERN).all()), f"canary after a {n}-byte buffer overwritten"
+

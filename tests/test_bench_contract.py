@@ -45,3 +45,18 @@ def test_too_few_warmup_steps_refused(warmup):
     out = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "tiny", "--steps", "1",
                           "--warmup", warmup], cwd=ROOT, capture_output=True, text=True, timeout=600)
     assert out.returncode != 0 and "warmup" in out.stderr
+
+
+def test_secondary_legs_are_long_enough_to_sample_clocks():
+    """Each secondary configuration times ~0.6 s of steps (the clock sampler polls every
+    200 ms), never fewer than the headline's steps, and reports its step in SM cycles."""
+    import bench
+    assert bench.secondary_steps(0.06, 20) == 4615          # one-token layer
+    assert bench.secondary_steps(3.6, 20) == 163             # prefill
+    assert bench.secondary_steps(3.6, 500) == 500
+    assert bench.secondary_steps(100.0, 3) == 10
+    assert set(bench.SECONDARY) == {"prefill", "wide", "sweep_T1", "sweep_T16", "sweep_T256", "sweep_T4096",
+                                    "dense_decode"}
+    c = bench.clock_summary({"sm_mhz": 2000.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 3}, 0.5)
+    assert c["kcycles_per_step"] == 1000.0 and c["samples"] == 3
+    assert bench.clock_summary(None, 1.0) is None

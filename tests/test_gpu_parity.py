@@ -7,7 +7,8 @@ import numpy as np
 import pytest
 
 from expert_gemm_gb300 import workloads as W
-from gpu_harness import TOL, align_to_numpy, assert_align_equal, dev_weights, dims_of, inputs, parity_error, to_dev
+from gpu_harness import (TOL, Guarded, align_to_numpy, assert_align_equal, dev_weights, dims_of, inputs, parity_error,
+                         to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -34,10 +35,12 @@ def run_case(ml, torch, oracle, wl, block_m=None, tokens=None, logits=None, lora
     lora = lora0 if lora is None else lora
     bm = block_m or ml.pick_block_m(wl.T, wl.k, wl.E)
     d = dims_of(wl, bm, ml)
-    layer = ml.Layer(d, dev_weights(w, torch))
+    guards = Guarded(torch)
+    layer = guards.guard_layer(ml.Layer(d, dev_weights(w, torch)))
     out = layer.step(to_dev(logits, torch), to_dev(lora, torch), to_dev(x, torch))
     torch.cuda.synchronize()
     assert int(layer.status.item()) == 0
+    guards.check()
     ids_o, w_o = oracle.route(logits, wl.k)
     if check_route:
         assert np.array_equal(layer.topk_ids.cpu().numpy(), ids_o)
