@@ -337,6 +337,58 @@ def roofline_of(m, ml):
     return roof, layer
 
 
+# The other configurations the layer is measured on, timed after the headline (decode)
+# in the default run; each gets its own clock record and CPU baseline.
+SECONDARY = ("prefill", "wide", "sweep_T1", "sweep_T16", "sweep_T256", "sweep_T4096", "dense_decode")
+
+
+def _weights_key(wl: W.Workload):
+    return (wl.H, wl.I, wl.E, wl.L, tuple(wl.ranks))
+
+
+def _upload(torch, w):
+    return {n: _dev(torch, w[n]) for n in ("W_gu", "W_dn", "A_gu", "B_gu", "A_dn", "B_dn")}
+
+
+def clock_summary(clk, ms):
+    """The leg's sampled clocks plus its step time in SM cycles (ms x median MHz)."""
+    if not clk:
+        return clk
+    out = dict(clk)
+    if clk.get("sm_mhz"):
+        out["kcycles_per_step"] = ms * clk["sm_mhz"]   # ms * MHz = thousands of cycles
+    return out
+
+
+def secondary_steps(ms_est: float, k_arg: int) -> int:
+    """Steps of a secondary leg: about 0.6 s of timed work with the L2 flushes between
+    steps (~0.07 ms each), so that the 200 ms clock sampler sees the leg; at least 10
+    and at least the headline's steps, at most 5000."""
+    k = int(0.6e3 / (max(ms_est, 1e-3) + 0.07))
+    return max(10, min(k_arg, 5000), min(k, 5000))
+
+
+def run_secondary(torch, ml, name, wd, w_host, rank, world, flush, args):
+    """One secondary configuration: device timing, roofline, clocks, oracle baseline."""
+    wl = W.get(name)
+    bm = ml.pick_block_m(wl.T, wl.k, wl.E)
+    probe = measure(torch, ml, wl, wd, rank, 3, 3, bm, world, flush, graph=False, e2e=False)
+    k = secondary_steps(probe["ms"], args.steps)
+    m = measure(torch, ml, wl, wd, rank, k, 3, bm, world, flush, graph=False, e2e=False,
+                clocks=ClockSampler(int(os.environ.get("LOCAL_RANK", "0"))))
+    roof, layer = roofline_of(m, ml)
+    res = {"workload": workload_config(wl, world)["workload"], "T": wl.T,
+           "value": job_throughput(wl.T, world, m["ms"]), "unit": "tokens/s", "ms_per_step": m["ms"],
+           "steps": k, "warmup": 3, "block_m": bm, "roofline": roof, "layer_roofline": layer,
+           "stage_ms": {n: float(np.mean(m["stage_ms"][:, j])) for j, n in enumerate(ml.STAGES)},
+           "touched": {k_: m["acct"][k_] for k_ in ("experts", "adapter_expert_pairs", "valid_pairs")},
+           "clocks": clock_summary(m["clocks"], m["ms"]), "gpu_launches": probe["launches"] + m["launches"],
+           "plan": m["plan"]}
+    if world == 1 and args.secondary_cpu_s > 0:
+        res["cpu_baseline"] = cpu_baseline(wl, args.secondary_cpu_s, w_host)
+    return res
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     from expert_gemm_gb300 import build, moe_lora as ml
@@ -344,9 +396,8 @@ def run_ours(args, rank, world, local_rank):
     build.build()
     ml.load()
     wl = workload_of(args)
-    w = W.make_weights(wl, 0)                     # same weights on every replica, own batch per rank
-    wd = {n: _dev(torch, w[n]) for n in ("W_gu", "W_dn", "A_gu", "B_gu", "A_dn", "B_dn")}
-    del w
+    w_host = W.make_weights(wl, 0)                # same weights on every replica, own batch per rank
+    wd = _upload(torch, w_host)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     bm = args.block_m or ml.pick_block_m(wl.T, wl.k, wl.E)
     m = measure(torch, ml, wl, wd, rank, args.steps, args.warmup, bm, world, flush,
@@ -373,7 +424,7 @@ def run_ours(args, rank, world, local_rank):
                 "direct": {"entry": "moe_lora_layer_host", "ms_per_step": m["e2e_direct_s"] * 1e3,
                            "value": job_throughput(wl.T, world, m["e2e_direct_s"] * 1e3)}},
         "gpu_launches": m["launches"],
-        "clocks": m["clocks"],
+        "clocks": clock_summary(m["clocks"], m["ms"]),
         "wall_s_timed": m["t_wall"],
         "align_totals": m["totals"],
         "plan": m["plan"],
@@ -383,33 +434,42 @@ def run_ours(args, rank, world, local_rank):
                              "unit": "tokens/s", "note": "the same step captured once and replayed"}
     elif "graph_error" in m:
         res["cuda_graph"] = {"error": m["graph_error"]}
-    # the prefill layer has the decode layer's shapes and weights: measure it too
+    if world == 1 and args.cpu_baseline_s > 0:
+        res["cpu_baseline"] = cpu_baseline(wl, args.cpu_baseline_s, w_host)
+    # the other configurations, each a full pass of the same hot path at its own shapes
     if args.secondary and wl.name == "decode":
-        pw = W.get("prefill")
-        pk = max(3, min(args.steps, 20))
-        pm = measure(torch, ml, pw, wd, rank, pk, 3, ml.pick_block_m(pw.T, pw.k, pw.E), world, flush,
-                     graph=False, e2e=False)
-        proof, player = roofline_of(pm, ml)
-        res["prefill"] = {"workload": f"prefill: T={pw.T} (16 requests x 1600 tokens), decode-layer shapes",
-                          "value": world * pw.T / (pm["ms"] * 1e-3), "unit": "tokens/s", "ms_per_step": pm["ms"],
-                          "steps": pk, "block_m": pm["bm"], "roofline": proof, "layer_roofline": player,
-                          "stage_ms": {n: float(np.mean(pm["stage_ms"][:, j])) for j, n in enumerate(ml.STAGES)}}
-        res["gpu_launches"] += pm["launches"]
+        res["secondary"] = {}
+        cur_key = _weights_key(wl)
+        for name in SECONDARY:
+            sw = W.get(name)
+            if _weights_key(sw) != cur_key:
+                del wd
+                wd = None
+                torch.cuda.empty_cache()
+                w_host = W.make_weights(sw, 0)
+                wd = _upload(torch, w_host)
+                cur_key = _weights_key(sw)
+            r = run_secondary(torch, ml, name, wd, w_host, rank, world, flush, args)
+            res["secondary"][name] = r
+            res["gpu_launches"] += r["gpu_launches"]
+        res["prefill"] = res["secondary"]["prefill"]   # the compute-bound headline beside decode
     return res
 
 
 # --------------------------------------------------------- oracle timings ---
 
-def oracle_sample_rate(wl: W.Workload, n_tokens: int, budget_s: float, seed: int = 0, threads: int = 0):
+def oracle_sample_rate(wl: W.Workload, n_tokens: int, budget_s: float, seed: int = 0, threads: int = 0, w=None):
     """Oracle (route + align + fp64 forward) on the first n_tokens tokens, repeated for ~budget_s.
 
-    threads > 0 caps the oracle's OpenMP threads for this sample (0: one per processor)."""
+    threads > 0 caps the oracle's OpenMP threads for this sample (0: one per processor);
+    w: the workload's host weights (drawn here when None)."""
     from oracle import Oracle
     o = Oracle()
     o.set_threads(threads)
     logits, lora = W.make_routing(wl, seed)
     x = W.make_activations(wl, seed)
-    w = W.make_weights(wl, seed)
+    if w is None:
+        w = W.make_weights(wl, seed)
     n = max(1, min(n_tokens, wl.T))
     lg, lr, xs = logits[:n], lora[:n], x[:n]
     bm = 16
@@ -453,14 +513,14 @@ def cpu_model():
     return None
 
 
-def cpu_baseline(wl, budget_s):
+def cpu_baseline(wl, budget_s, w=None):
     """The oracle on all host cores and on one, over the same bounded token sample.
 
     The oracle's forward is parallel over tokens, so the threads it uses are at most the
     sample's token count."""
     n = min(wl.T, 16)
-    v, n, reps, el = oracle_sample_rate(wl, n, budget_s)
-    v1, _, reps1, el1 = oracle_sample_rate(wl, n, budget_s / 3, threads=1)
+    v, n, reps, el = oracle_sample_rate(wl, n, budget_s, w=w)
+    v1, _, reps1, el1 = oracle_sample_rate(wl, n, budget_s / 3, threads=1, w=w)
     return {"value": v, "unit": "tokens/s", "cores": min(cores_used(), n), "kind": "oracle",
             "sample": f"first {n} of {wl.T} tokens, {reps} passes in {el:.1f} s (route + align + fp64 forward)",
             "one_core": {"value": v1, "unit": "tokens/s", "cores": 1,
@@ -516,8 +576,10 @@ def main():
     ap.add_argument("--tokens", type=int, default=0, help="override T of the workload (small profiling cases)")
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay timing")
     ap.add_argument("--no-secondary", dest="secondary", action="store_false",
-                    help="skip the prefill measurement that accompanies the decode workload")
+                    help="skip the other configurations that accompany the decode workload")
     ap.add_argument("--cpu-baseline-s", type=float, default=12.0, help="seconds of oracle time (0 = skip)")
+    ap.add_argument("--secondary-cpu-s", type=float, default=2.0,
+                    help="seconds of oracle time per secondary configuration (0 = skip)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -537,8 +599,6 @@ def main():
         torch.distributed.init_process_group("nccl")
     res = run_ours(args, rank, world, local_rank)
     if rank == 0:
-        if world == 1 and args.cpu_baseline_s > 0:
-            res["cpu_baseline"] = cpu_baseline(workload_of(args), args.cpu_baseline_s)
         print(json.dumps(res), flush=True)
     if world > 1:
         import torch
