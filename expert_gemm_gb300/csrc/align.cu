@@ -312,6 +312,123 @@ __device__ void scan_phase(const AlignLaunch& a) {
 
 __global__ void __launch_bounds__(1024) align_scan_kernel(AlignLaunch a) { scan_phase(a); }
 
+// Phase 2 with the per-bucket arrays in shared memory (E * (L+1) <= kScanSmemBuckets):
+// the same results as scan_phase, but every pass after the first reads and writes
+// shared memory instead of making a round trip to L2, and each block's first run comes
+// from one pass over the runs instead of a binary search per block.  The bucket bases
+// and the per-chunk offsets still go to global memory for the scatter.
+constexpr int kScanSmemBuckets = 16384;
+__global__ void __launch_bounds__(1024) align_scan_smem_kernel(AlignLaunch a) {
+  extern __shared__ int32_t s_buf[];
+  __shared__ int32_t s_warp[32];
+  __shared__ int32_t s_rows, s_runs;
+  const int LB = a.L + 1;
+  const int NB = a.E * LB;
+  const int BM = a.BM;
+  const int tid = threadIdx.x, nt = blockDim.x;
+  const moe_lora_align_buf& o = a.out;
+  int32_t* s_tot = s_buf;            // [NB] pairs per bucket
+  int32_t* s_base = s_buf + NB;      // [NB] first sorted row of each bucket
+  int32_t* s_rb = s_buf + 2 * NB;    // [NB] first run of each bucket
+  int32_t* s_en = s_buf + 3 * NB;    // [E] pairs per expert
+  // 1. bucket totals; counts[c][b] becomes the offset of chunk c inside bucket b (all of
+  //    a thread's loads are issued before its stores)
+  constexpr int kBatch = 8;
+  for (int b = tid; b < NB; b += nt) {
+    int run = 0;
+    for (int c0 = 0; c0 < a.nchunks; c0 += kBatch) {
+      int v[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u)
+        v[u] = c0 + u < a.nchunks ? a.counts[static_cast<int64_t>(c0 + u) * NB + b] : 0;
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        if (c0 + u < a.nchunks) a.counts[static_cast<int64_t>(c0 + u) * NB + b] = run;
+        run += v[u];
+      }
+    }
+    s_tot[b] = run;
+  }
+  __syncthreads();
+  // 2. pairs per expert
+  for (int e = tid; e < a.E; e += nt) {
+    int n = 0;
+    for (int j = 0; j < LB; ++j) n += s_tot[e * LB + j];
+    s_en[e] = n;
+  }
+  __syncthreads();
+  // 3. padded expert starts
+  const int rows = block_exclusive_scan(
+      a.E, [&](int e) { return (s_en[e] + BM - 1) / BM * BM; }, [&](int e, int pre) { o.expert_begin[e] = pre; },
+      s_warp);
+  if (tid == 0) {
+    o.expert_begin[a.E] = rows;
+    s_rows = rows;
+  }
+  __syncthreads();
+  // 4. bucket starts: expert start + earlier adapters of the same expert
+  for (int e = tid; e < a.E; e += nt) {
+    int base = o.expert_begin[e];
+    for (int j = 0; j < LB; ++j) {
+      s_base[e * LB + j] = base;
+      a.bucket_base[e * LB + j] = base;
+      base += s_tot[e * LB + j];
+    }
+  }
+  __syncthreads();
+  // 5. runs: a bucket of adapter >= 0 splits at block boundaries
+  auto nruns_of = [&](int b) -> int {
+    const int tot = s_tot[b];
+    if (tot == 0 || (b % LB) == 0) return 0;
+    const int st = s_base[b];
+    return (st + tot - 1) / BM - st / BM + 1;
+  };
+  const int nruns = block_exclusive_scan(NB, nruns_of, [&](int b, int pre) { s_rb[b] = pre; }, s_warp);
+  if (tid == 0) s_runs = nruns;
+  __syncthreads();
+  // 6. write runs; 7. block experts; 8. padding sentinels
+  for (int b = tid; b < NB; b += nt) {
+    const int cnt = nruns_of(b);
+    if (!cnt) continue;
+    const int st = s_base[b], end = st + s_tot[b];
+    const int adapter = (b % LB) - 1;
+    const int r0 = s_rb[b];
+    for (int i = 0; i < cnt; ++i) {
+      const int blk = st / BM + i;
+      int* r = o.runs + 4 * static_cast<int64_t>(r0 + i);
+      r[0] = blk;
+      r[1] = adapter;
+      r[2] = max(st, blk * BM);
+      r[3] = min(end, (blk + 1) * BM);
+    }
+  }
+  for (int e = tid; e < a.E; e += nt) {
+    const int st = o.expert_begin[e], end = o.expert_begin[e + 1];
+    for (int blk = st / BM; blk < end / BM; ++blk) o.block_expert[blk] = e;
+    for (int r = st + s_en[e]; r < end; ++r) o.sorted_p[r] = static_cast<int32_t>(a.P);
+  }
+  if (tid == 0) {
+    int dropped = 0;
+    for (int c = 0; c < a.nchunks; ++c) dropped += a.chunk_invalid[c];
+    o.totals[0] = s_rows;
+    o.totals[1] = s_rows / BM;
+    o.totals[2] = s_runs;
+    o.totals[3] = dropped;
+  }
+  __syncthreads();   // the runs written above are visible to the whole CTA
+  // 9. first run of each block: run i owns the blocks after the previous run's block up
+  //    to its own (blocks without runs point at the next run); blocks after the last
+  //    run point past the end
+  const int nblocks = s_rows / BM;
+  for (int i = tid; i < s_runs; i += nt) {
+    const int blk = o.runs[4 * static_cast<int64_t>(i)];
+    const int prev = i == 0 ? -1 : o.runs[4 * static_cast<int64_t>(i - 1)];
+    for (int q = prev + 1; q <= blk; ++q) o.block_runs[q] = i;
+  }
+  const int last = s_runs > 0 ? o.runs[4 * static_cast<int64_t>(s_runs - 1)] : -1;
+  for (int q = last + 1 + tid; q <= nblocks; q += nt) o.block_runs[q] = s_runs;
+}
+
 // Phase 3 for one chunk whose sorted keys are in keys[] (shared): place each pair.
 __device__ void scatter_phase(const AlignLaunch& a, const uint32_t* keys, int chunk) {
   const int CH = 1 << a.ch_log2;
@@ -493,7 +610,21 @@ cudaError_t launch_align(const AlignLaunch& a, cudaStream_t s) {
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
   }
-  align_scan_kernel<<<1, 1024, 0, s>>>(a);
+  const int64_t nb_buckets = static_cast<int64_t>(a.E) * (a.L + 1);
+  if (nb_buckets <= kScanSmemBuckets) {
+    const size_t smem = static_cast<size_t>(3 * nb_buckets + a.E) * sizeof(int32_t);
+    static bool attr_set = false;   // one device model per process
+    if (!attr_set) {
+      const cudaError_t e2 = cudaFuncSetAttribute(align_scan_smem_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                  static_cast<int>((3 * kScanSmemBuckets + MOE_LORA_MAX_EXPERTS) *
+                                                                   sizeof(int32_t)));
+      if (e2 != cudaSuccess) return e2;
+      attr_set = true;
+    }
+    align_scan_smem_kernel<<<1, 1024, smem, s>>>(a);
+  } else {
+    align_scan_kernel<<<1, 1024, 0, s>>>(a);
+  }
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   if (a.nchunks > 0) {

@@ -455,3 +455,49 @@ def test_layer_graph_replay(ml, torch, oracle, name):
         assert elem <= TOL, (wl.name, elem, norm)
     finally:
         graph.close()
+
+
+@pytest.mark.parametrize("block_m", [16, 64, 128, 256])
+def test_rank_padding_may_hold_any_finite_values(ml, torch, oracle, block_m):
+    """A and B rows at or beyond each adapter's rank are outside the layer.  The kernels
+    read them in 16-rank chunks, but the shrinks write S = 0 at those ranks (a select,
+    not a product), so finite junk there changes nothing: the device banks get N(0,1)
+    junk in every padding row, the oracle sees the clean banks."""
+    wl = W.custom(name="pad", T=120, H=320, I=448, E=4, k=2, L=4, ranks=(40, 8, 24, 48),
+                  lora_mode="uniform_with_none")
+    logits, lora, x, w = inputs(wl)
+    dev = {n: to_dev(w[n], torch) for n in ("W_gu", "W_dn", "A_gu", "B_gu", "A_dn", "B_dn")}
+    g = torch.Generator(device="cuda").manual_seed(5)
+    for name in ("A_gu", "B_gu", "A_dn", "B_dn"):
+        t = dev[name]
+        for a, r in enumerate(wl.ranks):
+            pad = t[a, :, r:, :]
+            pad.copy_(torch.randn(pad.shape, generator=g, device="cuda").to(torch.bfloat16))
+    d = dims_of(wl, block_m, ml)
+    layer = ml.Layer(d, dev)
+    out = layer.step(to_dev(logits, torch), to_dev(lora, torch), to_dev(x, torch))
+    torch.cuda.synchronize()
+    assert int(layer.status.item()) == 0
+    ids, tw = oracle.route(logits, wl.k)
+    ref = oracle.forward(x, ids, tw.astype(np.float32), lora, w)
+    elem, norm = parity_error(out.float().cpu().numpy(), ref)
+    assert elem <= TOL, (block_m, elem, norm)
+
+
+def test_align_scan_in_global_memory(ml, torch, oracle):
+    """More than 16,384 (expert, adapter) buckets (1024 experts x 17): the chunked align's
+    scan keeps its per-bucket arrays in global scratch instead of shared memory; bit-exact
+    against the oracle, as the shared-memory scan is in every other chunked case."""
+    wl = W.custom(name="nb17k", T=6000, H=64, I=64, E=1024, k=1, L=16, ranks=(16,) * 16,
+                  lora_mode="zipf_with_none", bias_std=0.5, none_frac=0.1)
+    assert wl.E * (wl.L + 1) > 16384 and wl.T * wl.k > 4096
+    logits, lora = W.make_routing(wl, 0)
+    ids, _ = oracle.route(logits, wl.k)
+    for bm in (16, 128):
+        d = dims_of(wl, bm, ml)
+        a_bytes, _ = ml.workspace_size(d)
+        bufs = ml.alloc_align(d)
+        ws = torch.empty(a_bytes, dtype=torch.uint8, device="cuda")
+        ml.align(d, to_dev(ids, torch), to_dev(lora, torch), bufs, ws)
+        torch.cuda.synchronize()
+        assert_align_equal(align_to_numpy(bufs), oracle.align(ids, lora, wl.E, wl.L, bm))
