@@ -9,9 +9,12 @@ namespace moe {
 namespace {
 
 // One warp per sorted row: lane 0 records pair_row[p] = row (for the combine and the
-// token-order copy), padding rows are zeroed, and with copy_rows the real rows get
-// x[sorted_p[row] / k] (16-byte vectors).  The same launch zeroes the call's device
-// status word and the GEMMs' tile counters, so the forward needs no memset nodes.
+// token-order copy), and with copy_rows the real rows get x[sorted_p[row] / k] (16-byte
+// vectors).  Padding rows are left as they are: every product treats token rows
+// independently (a padding row only feeds its own accumulator row or column, whose
+// output nothing reads) and the shrinks select S = 0 outside each adapter run.  The
+// same launch zeroes the call's device status word and the GEMMs' tile counters, so the
+// forward needs no memset nodes.
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ sorted_p,
                                                           const int32_t* __restrict__ totals, int64_t max_rows, int vec_per_row,
                                                           int k, int P, uint4* __restrict__ xs,
@@ -30,9 +33,7 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
   if (row >= max_rows || row >= totals[0]) return;
   const int p = sorted_p[row];
   uint4* dst = xs + row * vec_per_row;
-  if (p >= P) {
-    for (int v = lane; v < vec_per_row; v += 32) dst[v] = make_uint4(0, 0, 0, 0);
-  } else {
+  if (p < P) {
     if (lane == 0) pair_row[p] = static_cast<int32_t>(row);
     if (!copy_rows) return;
     const uint4* src = x + static_cast<int64_t>(p / k) * vec_per_row;
