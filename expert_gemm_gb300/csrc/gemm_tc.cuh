@@ -29,11 +29,16 @@
 // Persistent CTAs (one per SM, or as many as fit): each CTA takes tiles from a
 // global counter until none are left, so per-CTA set-up is paid once, the TMA ring
 // runs on from one tile into the next, and with two TMEM accumulator buffers the
-// epilogue of one tile overlaps the MMAs of the next.  Warp roles (192 threads):
-//   warp 0    TMA producer; also takes the next tile id and publishes it through a
-//             small shared ring to the other roles;
+// epilogue of one tile overlaps the MMAs of the next.  Warp roles (224 threads):
+//   warp 0    TMA producer;
 //   warp 1    TMEM owner and MMA issuer;
-//   warps 2-5 epilogue (warp w drains TMEM lanes 32*(w%4) .. +31).
+//   warps 2-5 epilogue (warp w drains TMEM lanes 32*(w%4) .. +31);
+//   warp 6    tile scheduler: takes the next tile id, decodes it with all 32 lanes
+//             (the block's adapter runs are looked up in parallel) and publishes it
+//             through a small shared ring to the other roles.  It claims tile i + 1
+//             when the producer is a few stages from the end of tile i, so the
+//             decode's chain of dependent loads is off the producer's path while the
+//             claim stays late enough for the dynamic balance across CTAs.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -125,6 +130,7 @@ struct GemmBars {
   uint64_t acc_empty[2];     // accumulator buffer drained (one arrive per epilogue warp)
   uint64_t sched_full[4];    // tile id published (producer)
   uint64_t sched_empty[4];   // tile id read (MMA thread + one arrive per epilogue warp)
+  uint64_t sched_req;        // the producer is near the end of its tile: claim the next
   uint64_t drain;            // all MMAs of this CTA finished (teardown)
   uint32_t tmem_base;
   int32_t abort;
@@ -155,9 +161,11 @@ __device__ __forceinline__ int live_tiles(const GemmParams& prm) {
   else return prm.totals[1] * prm.n_ft * prm.ksplit;
 }
 
+// Called by all 32 lanes of the scheduler warp with the same tau; every lane returns
+// the same header, and lane j writes the chunk count and adapter of runs j, j + 32, ...
 template <int MODE, bool SWAP, int BT>
 __device__ __forceinline__ TileHdr decode_tile(int tau, const GemmParams& prm, uint8_t* nch_out, int16_t* ad_out,
-                                               int workers) {
+                                               int workers, int lane) {
   using C = GemmCfg<MODE, SWAP, BT>;
   TileHdr t;
   t.tau = tau;
@@ -216,16 +224,20 @@ __device__ __forceinline__ TileHdr decode_tile(int tau, const GemmParams& prm, u
     t.kb0 = ks * nk_all / prm.ksplit;
     t.nk = (ks + 1) * nk_all / prm.ksplit - t.kb0;
     int chunks = 0;
-    for (int r = 0; r < t.nruns; ++r) {
+    for (int r = lane; r < t.nruns; r += 32) {
       const int a = prm.runs[4 * (t.run0 + r) + 1];
       const int nch = (prm.ranks[a] + kRankChunk - 1) / kRankChunk;
       nch_out[r] = static_cast<uint8_t>(nch);
       ad_out[r] = static_cast<int16_t>(a);
       chunks += nch;
     }
+    chunks = __reduce_add_sync(0xffffffffu, chunks);
     // the runs' rank chunks fill the LoRA stages back to back, CPS per stage
     t.n_it = t.nk + (chunks + C::CPS - 1) / C::CPS;
     t.snch = chunks;
+    t.e = e;   // block t.b is one of expert e's blocks
+    t.row0 = t.b * BT;
+    return t;
   }
   t.e = prm.block_expert[t.b];
   t.row0 = t.b * BT;
@@ -271,8 +283,13 @@ __device__ __forceinline__ void store_out_chunk(const CUtensorMap* map, const ui
   ++n_out;
 }
 
+constexpr int kGemmThreads = 224;
+constexpr int kSchedWarp = 6;
+// The producer asks for the next tile this many stages before the end of its tile.
+constexpr int kClaimAhead = 6;
+
 template <int MODE, bool SWAP, int BT>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kGemmThreads, 1)
     moe_gemm_kernel(const __grid_constant__ GemmMaps maps, const __grid_constant__ GemmParams prm) {
   using C = GemmCfg<MODE, SWAP, BT>;
   const int warp = threadIdx.x >> 5;
@@ -310,8 +327,9 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int j = 0; j < C::SD; ++j) {
       mbar_init(&bars->sched_full[j], 1);
-      mbar_init(&bars->sched_empty[j], 1 + 4);
+      mbar_init(&bars->sched_empty[j], 1 + 1 + 4);   // producer, MMA issuer, epilogue warps
     }
+    mbar_init(&bars->sched_req, 1);
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
     fence_barrier_init();
@@ -347,29 +365,25 @@ __global__ void __launch_bounds__(192, 1)
       int pst = 0;       // gs % STAGES
       uint32_t pph = 0;  // (gs / STAGES) & 1
       for (int i = 0;; ++i) {
-        // take the next tile and publish it (n_live = no more work)
-        // a CTA pair walks a fixed stride of tiles (both CTAs must take the same ones)
-        const int tau = aborted(bars) ? n_live
-                        : C::CTA2     ? static_cast<int>(blockIdx.x >> 1) + i * static_cast<int>(gridDim.x >> 1)
-                                      : atomicAdd(prm.tile_ctr, 1);
+        const Tile* tp = sched_read(bars, i, prm.status);
+        if (!tp) break;
         const int slot = i & 3;
-        if (!mbar_wait(&bars->sched_empty[slot], ((i >> 2) & 1) ^ 1)) {
-          record_timeout(bars, prm.status);
+        const TileHdr t = tp->h;   // registers; the slot (runs' adapters and chunks) is released after the tile
+        if (t.tau >= n_live) {
+          mbar_arrive(&bars->sched_empty[slot]);
           break;
         }
-        TileHdr t;
-        t.tau = n_live;
-        if (tau < n_live)
-          t = decode_tile<MODE, SWAP, BT>(tau, prm, bars->tiles[slot].nch, bars->tiles[slot].ad,
-                                          C::CTA2 ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x));
-        bars->tiles[slot].h = t;
-        mbar_arrive(&bars->sched_full[slot]);   // release: the tile fields are visible to the readers
-        if (tau >= n_live) break;
+        const int claim_at = t.n_it > kClaimAhead ? t.n_it - kClaimAhead : 0;
+        bool claimed = false;
         int lr = 0, lc = 0;   // LoRA run and first rank chunk of the next LoRA stage
         bool ok = true;
         for (int it = 0; it < t.n_it; ++it) {
           const int s = pst;
           const uint32_t ph = pph;
+          if (it == claim_at) {
+            mbar_arrive(&bars->sched_req);
+            claimed = true;
+          }
           if (aborted(bars)) {
             ok = false;
             break;
@@ -459,6 +473,8 @@ __global__ void __launch_bounds__(192, 1)
             pph ^= 1;
           }
         }
+        if (!claimed) mbar_arrive(&bars->sched_req);   // the scheduler waits for one request per tile
+        mbar_arrive(&bars->sched_empty[slot]);
         if (!ok) break;
       }
       // Leave no copy in flight after an abort: wait (bounded) for the last stages issued.
@@ -578,6 +594,38 @@ __global__ void __launch_bounds__(192, 1)
         if (!ok) break;
       }
       commit(&bars->drain);   // arrives once every MMA issued above has completed
+    }
+  } else if (warp == kSchedWarp) {
+    // ------------------------------------------------------------ tile scheduler
+    // n_live = no more work; a CTA pair walks a fixed stride of tiles (both CTAs
+    // must take the same ones)
+    const int workers = C::CTA2 ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+    for (int i = 0;; ++i) {
+      const int slot = i & 3;
+      int tau = n_live;
+      if (lane == 0) {
+        // tile i > 0 once the producer has asked for it; the slot once its last tile is done
+        bool ok = i == 0 || mbar_wait(&bars->sched_req, (i - 1) & 1);
+        ok = ok && mbar_wait(&bars->sched_empty[slot], ((i >> 2) & 1) ^ 1);
+        if (!ok) {
+          record_timeout(bars, prm.status);
+          tau = -1;
+        } else if (!aborted(bars)) {
+          tau = C::CTA2 ? static_cast<int>(blockIdx.x >> 1) + i * workers : atomicAdd(prm.tile_ctr, 1);
+        }
+      }
+      tau = __shfl_sync(0xffffffffu, tau, 0);
+      if (tau < 0) break;   // a wait gave up: the readers' own bounded waits end their loops
+      TileHdr t;
+      t.tau = n_live;
+      if (tau < n_live) t = decode_tile<MODE, SWAP, BT>(tau, prm, bars->tiles[slot].nch, bars->tiles[slot].ad,
+                                                        workers, lane);
+      __syncwarp();   // every lane's run entries are written before lane 0 publishes
+      if (lane == 0) {
+        bars->tiles[slot].h = t;
+        mbar_arrive(&bars->sched_full[slot]);   // release: the tile fields are visible to the readers
+      }
+      if (tau >= n_live) break;
     }
   } else {
     // ------------------------------------------------------------ epilogue
@@ -846,7 +894,7 @@ __global__ void __launch_bounds__(192, 1)
   }
 
   if constexpr (C::TMA_STORE) {
-    if (warp >= 2 && lane == 0) bulk_wait_all();   // the epilogue's output stores have completed
+    if (warp >= 2 && warp < kSchedWarp && lane == 0) bulk_wait_all();   // the epilogue's output stores have completed
   }
   __syncwarp();   // lanes of every warp reconverge before the CTA barrier
   tc_fence_before_sync();
@@ -875,7 +923,7 @@ cudaError_t launch_gemm_t(const GemmMaps& maps, const GemmParams& prm, int64_t m
   else cap_tiles = max_blocks * prm.n_ft * prm.ksplit;
   if (cap_tiles <= 0) return cudaSuccess;
   cudaLaunchConfig_t cfg = {};
-  cfg.blockDim = dim3(192, 1, 1);
+  cfg.blockDim = dim3(kGemmThreads, 1, 1);
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
@@ -914,7 +962,7 @@ cudaError_t launch_gemm_t(const GemmMaps& maps, const GemmParams& prm, int64_t m
       if (occ > sms / 2) occ = sms / 2;
       max_ctas = 2 * static_cast<int64_t>(occ);
     } else {
-      err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, 192, C::SMEM_BYTES);
+      err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kGemmThreads, C::SMEM_BYTES);
       if (err != cudaSuccess) return err;
       // The query can answer for a smaller shared-memory carveout than the launch gets;
       // the CTAs that fit by shared memory, registers, threads and TMEM co-reside
@@ -923,9 +971,9 @@ cudaError_t launch_gemm_t(const GemmMaps& maps, const GemmParams& prm, int64_t m
       err = cudaFuncGetAttributes(&fa, kern);
       if (err != cudaSuccess) return err;
       int fit = smem_sm / (C::SMEM_BYTES + smem_rsv);
-      const int by_regs = fa.numRegs > 0 ? 65536 / (fa.numRegs * 192) : fit;
+      const int by_regs = fa.numRegs > 0 ? 65536 / (fa.numRegs * kGemmThreads) : fit;
       if (fit > by_regs) fit = by_regs;
-      if (fit > 2048 / 192) fit = 2048 / 192;
+      if (fit > 2048 / kGemmThreads) fit = 2048 / kGemmThreads;
       if (occ < fit) occ = fit;
       if (occ < 1) occ = 1;
       // co-resident CTAs share TMEM: keep their accumulators within its 512 columns
