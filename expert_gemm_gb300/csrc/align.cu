@@ -106,6 +106,29 @@ __device__ void bitonic_sort(uint32_t* keys, int n) {
   __syncthreads();
 }
 
+// Ascending sort of n <= blockDim.x keys in shared memory by rank counting: key i goes
+// to the number of keys below it (equal keys -- only the invalid marker repeats -- in
+// index order).  One pass over the keys per thread, two barriers; for the few keys of
+// a decode batch this replaces the bitonic network's chain of dependent exchange
+// stages.  Ends with a barrier.
+constexpr int kRankSortMax = 512;
+__device__ void rank_sort(uint32_t* keys, int n) {
+  const int t = threadIdx.x;
+  __syncthreads();   // the keys every thread wrote
+  uint32_t mine = 0;
+  int rank = 0;
+  if (t < n) {
+    mine = keys[t];
+    for (int j = 0; j < n; ++j) {
+      const uint32_t o = keys[j];   // the same word for the whole warp: a broadcast read
+      rank += (o < mine) || (o == mine && j < t);
+    }
+  }
+  __syncthreads();
+  if (t < n) keys[rank] = mine;
+  __syncthreads();
+}
+
 // Phase 1 for one chunk: keys of its pairs sorted in keys[] (shared), per-bucket
 // counts of the chunk and its invalid-pair count written to global scratch.  ids: the
 // expert ids [P] (global, or shared when the same CTA has just routed them).
@@ -480,7 +503,8 @@ __device__ int small_keys(const AlignLaunch& a, const int32_t* ids, uint32_t* ke
     keys[i] = key;
   }
   if (inval) atomicAdd(&s_invalid, inval);
-  bitonic_sort(keys, CH);
+  if (CH <= static_cast<int>(blockDim.x) && CH <= kRankSortMax) rank_sort(keys, CH);
+  else bitonic_sort(keys, CH);
   return s_invalid;
 }
 

@@ -36,31 +36,34 @@ __device__ __forceinline__ void route_token_n(const float* __restrict__ l, int E
   float my_v = 0.f;     // lane j: the j-th chosen logit and expert
   int my_e = 0;
   for (int j = 0; j < k; ++j) {
-    float bv = -INFINITY;
+    // this lane's best remaining expert (ties: the lower index, i.e. the lower slot)
+    float bv = 0.f;
     int bi = 0x7fffffff;
 #pragma unroll
     for (int s = 0; s < SLOTS; ++s) {
       const int ex = lane + 32 * s;
       if (ex >= E || (taken & (1u << s))) continue;
       const float v = REGS ? lv[s] : l[ex];
-      if (bi == 0x7fffffff || v > bv || (v == bv && ex < bi)) {
+      if (bi == 0x7fffffff || v > bv) {
         bv = v;
         bi = ex;
       }
     }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-      if (oi != 0x7fffffff && (bi == 0x7fffffff || ov > bv || (ov == bv && oi < bi))) {
-        bv = ov;
-        bi = oi;
-      }
-    }
-    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    // the warp's best: the largest logit by an order-preserving integer image (-0 and
+    // +0 made equal, as the float comparison has them), then the lowest expert index
+    // among the lanes holding it
+    const float z0 = bv + 0.0f;
+    const uint32_t u = __float_as_uint(z0);
+    const uint32_t key = bi == 0x7fffffff ? 0u : ((u & 0x80000000u) ? ~u : (u | 0x80000000u));
+    const uint32_t kmax = __reduce_max_sync(0xffffffffu, key);
+    const int win = static_cast<int>(__reduce_min_sync(0xffffffffu, key == kmax && bi != 0x7fffffff
+                                                                         ? static_cast<uint32_t>(bi)
+                                                                         : 0xffffffffu));
+    const float wv = __shfl_sync(0xffffffffu, bv, win & 31);
+    if ((win & 31) == lane) taken |= 1u << (win >> 5);
     if (lane == j) {
-      my_v = bv;
-      my_e = bi;
+      my_v = wv;
+      my_e = win;
     }
   }
   // every lane forms the same sum, in choice order
