@@ -60,6 +60,11 @@ struct GemmParams {
   int32_t n_ft;                 // feature tiles per token block (kGateUp, kDown)
   int32_t ksplit;               // K splits; each split stores its own partial sums
   int32_t lora_after_pdl;       // previous kernel is the shrink: wait for it only before the LoRA K-steps
+  // kShrink on 128-row token blocks: the rank-chunk groups (block, first chunk) of the
+  // block-diagonal shrink tiles and their count, built by the gather launch
+  const int32_t* plan_block;
+  const int32_t* plan_c0;
+  const int32_t* plan_count;
   int32_t ranks[MOE_LORA_MAX_ADAPTERS];
 };
 
@@ -106,9 +111,25 @@ inline bool gather_token_order(int64_t T, int H) { return T * static_cast<int64_
 // the sorted row of every placed pair in
 // pair_row [T*k], and zeroes *status and the n_ctr tile counters of the forward's
 // GEMM launches.
+// The group table of the block-diagonal shrink (128-row token blocks): the rank chunks
+// of each block's adapter runs, in run order, cut into groups of kShrinkGroupChunks;
+// group g is (plan_block[g], plan_c0[g] = its first chunk inside the block), groups in
+// block order, plan_count[0] groups in all.  block_chunks is [blocks] scratch.
+constexpr int kShrinkGroupChunks = 16;
+struct ShrinkPlanArgs {
+  const int32_t* block_runs;   // [blocks+1]
+  const int32_t* runs;         // [runs][4]
+  int32_t* block_chunks;
+  int32_t* plan_block;
+  int32_t* plan_c0;
+  int32_t* plan_count;
+  int32_t ranks[MOE_LORA_MAX_ADAPTERS];
+};
+// plan: when non-null, one extra CTA of the launch builds the group table (it reads
+// only the align outputs, so it overlaps the row copies).
 cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* sorted_p, const int32_t* totals, int64_t max_rows,
                                int H, int k, int P, uint16_t* x_sorted, int32_t* pair_row, int32_t* status,
-                               int32_t* ctr, int n_ctr, cudaStream_t s);
+                               int32_t* ctr, int n_ctr, const ShrinkPlanArgs* plan, cudaStream_t s);
 // out[t] = bf16(sum_j topk_w[t,j] * y(row of pair t*k+j)) in a fixed order; y is bf16
 // [rows][H] when ksplit == 1, else fp32 partials [ksplit][part_rows][H] summed in order.
 cudaError_t launch_combine(const void* y, int ksplit, int64_t part_rows, const int32_t* pair_row,
@@ -136,8 +157,10 @@ struct ShrinkRowsLaunch {
 };
 cudaError_t launch_shrink_rows(const ShrinkRowsLaunch& a, int64_t max_runs, bool pdl, cudaStream_t s);
 // pdl: launch with programmatic stream serialisation (may overlap the previous kernel).
+// block_diag (kShrink, bt 128 only): the block-diagonal shrink, whose tiles are the
+// group table's entries (prm.plan_*, built by the gather launch of the same forward).
 cudaError_t launch_gemm(int mode, int bt, const GemmMaps& maps, const GemmParams& prm, int64_t max_blocks,
-                        int64_t max_runs, bool pdl, cudaStream_t s);
+                        int64_t max_runs, bool pdl, cudaStream_t s, bool block_diag = false);
 // K elements per pipeline stage and stage count of the compiled GEMM for (mode, bt);
 // false if no kernel is compiled for it.  Host only, no device calls.
 bool gemm_stage_shape(int mode, int bt, int* k_tile, int* stages);

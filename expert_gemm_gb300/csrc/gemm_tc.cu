@@ -4,7 +4,12 @@
 namespace moe {
 
 cudaError_t launch_gemm(int mode, int bt, const GemmMaps& maps, const GemmParams& prm, int64_t max_blocks,
-                        int64_t max_runs, bool pdl, cudaStream_t s) {
+                        int64_t max_runs, bool pdl, cudaStream_t s, bool block_diag) {
+  // the block-diagonal shrink of 128-row blocks: its own kernel, fed by the group table
+  if (block_diag) {
+    if (mode != kShrink || bt != 128) return cudaErrorInvalidValue;
+    return launch_gemm_t<kShrink, false, 128, true>(maps, prm, max_blocks, max_runs, pdl, s);
+  }
 #define MOE_GEMM_CASE(BT_, SWAP_)                                                                       \
   if (bt == BT_) {                                                                                      \
     switch (mode) {                                                                                     \

@@ -48,9 +48,15 @@
 
 namespace moe {
 
-template <int MODE, bool SWAP, int BT>
+template <int MODE, bool SWAP, int BT, bool BD = false>
 struct GemmCfg {
   static constexpr bool kLora = MODE != kShrink;
+  // BD: the block-diagonal shrink of 128-row token blocks: a tile is one group of up to
+  // 16 rank chunks of the block's adapter runs, N = their ranks side by side, so a
+  // stage brings up to 32 KB of A rows (the HBM stream) per 16 KB of token rows.  Its
+  // tiles come from the group table the gather launch builds.
+  static constexpr bool BDIAG = BD;
+  static_assert(!BD || (MODE == kShrink && !SWAP && BT == 128), "block-diagonal tiles: the 128-row shrink");
   // 256-token blocks of gate_up / down run on a CTA pair (a cluster of 2): one 2-SM
   // MMA of M = 256 tokens x N = 256 weight rows per K-step; each CTA stages its own
   // 128 token rows and half of the weight rows, and holds its tokens' accumulator.
@@ -63,7 +69,7 @@ struct GemmCfg {
   static constexpr int CPS = BK / kRankChunk;         // LoRA rank chunks per stage
   // weight-side rows staged per K-tile (a shrink's A: rank <= 64 rows, so the weight-
   // streaming shrink issues M = 64 MMAs over them)
-  static constexpr int WROWS = MODE == kShrink ? 64 : (CTA2 ? 128 : 256);
+  static constexpr int WROWS = MODE == kShrink ? (BDIAG ? 256 : 64) : (CTA2 ? 128 : 256);
   static constexpr int WM = SWAP ? (MODE == kShrink ? 64 : 128) : 0;   // MMA M of weight-streaming tiles
   static constexpr int W_BYTES = WROWS * ROWB;
   static constexpr int T_BYTES = TROWS * ROWB;
@@ -78,7 +84,7 @@ struct GemmCfg {
   // accumulators: non-swapped MT tiles of M=128 tokens x N; swapped NH tiles of 128 x BT
   static constexpr int NH = MODE == kShrink ? 1 : 2;
   static constexpr int MT = SWAP ? 1 : TROWS / 128;
-  static constexpr int NACC = MODE == kShrink ? 64 : 256;   // columns of one non-swapped accumulator
+  static constexpr int NACC = MODE == kShrink && !BDIAG ? 64 : 256;   // columns of one non-swapped accumulator
   static constexpr int ACC_COLS = SWAP ? NH * BT : MT * NACC;
   static constexpr int NBUF = 2 * ACC_COLS <= 512 ? 2 : 1;  // TMEM accumulator buffers
   static constexpr int TMEM_NEED = NBUF * ACC_COLS;
@@ -117,11 +123,29 @@ struct TileHdr {
   int srun, sa, snch;     // kShrink: run, adapter, rank chunks
   int ks;                 // K split of this tile
 };
-struct Tile {
-  TileHdr h;                    // copied to registers by every reader
-  uint8_t nch[kMaxBlockRuns];   // rank chunks of each adapter run of the block
-  int16_t ad[kMaxBlockRuns];    // adapter of each run (the producer's LoRA loads)
+// Block-diagonal shrink: the part of one adapter run inside a tile's chunk group.
+struct ShrinkSeg {
+  int32_t run;        // run index (its S tile)
+  int16_t ad;         // adapter
+  int16_t beg, end;   // the run's rows inside the block
+  int16_t rank;       // the adapter's rank
+  uint8_t cl;         // first chunk of the run in this tile
+  uint8_t n;          // chunks of the run in this tile
+  uint8_t pos;        // tile-local chunk of chunk cl (its A rows and accumulator columns)
+  uint8_t pad;
 };
+static_assert(sizeof(ShrinkSeg) == 16, "segment layout");
+static_assert(kShrinkGroupChunks * sizeof(ShrinkSeg) <= kMaxBlockRuns, "segments fit the run-chunk array");
+struct Tile {
+  TileHdr h;                               // copied to registers by every reader
+  alignas(16) uint8_t nch[kMaxBlockRuns];  // rank chunks of each adapter run of the block
+                                           //   (block-diagonal shrink: ShrinkSeg[16] instead)
+  int16_t ad[kMaxBlockRuns];               // adapter of each run (the producer's LoRA loads)
+};
+__device__ __forceinline__ ShrinkSeg* tile_segs(uint8_t* nch) { return reinterpret_cast<ShrinkSeg*>(nch); }
+__device__ __forceinline__ const ShrinkSeg* tile_segs(const uint8_t* nch) {
+  return reinterpret_cast<const ShrinkSeg*>(nch);
+}
 
 struct GemmBars {
   uint64_t full[8];          // stage loaded (TMA transaction bytes)
@@ -155,18 +179,19 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
 // rounded to bf16): the epilogue's instruction count competes with the MMA issuer.
 __device__ __forceinline__ float silu_f(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
-template <int MODE>
+template <int MODE, bool SWAP, int BT, bool BD>
 __device__ __forceinline__ int live_tiles(const GemmParams& prm) {
-  if constexpr (MODE == kShrink) return prm.totals[2] * prm.ksplit;
+  if constexpr (BD) return *prm.plan_count;
+  else if constexpr (MODE == kShrink) return prm.totals[2] * prm.ksplit;
   else return prm.totals[1] * prm.n_ft * prm.ksplit;
 }
 
 // Called by all 32 lanes of the scheduler warp with the same tau; every lane returns
 // the same header, and lane j writes the chunk count and adapter of runs j, j + 32, ...
-template <int MODE, bool SWAP, int BT>
+template <int MODE, bool SWAP, int BT, bool BD>
 __device__ __forceinline__ TileHdr decode_tile(int tau, const GemmParams& prm, uint8_t* nch_out, int16_t* ad_out,
                                                int workers, int lane) {
-  using C = GemmCfg<MODE, SWAP, BT>;
+  using C = GemmCfg<MODE, SWAP, BT, BD>;
   TileHdr t;
   t.tau = tau;
   const int nk_all = prm.K / C::BK;
@@ -174,7 +199,64 @@ __device__ __forceinline__ TileHdr decode_tile(int tau, const GemmParams& prm, u
   t.nruns = 0;
   t.f0 = 0;
   t.srun = t.sa = t.snch = 0;
-  if constexpr (MODE == kShrink) {
+  if constexpr (C::BDIAG) {
+    // group tau: chunks [c0, c0 + 16) of block b's runs, in run order.  The lanes take
+    // 32 runs at a time: each its chunk count, a warp scan places its chunks in the
+    // block, and the runs overlapping the group become the tile's segments.
+    const int b = prm.plan_block[tau];
+    const int c0 = prm.plan_c0[tau];
+    const int rb = prm.block_runs[b], re = prm.block_runs[b + 1];
+    t.b = b;
+    t.e = prm.block_expert[b];
+    t.row0 = b * BT;
+    t.ks = 0;
+    t.kb0 = 0;
+    t.nk = nk_all;
+    t.n_it = nk_all;
+    t.run0 = rb;
+    ShrinkSeg* seg = tile_segs(nch_out);
+    int carry = 0, nseg = 0, nch = 0;
+    for (int r0 = rb; r0 < re && carry < c0 + kShrinkGroupChunks; r0 += 32) {
+      const int j = r0 + lane;
+      int a = 0, n = 0, beg = 0, end = 0;
+      if (j < re) {
+        a = prm.runs[4 * j + 1];
+        beg = prm.runs[4 * j + 2] - t.row0;
+        end = prm.runs[4 * j + 3] - t.row0;
+        n = (prm.ranks[a] + kRankChunk - 1) / kRankChunk;
+      }
+      int incl = n;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+      }
+      const int cs = carry + incl - n;   // the block-local chunk where run j starts
+      const int lo = cs > c0 ? cs : c0;
+      const int hi = cs + n < c0 + kShrinkGroupChunks ? cs + n : c0 + kShrinkGroupChunks;
+      const bool take = j < re && lo < hi;
+      const uint32_t m = __ballot_sync(0xffffffffu, take);
+      if (take) {
+        ShrinkSeg sg;
+        sg.run = j;
+        sg.ad = static_cast<int16_t>(a);
+        sg.beg = static_cast<int16_t>(beg);
+        sg.end = static_cast<int16_t>(end);
+        sg.rank = static_cast<int16_t>(prm.ranks[a]);
+        sg.cl = static_cast<uint8_t>(lo - cs);
+        sg.n = static_cast<uint8_t>(hi - lo);
+        sg.pos = static_cast<uint8_t>(lo - c0);
+        sg.pad = 0;
+        seg[nseg + __popc(m & ((1u << lane) - 1u))] = sg;
+      }
+      nseg += __popc(m);
+      nch += __reduce_add_sync(0xffffffffu, take ? hi - lo : 0);
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    t.nruns = nseg;
+    t.snch = nch;
+    return t;
+  } else if constexpr (MODE == kShrink) {
     // the K splits of one run are consecutive tiles
     t.srun = tau / prm.ksplit;
     t.ks = tau % prm.ksplit;
@@ -288,10 +370,10 @@ constexpr int kSchedWarp = 6;
 // The producer asks for the next tile this many stages before the end of its tile.
 constexpr int kClaimAhead = 6;
 
-template <int MODE, bool SWAP, int BT>
+template <int MODE, bool SWAP, int BT, bool BD>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     moe_gemm_kernel(const __grid_constant__ GemmMaps maps, const __grid_constant__ GemmParams prm) {
-  using C = GemmCfg<MODE, SWAP, BT>;
+  using C = GemmCfg<MODE, SWAP, BT, BD>;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t rank = C::CTA2 ? cluster_ctarank() : 0u;   // 0: issues the pair's MMAs
@@ -309,7 +391,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     pdl_trigger();
   }
   // The routing metadata comes from align, complete before the previous kernel began.
-  const int n_live = live_tiles<MODE>(prm);
+  const int n_live = live_tiles<MODE, SWAP, BT, BD>(prm);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -416,6 +498,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               mbar_arrive_expect_tx(fb, C::W_BYTES + C::T_BYTES);
               tma_load_3d(wdst, &maps.w, fb, k0, t.f0, t.e);
               tma_load_3d(wdst + 128 * C::ROWB, &maps.w, fb, k0, t.f0 + 128, t.e);
+            } else if constexpr (C::BDIAG) {
+              // each segment's rank rows in one box, at its tile-local chunk
+              const ShrinkSeg* seg = tile_segs(bars->tiles[slot].nch);
+              mbar_arrive_expect_tx(fb, t.snch * kRankChunk * C::ROWB + C::T_BYTES);
+              for (int sgi = 0; sgi < t.nruns; ++sgi) {
+                const ShrinkSeg sg = seg[sgi];
+                tma_load_3d(wdst + sg.pos * kRankChunk * C::ROWB, sg.n <= 1 ? &maps.w : &maps.w_rank[sg.n - 2], fb,
+                            k0, sg.cl * kRankChunk, sg.ad * prm.E + t.e);
+              }
             } else {
               // the adapter's rank rows in one box: the producer thread's issue loop, not
               // the bytes, paces the shrink's stages
@@ -618,7 +709,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (tau < 0) break;   // a wait gave up: the readers' own bounded waits end their loops
       TileHdr t;
       t.tau = n_live;
-      if (tau < n_live) t = decode_tile<MODE, SWAP, BT>(tau, prm, bars->tiles[slot].nch, bars->tiles[slot].ad,
+      if (tau < n_live) t = decode_tile<MODE, SWAP, BT, BD>(tau, prm, bars->tiles[slot].nch, bars->tiles[slot].ad,
                                                         workers, lane);
       __syncwarp();   // every lane's run entries are written before lane 0 publishes
       if (lane == 0) {
@@ -653,7 +744,31 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int row0 = t.row0 + 128 * static_cast<int>(rank), f0 = t.f0;
       if (ok) {
         uint32_t v[16], u[16];
-        if constexpr (MODE == kShrink) {
+        if constexpr (C::BDIAG) {
+          // each segment's chunks: the run's rank columns of row m, zero outside the run
+          const ShrinkSeg* seg = tile_segs(tp->nch);
+          for (int sgi = 0; sgi < t.nruns; ++sgi) {
+            const ShrinkSeg sg = seg[sgi];
+            const bool in_run = m >= sg.beg && m < sg.end;
+            uint16_t* srow = prm.s_out + (static_cast<size_t>(sg.run) * BT + m) * prm.r_pad;
+            for (int c = 0; c < sg.n; ++c) {
+              tmem_ld16(tq + (sg.pos + c) * kRankChunk, v);
+              tmem_ld_wait();
+              const int col0 = (sg.cl + c) * kRankChunk;   // rank column of the run
+              uint32_t pk[8];
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const int c2 = col0 + 2 * j;
+                const float a0 = (in_run && c2 < sg.rank) ? __uint_as_float(v[2 * j]) : 0.f;
+                const float a1 = (in_run && c2 + 1 < sg.rank) ? __uint_as_float(v[2 * j + 1]) : 0.f;
+                pk[j] = pack_bf16x2(a0, a1);
+              }
+              uint4* dst = reinterpret_cast<uint4*>(srow + col0);
+              dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+              dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+            }
+          }
+        } else if constexpr (MODE == kShrink) {
           const int beg = prm.runs[4 * t.srun + 2] - row0;
           const int end = prm.runs[4 * t.srun + 3] - row0;
           const int r_a = prm.ranks[t.sa];
@@ -913,13 +1028,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if constexpr (C::CTA2) cluster_sync();
 }
 
-template <int MODE, bool SWAP, int BT>
+template <int MODE, bool SWAP, int BT, bool BD = false>
 cudaError_t launch_gemm_t(const GemmMaps& maps, const GemmParams& prm, int64_t max_blocks, int64_t max_runs,
                           bool pdl, cudaStream_t s) {
-  using C = GemmCfg<MODE, SWAP, BT>;
-  auto kern = moe_gemm_kernel<MODE, SWAP, BT>;
+  using C = GemmCfg<MODE, SWAP, BT, BD>;
+  auto kern = moe_gemm_kernel<MODE, SWAP, BT, BD>;
   int64_t cap_tiles;
-  if constexpr (MODE == kShrink) cap_tiles = max_runs * prm.ksplit;
+  if constexpr (C::BDIAG) cap_tiles = max_runs + max_blocks;   // groups <= chunks / 16 + blocks <= runs + blocks
+  else if constexpr (MODE == kShrink) cap_tiles = max_runs * prm.ksplit;
   else cap_tiles = max_blocks * prm.n_ft * prm.ksplit;
   if (cap_tiles <= 0) return cudaSuccess;
   cudaLaunchConfig_t cfg = {};

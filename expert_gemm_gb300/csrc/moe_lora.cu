@@ -208,7 +208,7 @@ AlignLayout align_layout(const moe_lora_dims* d) {
 
 // ---- forward scratch layout
 struct FwdLayout {
-  size_t xs, hs, sgu, sdn, y, prow, ctr, gpart, pgu, pdn, bytes;
+  size_t xs, hs, sgu, sdn, y, prow, ctr, gpart, pgu, pdn, plan, bytes;
   int n_ctr, ks_gu, ks_dn;
 };
 constexpr int kNumGemmCounters = 4;   // tile counters: shrink_gu, gate_up, shrink_dn, down
@@ -233,6 +233,21 @@ bool shrink_on_cores(const moe_lora_dims* d, const Caps& cap) {
 }
 int shrink_slices(int K) { return (K + moe::kShrinkSlice - 1) / moe::kShrinkSlice; }
 int shrink_ksplit(const moe_lora_dims* d, const Caps& cap, int K);
+// The tcgen05 shrink of 128-row token blocks can run block-diagonal tiles (several
+// adapter runs side by side in N, from a group table the gather launch builds): each
+// stage then brings up to 32 KB of A rows instead of one run's 2-8 KB.  A block gives
+// one to a few such tiles against one per run, so they pay once the blocks alone fill
+// the SMs twice over (sweep T = 4096: 319 blocks, shrinks 227/96 -> 193/80 us); with
+// fewer blocks (wide: 64) the long K loops of too few tiles leave SMs idle
+// (shrinks 41/77 -> 68/161 us) and the per-run tiles stay.
+std::atomic<int> g_shrink_tiles{0};   // test hook: 0 by shape, 1 block-diagonal, 2 per run
+bool block_diag_space(const moe_lora_dims* d) { return d->L > 0 && d->block_m == 128; }
+bool block_diag_shrink(const moe_lora_dims* d, const Caps& cap) {
+  if (!block_diag_space(d)) return false;
+  const int mode = g_shrink_tiles.load(std::memory_order_relaxed);
+  if (mode != 0) return mode == 1;
+  return cap.blocks >= 2 * kPlanSMs;
+}
 int gate_up_ksplit(const moe_lora_dims* d, const Caps& cap);
 int down_ksplit(const moe_lora_dims* d, const Caps& cap);
 FwdLayout fwd_layout(const moe_lora_dims* d) {
@@ -257,6 +272,10 @@ FwdLayout fwd_layout(const moe_lora_dims* d) {
   const bool cores = shrink_on_cores(d, c);
   l.pgu = off; off += up256((size_t)(cores ? shrink_slices(d->H) : shrink_ksplit(d, c, d->H)) * s_part);
   l.pdn = off; off += up256((size_t)(cores ? shrink_slices(d->I) : shrink_ksplit(d, c, d->I)) * s_part);
+  // group table of the block-diagonal shrink (128-row blocks): [groups] block, [groups]
+  // first chunk, [blocks] chunk counts, the group count; groups <= runs + blocks
+  l.plan = off;
+  if (block_diag_space(d)) off += up256((size_t)(2 * (c.runs + c.blocks) + c.blocks + 1) * 4);
   l.n_ctr = kNumGemmCounters + 2 * 4 * (int)c.runs;
   l.bytes = off;
   return l;
@@ -596,6 +615,22 @@ int do_forward(const moe_lora_dims* d, const uint16_t* x, const float* topk_w, c
   p.lora_after_pdl = 0;
   p.max_runs = (int32_t)cap.runs;
   for (int a = 0; a < d->L; ++a) p.ranks[a] = d->ranks[a];
+  const bool bdiag = block_diag_shrink(d, cap);
+  moe::ShrinkPlanArgs plan{};
+  if (bdiag) {
+    int32_t* pb = reinterpret_cast<int32_t*>(base + l.plan);
+    const int64_t G = cap.runs + cap.blocks;
+    plan.block_runs = al->block_runs;
+    plan.runs = al->runs;
+    plan.plan_block = pb;
+    plan.plan_c0 = pb + G;
+    plan.block_chunks = pb + 2 * G;
+    plan.plan_count = pb + 2 * G + cap.blocks;
+    for (int a = 0; a < d->L; ++a) plan.ranks[a] = d->ranks[a];
+    p.plan_block = plan.plan_block;
+    p.plan_c0 = plan.plan_c0;
+    p.plan_count = plan.plan_count;
+  }
 
   auto mark = [&](int i) -> cudaError_t {
     return ev ? cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), s) : cudaSuccess;
@@ -607,7 +642,7 @@ int do_forward(const moe_lora_dims* d, const uint16_t* x, const float* topk_w, c
   const bool lora = d->L > 0;
   MOE_CUDA(mark(0));
   MOE_CUDA(moe::launch_gather_rows(x, al->sorted_p, al->totals, cap.rows, d->H, d->k, p.P, xs, prow, dev_status, ctr,
-                                   l.n_ctr, s));
+                                   l.n_ctr, bdiag ? &plan : nullptr, s));
   MOE_CUDA(mark(1 + MOE_LORA_STAGE_GATHER));
 
   const bool cores = shrink_on_cores(d, cap);
@@ -642,7 +677,7 @@ int do_forward(const moe_lora_dims* d, const uint16_t* x, const float* topk_w, c
     q.s_part = reinterpret_cast<float*>(base + l.pgu);
     q.s_cnt = ctr + kNumGemmCounters;
     if (cores) MOE_CUDA(shrink_rows(xs, A_gu, d->H, sgu, l.pgu, q.s_cnt));
-    else MOE_CUDA(moe::launch_gemm(moe::kShrink, BT, m_sgu, q, cap.blocks, cap.runs, true, s));
+    else MOE_CUDA(moe::launch_gemm(moe::kShrink, BT, m_sgu, q, cap.blocks, cap.runs, true, s, bdiag));
   }
   MOE_CUDA(mark(1 + MOE_LORA_STAGE_SHRINK_GU));
   {
@@ -670,7 +705,7 @@ int do_forward(const moe_lora_dims* d, const uint16_t* x, const float* topk_w, c
     q.s_part = reinterpret_cast<float*>(base + l.pdn);
     q.s_cnt = ctr + kNumGemmCounters + 4 * cap.runs;
     if (cores) MOE_CUDA(shrink_rows(hs, A_dn, d->I, sdn, l.pdn, q.s_cnt));
-    else MOE_CUDA(moe::launch_gemm(moe::kShrink, BT, m_sdn, q, cap.blocks, cap.runs, true, s));
+    else MOE_CUDA(moe::launch_gemm(moe::kShrink, BT, m_sdn, q, cap.blocks, cap.runs, true, s, bdiag));
   }
   MOE_CUDA(mark(1 + MOE_LORA_STAGE_SHRINK_DN));
   {
@@ -724,10 +759,16 @@ LayerLayout layer_layout(const moe_lora_dims* d) {
 
 extern "C" {
 
-int moe_lora_version(void) { return 301; }
+int moe_lora_version(void) { return 302; }
 
 int moe_lora_debug_set_acc_wait_ns(uint64_t ns) {
   g_acc_wait_ns.store(ns, std::memory_order_relaxed);
+  return MOE_LORA_OK;
+}
+
+int moe_lora_debug_set_shrink_tiles(int32_t mode) {
+  if (mode < 0 || mode > 2) return fail(MOE_LORA_EINVAL, "shrink tile mode %d not in {0, 1, 2}", mode);
+  g_shrink_tiles.store(mode, std::memory_order_relaxed);
   return MOE_LORA_OK;
 }
 
@@ -763,6 +804,7 @@ int moe_lora_plan_query(const moe_lora_dims* d, moe_lora_plan* out) {
   const bool lora = d->L > 0;
   const bool cores = shrink_on_cores(d, cap);
   p.shrink_on_cores = cores ? 1 : 0;
+  p.shrink_block_diag = block_diag_shrink(d, cap) ? 1 : 0;
   p.ksplit[0] = lora ? (cores ? shrink_slices(d->H) : shrink_ksplit(d, cap, d->H)) : 0;
   p.ksplit[1] = l.ks_gu;
   p.ksplit[2] = lora ? (cores ? shrink_slices(d->I) : shrink_ksplit(d, cap, d->I)) : 0;

@@ -15,11 +15,71 @@ namespace {
 // output nothing reads) and the shrinks select S = 0 outside each adapter run.  The
 // same launch zeroes the call's device status word and the GEMMs' tile counters, so the
 // forward needs no memset nodes.
+// The group table of the block-diagonal shrink, built by one CTA: each block's rank
+// chunks (sum over its runs of ceil(rank / 16)), then a block-order scan of
+// ceil(chunks / 16) groups per block and one table entry per group.
+__device__ void build_shrink_plan(const ShrinkPlanArgs& pl, const int32_t* __restrict__ totals) {
+  __shared__ int32_t s_warp[32];
+  __shared__ int32_t s_carry;
+  const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5, nw = nt >> 5;
+  const int nb = totals[1], nr = totals[2];
+  for (int b = tid; b < nb; b += nt) pl.block_chunks[b] = 0;
+  __syncthreads();
+  // eight runs' loads in flight per thread before their atomics
+  constexpr int kBatch = 8;
+  for (int j0 = tid; j0 < nr; j0 += kBatch * nt) {
+    int bb[kBatch], aa[kBatch];
+#pragma unroll
+    for (int q = 0; q < kBatch; ++q) {
+      const int j = j0 + q * nt;
+      bb[q] = j < nr ? pl.runs[4 * j] : -1;
+      aa[q] = j < nr ? pl.runs[4 * j + 1] : 0;
+    }
+#pragma unroll
+    for (int q = 0; q < kBatch; ++q)
+      if (bb[q] >= 0) atomicAdd(pl.block_chunks + bb[q], (pl.ranks[aa[q]] + kRankChunk - 1) / kRankChunk);
+  }
+  if (tid == 0) s_carry = 0;
+  __syncthreads();   // the block's atomics are complete and visible to the block
+  for (int base = 0; base < nb; base += nt) {
+    const int b = base + tid;
+    const int g = b < nb ? (__ldcg(pl.block_chunks + b) + kShrinkGroupChunks - 1) / kShrinkGroupChunks : 0;
+    int x = g;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, off);
+      if (lane >= off) x += y;
+    }
+    if (lane == 31) s_warp[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+      int w = lane < nw ? s_warp[lane] : 0;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, w, off);
+        if (lane >= off) w += y;
+      }
+      if (lane < nw) s_warp[lane] = w;
+    }
+    __syncthreads();
+    const int first = s_carry + (warp > 0 ? s_warp[warp - 1] : 0) + x - g;
+    for (int i = 0; i < g; ++i) {
+      pl.plan_block[first + i] = b;
+      pl.plan_c0[first + i] = i * kShrinkGroupChunks;
+    }
+    __syncthreads();   // every thread has read s_carry and s_warp
+    if (tid == 0) s_carry += s_warp[nw - 1];
+    __syncthreads();
+  }
+  if (tid == 0) *pl.plan_count = s_carry;
+}
+
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ sorted_p,
                                                           const int32_t* __restrict__ totals, int64_t max_rows, int vec_per_row,
                                                           int k, int P, uint4* __restrict__ xs,
                                                           int32_t* __restrict__ pair_row, int32_t* __restrict__ status,
-                                                          int32_t* __restrict__ ctr, int n_ctr, bool copy_rows) {
+                                                          int32_t* __restrict__ ctr, int n_ctr, bool copy_rows,
+                                                          const __grid_constant__ ShrinkPlanArgs plan, int plan_ctas) {
   // Launched as a programmatic dependent of whatever precedes the forward (the align):
   // its launch overlaps that kernel's tail, its reads wait for it.
   pdl_wait();
@@ -28,8 +88,12 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
   const int64_t nthr = static_cast<int64_t>(gridDim.x) * blockDim.x;
   if (tid == 0) *status = 0;
   for (int64_t i = tid; i < n_ctr; i += nthr) ctr[i] = 0;
+  if (static_cast<int>(blockIdx.x) < plan_ctas) {   // the first CTA: the shrink's group table
+    build_shrink_plan(plan, totals);
+    return;
+  }
   const int lane = threadIdx.x & 31;
-  const int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int64_t row = static_cast<int64_t>(blockIdx.x - plan_ctas) * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (row >= max_rows || row >= totals[0]) return;
   const int p = sorted_p[row];
   uint4* dst = xs + row * vec_per_row;
@@ -231,10 +295,13 @@ __global__ void __launch_bounds__(kCombineThreads)
 
 cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* sorted_p, const int32_t* totals, int64_t max_rows,
                                int H, int k, int P, uint16_t* x_sorted, int32_t* pair_row, int32_t* status,
-                               int32_t* ctr, int n_ctr, cudaStream_t s) {
+                               int32_t* ctr, int n_ctr, const ShrinkPlanArgs* plan, cudaStream_t s) {
   const int rows_per_cta = 8;
-  int64_t grid = (max_rows + rows_per_cta - 1) / rows_per_cta;
+  const int plan_ctas = plan ? 1 : 0;
+  int64_t grid = (max_rows + rows_per_cta - 1) / rows_per_cta + plan_ctas;
   if (grid < 1) grid = 1;
+  ShrinkPlanArgs pl{};
+  if (plan) pl = *plan;
   // When x is larger than half the 129 MB L2, its k re-reads in sorted-row order come
   // from DRAM: copy in token order then (x read once).  Otherwise one row-order pass.
   const bool token_order = gather_token_order(P / k, H);
@@ -251,7 +318,7 @@ cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* sorted_p, const
     cfg.numAttrs = 1;
     err = cudaLaunchKernelEx(&cfg, gather_rows_kernel, reinterpret_cast<const uint4*>(x), sorted_p, totals, max_rows,
                              H / 8, k, P, reinterpret_cast<uint4*>(x_sorted), pair_row, status, ctr, n_ctr,
-                             !token_order);
+                             !token_order, pl, plan_ctas);
   }
   if (err != cudaSuccess || !token_order) return err;
   const int64_t T = P / k;

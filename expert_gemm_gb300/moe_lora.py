@@ -24,7 +24,8 @@ EXPORTS = ["moe_lora_align_capacity", "moe_lora_workspace_size", "moe_lora_pick_
            "moe_lora_align", "moe_lora_forward", "moe_lora_layer_workspace_size", "moe_lora_layer_host",
            "moe_lora_status_string", "moe_lora_last_error", "moe_lora_version", "moe_lora_align_static",
            "moe_lora_route_align", "moe_lora_plan_query", "moe_lora_layer_graph_create",
-           "moe_lora_layer_graph_run", "moe_lora_layer_graph_destroy", "moe_lora_debug_set_acc_wait_ns"]
+           "moe_lora_layer_graph_run", "moe_lora_layer_graph_destroy", "moe_lora_debug_set_acc_wait_ns",
+           "moe_lora_debug_set_shrink_tiles"]
 STATIC_SCRATCH_BYTES = 4 << 20
 
 
@@ -42,7 +43,7 @@ class Plan(C.Structure):
     _fields_ = [("block_m", C.c_int32), ("table_row", C.c_int32), ("weight_streaming", C.c_int32),
                 ("ksplit", C.c_int32 * 4), ("k_tile", C.c_int32 * 4), ("stages", C.c_int32 * 4),
                 ("launches_route_align", C.c_int32), ("launches_forward", C.c_int32),
-                ("shrink_on_cores", C.c_int32)]
+                ("shrink_on_cores", C.c_int32), ("shrink_block_diag", C.c_int32)]
 
 
 GEMMS = ("shrink_gu", "gate_up", "shrink_dn", "down")
@@ -85,6 +86,8 @@ def load(path: str = LIB_PATH):
     lib.moe_lora_layer_host.argtypes = [DP, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, C.POINTER(i64), vp]
     lib.moe_lora_debug_set_acc_wait_ns.argtypes = [C.c_uint64]
     lib.moe_lora_debug_set_acc_wait_ns.restype = C.c_int
+    lib.moe_lora_debug_set_shrink_tiles.argtypes = [C.c_int32]
+    lib.moe_lora_debug_set_shrink_tiles.restype = C.c_int
     lib.moe_lora_status_string.restype = C.c_char_p
     lib.moe_lora_status_string.argtypes = [C.c_int]
     lib.moe_lora_last_error.restype = C.c_char_p
@@ -151,6 +154,12 @@ def debug_set_acc_wait_ns(ns: int):
     _check(load().moe_lora_debug_set_acc_wait_ns(int(ns)))
 
 
+def debug_set_shrink_tiles(mode: int):
+    """Test hook: tile form of the tcgen05 shrinks of 128-row blocks in later forward
+    calls (0 by shape, 1 block-diagonal, 2 one run per tile).  See moe_lora.h."""
+    _check(load().moe_lora_debug_set_shrink_tiles(int(mode)))
+
+
 def pick_block_m(T: int, k: int, E: int) -> int:
     return load().moe_lora_pick_block_m(T, k, E)
 
@@ -162,7 +171,8 @@ def plan(d: LayerDims) -> dict:
     return {"block_m": p.block_m, "table_row": p.table_row, "weight_streaming": bool(p.weight_streaming),
             "ksplit": dict(zip(GEMMS, p.ksplit)), "k_tile": dict(zip(GEMMS, p.k_tile)),
             "stages": dict(zip(GEMMS, p.stages)), "launches_route_align": p.launches_route_align,
-            "launches_forward": p.launches_forward, "shrink_on_cores": bool(p.shrink_on_cores)}
+            "launches_forward": p.launches_forward, "shrink_on_cores": bool(p.shrink_on_cores),
+            "shrink_block_diag": bool(p.shrink_block_diag)}
 
 
 def align_capacity(d: LayerDims):

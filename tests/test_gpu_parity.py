@@ -184,6 +184,57 @@ def test_ranks_off_the_chunk_grid(ml, torch, oracle, block_m):
     run_case(ml, torch, oracle, wl, block_m=block_m)
 
 
+# Shapes for both shrink tile forms on 128-row blocks: ranks off the 16-chunk grid, and a
+# block with more than 32 adapter runs (the group decode takes them 32 at a time) whose
+# rank chunks fill several 16-chunk groups with runs cut at the group boundaries.
+SHRINK_FORM_CASES = [
+    dict(name="rk48", T=160, H=448, I=320, E=4, k=2, L=4, ranks=(40, 24, 48, 8), lora_mode="uniform_with_none"),
+    dict(name="manyruns", T=300, H=320, I=192, E=2, k=1, L=48, ranks=tuple(16 if a % 3 else 48 for a in range(48)),
+         lora_mode="uniform_with_none"),
+]
+
+
+@pytest.mark.parametrize("form", [1, 2])
+@pytest.mark.parametrize("case", SHRINK_FORM_CASES, ids=lambda c: c["name"])
+def test_shrink_tile_forms(ml, torch, oracle, case, form):
+    """The tcgen05 shrink of 128-row blocks as block-diagonal groups (form 1: up to 16
+    rank chunks of a block's runs per tile) and one run per tile (form 2), against the
+    oracle; align bit for bit.  The shape picks a form by itself (block count against the
+    SMs); the test hook forces each."""
+    wl = W.custom(**case)
+    ml.debug_set_shrink_tiles(form)
+    try:
+        assert ml.plan(dims_of(wl, 128, ml))["shrink_block_diag"] == (form == 1)
+        run_case(ml, torch, oracle, wl, block_m=128)
+    finally:
+        ml.debug_set_shrink_tiles(0)
+
+
+def test_shrink_tile_forms_same_bytes(ml, torch):
+    """Both shrink forms form each S element from the same products summed in the same K
+    order in fp32, rounded once: the layer outputs are identical bit for bit."""
+    wl = W.custom(**SHRINK_FORM_CASES[1])
+    logits, lora, x, w = inputs(wl)
+    outs = []
+    for form in (1, 2):
+        ml.debug_set_shrink_tiles(form)
+        try:
+            layer = ml.Layer(dims_of(wl, 128, ml), dev_weights(w, torch))
+            outs.append(layer.step(to_dev(logits, torch), to_dev(lora, torch), to_dev(x, torch)).clone())
+            torch.cuda.synchronize()
+            assert int(layer.status.item()) == 0
+        finally:
+            ml.debug_set_shrink_tiles(0)
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+
+
+def test_shrink_tile_form_hook_rejects_unknown_modes(ml):
+    with pytest.raises(ml.MoeLoraError):
+        ml.debug_set_shrink_tiles(3)
+    assert ml.plan(dims_of(W.get("sweep_T4096"), 128, ml))["shrink_block_diag"]
+    assert not ml.plan(dims_of(W.get("wide"), 128, ml))["shrink_block_diag"]
+
+
 @pytest.mark.parametrize("T,k", [(512, 8), (4097, 1)])
 def test_align_one_chunk_boundary(ml, torch, oracle, T, k):
     """P = 4096 pairs, the largest batch the one-CTA align takes (layout from the sorted
@@ -474,14 +525,19 @@ def test_rank_padding_may_hold_any_finite_values(ml, torch, oracle, block_m):
             pad = t[a, :, r:, :]
             pad.copy_(torch.randn(pad.shape, generator=g, device="cuda").to(torch.bfloat16))
     d = dims_of(wl, block_m, ml)
-    layer = ml.Layer(d, dev)
-    out = layer.step(to_dev(logits, torch), to_dev(lora, torch), to_dev(x, torch))
-    torch.cuda.synchronize()
-    assert int(layer.status.item()) == 0
     ids, tw = oracle.route(logits, wl.k)
     ref = oracle.forward(x, ids, tw.astype(np.float32), lora, w)
-    elem, norm = parity_error(out.float().cpu().numpy(), ref)
-    assert elem <= TOL, (block_m, elem, norm)
+    for form in ((1, 2) if block_m == 128 else (0,)):   # both shrink tile forms of 128-row blocks
+        ml.debug_set_shrink_tiles(form)
+        try:
+            layer = ml.Layer(d, dev)
+            out = layer.step(to_dev(logits, torch), to_dev(lora, torch), to_dev(x, torch))
+            torch.cuda.synchronize()
+        finally:
+            ml.debug_set_shrink_tiles(0)
+        assert int(layer.status.item()) == 0
+        elem, norm = parity_error(out.float().cpu().numpy(), ref)
+        assert elem <= TOL, (block_m, form, elem, norm)
 
 
 def test_align_scan_in_global_memory(ml, torch, oracle):
