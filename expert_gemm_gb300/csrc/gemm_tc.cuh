@@ -61,7 +61,12 @@ struct GemmCfg {
   // MMA of M = 256 tokens x N = 256 weight rows per K-step; each CTA stages its own
   // 128 token rows and half of the weight rows, and holds its tokens' accumulator.
   static constexpr bool CTA2 = !SWAP && BT == 256 && MODE != kShrink;
-  static constexpr int TROWS = CTA2 ? 128 : BT;       // token rows staged by this CTA
+  // The shrink of 256-row blocks takes a run's block in 128-row halves, one tile each:
+  // most runs sit in one half, and an M = 256 tile would spend half its MMAs and token
+  // loads on rows outside the run.  A half the run does not reach is a tile without
+  // K-steps that writes the half's S rows as zeros.
+  static constexpr bool HALF = MODE == kShrink && !SWAP && BT == 256;
+  static constexpr int TROWS = CTA2 || HALF ? 128 : BT;   // token rows staged by this CTA
   static constexpr int BK = gemm_bk(MODE, BT);        // K elements per stage
   static constexpr int ROWB = BK * 2;                 // bytes of one staged row = swizzle span
   static constexpr uint32_t SW = BK == 64 ? kSw128 : kSw64;
@@ -182,7 +187,7 @@ __device__ __forceinline__ float silu_f(float z) { return __fdividef(z, 1.0f + _
 template <int MODE, bool SWAP, int BT, bool BD>
 __device__ __forceinline__ int live_tiles(const GemmParams& prm) {
   if constexpr (BD) return *prm.plan_count;
-  else if constexpr (MODE == kShrink) return prm.totals[2] * prm.ksplit;
+  else if constexpr (MODE == kShrink) return prm.totals[2] * prm.ksplit * (GemmCfg<MODE, SWAP, BT>::HALF ? 2 : 1);
   else return prm.totals[1] * prm.n_ft * prm.ksplit;
 }
 
@@ -255,6 +260,20 @@ __device__ __forceinline__ TileHdr decode_tile(int tau, const GemmParams& prm, u
     }
     t.nruns = nseg;
     t.snch = nch;
+    return t;
+  } else if constexpr (C::HALF) {
+    // run tau / 2, half tau % 2 of its 256-row block (no K split on token-tiled blocks)
+    t.srun = tau >> 1;
+    t.ks = 0;
+    t.b = prm.runs[4 * t.srun + 0];
+    t.sa = prm.runs[4 * t.srun + 1];
+    const int beg = prm.runs[4 * t.srun + 2], end = prm.runs[4 * t.srun + 3];
+    t.snch = (prm.ranks[t.sa] + kRankChunk - 1) / kRankChunk;
+    t.kb0 = 0;
+    t.nk = nk_all;
+    t.e = prm.block_expert[t.b];
+    t.row0 = t.b * BT + 128 * (tau & 1);
+    t.n_it = beg < t.row0 + 128 && end > t.row0 ? nk_all : 0;   // 0: the half is zeros only
     return t;
   } else if constexpr (MODE == kShrink) {
     // the K splits of one run are consecutive tiles
@@ -772,7 +791,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const int beg = prm.runs[4 * t.srun + 2] - row0;
           const int end = prm.runs[4 * t.srun + 3] - row0;
           const int r_a = prm.ranks[t.sa];
-          uint16_t* srun = prm.s_out + static_cast<size_t>(t.srun) * BT * prm.r_pad;
+          // (a half tile of a 256-row block writes rows row0 - b*BT .. + 127 of the run's S tile)
+          uint16_t* srun = prm.s_out + (static_cast<size_t>(t.srun) * BT + (row0 - t.b * BT)) * prm.r_pad;
           // weight-streaming (M = 64 accumulator): rank row mr sits in lane mr % 16 of
           // TMEM lane quarter mr / 16
           const int mr = lane < 16 ? 16 * q + lane : (1 << 30);
@@ -1035,7 +1055,7 @@ cudaError_t launch_gemm_t(const GemmMaps& maps, const GemmParams& prm, int64_t m
   auto kern = moe_gemm_kernel<MODE, SWAP, BT, BD>;
   int64_t cap_tiles;
   if constexpr (C::BDIAG) cap_tiles = max_runs + max_blocks;   // groups <= chunks / 16 + blocks <= runs + blocks
-  else if constexpr (MODE == kShrink) cap_tiles = max_runs * prm.ksplit;
+  else if constexpr (MODE == kShrink) cap_tiles = max_runs * prm.ksplit * (C::HALF ? 2 : 1);
   else cap_tiles = max_blocks * prm.n_ft * prm.ksplit;
   if (cap_tiles <= 0) return cudaSuccess;
   cudaLaunchConfig_t cfg = {};

@@ -111,9 +111,13 @@ int validate_dims(const moe_lora_dims* d) {
 // block) and, for the weight-streaming kernels, the targets of the K-split rules,
 // which then weigh the tile counts against H, I and the SM count.  Rows were set from
 // GB300 sweeps over the workloads' shapes: 256-row blocks (CTA pairs, 2-SM MMA) win
-// once experts see thousands of tokens (3200 pairs per expert: 3.88 vs 4.13 ms); at
-// 1024 their padding, the 256-row shrink (one CTA per SM) and the extra adapter runs
-// per block cost more than the halved weight traffic per SM saves (1.91 vs 1.86 ms).
+// once experts see thousands of tokens (3200 pairs per expert: 3.88 vs 4.13 ms).
+// Between 768 and 2047 pairs per expert they win only where the adapter runs are long
+// (pairs per (expert, adapter-or-none bucket) T*k / (E*(L+1)) >= 20): a 256-row block of
+// short runs carries twice the LoRA expand chunks of a 128-row one.  Measured, 128 vs
+// 256 rows: the wide layer (32 adapters) at 768 / 1024 pairs per expert 1.445 / 1.791
+// vs 1.398 / 1.736 ms, at 512 1.075 vs 1.094 ms; the sweep layer (64 adapters) at 512 /
+// 1024 pairs per expert 1.34 / 2.05 vs 1.80 / 2.48 ms.
 struct TileClass {
   double ppe_above;       // the class holds shapes whose T*k/E exceeds this
   int block_m;            // token tile: < 128 weight-streaming, >= 128 token-tiled
@@ -133,12 +137,17 @@ constexpr TileClass kTileTable[] = {
 constexpr int kTableRows = sizeof(kTileTable) / sizeof(kTileTable[0]);
 
 // Row of the shape class of (T, k, E).
-int class_row(int64_t T, int32_t k, int32_t E) {
+constexpr double kLongRunsPpe = 768.0;     // from here 256-row blocks can win ...
+constexpr double kLongRunsPerBucket = 20.0; // ... when the runs are this long
+int class_row(int64_t T, int32_t k, int32_t E, int32_t L) {
   if (E <= 0 || k <= 0 || T <= 0) return 0;
   const double ppe = (double)T * k / E;
   int row = 0;
   for (int i = 0; i < kTableRows; ++i)
     if (ppe > kTileTable[i].ppe_above) row = i;
+  if (kTileTable[row].block_m == 128 && row + 1 < kTableRows && ppe >= kLongRunsPpe &&
+      ppe / ((L > 0 ? L : 0) + 1) >= kLongRunsPerBucket)
+    ++row;
   return row;
 }
 
@@ -154,7 +163,7 @@ int block_row(int block_m) {
 int resolve(const moe_lora_dims* in, moe_lora_dims* out) {
   if (!in) return fail(MOE_LORA_EINVAL, "dims is NULL");
   *out = *in;
-  if (out->block_m == 0) out->block_m = kTileTable[class_row(out->T, out->k, out->E)].block_m;
+  if (out->block_m == 0) out->block_m = kTileTable[class_row(out->T, out->k, out->E, out->L)].block_m;
   return MOE_LORA_OK;
 }
 #define MOE_RESOLVE(d)                           \
@@ -512,6 +521,8 @@ int do_forward(const moe_lora_dims* d, const uint16_t* x, const float* topk_w, c
   // token rows one CTA of a gate_up / down launch stages: 256-row blocks run on CTA
   // pairs, each CTA taking its 128 rows
   const uint32_t tok_rows = BT == 256 ? 128u : (uint32_t)BT;
+  // token rows a shrink tile stages: 256-row blocks are shrunk in 128-row halves
+  const uint32_t sh_rows = BT == 256 ? 128u : (uint32_t)BT;
   {
     const uint64_t dm[4] = {H, I, 2, E}, st[3] = {H * 2, I * H * 2, 2 * I * H * 2};
     const uint32_t bx[4] = {bk_gu, 128, 1, 1};
@@ -526,14 +537,14 @@ int do_forward(const moe_lora_dims* d, const uint16_t* x, const float* topk_w, c
     const uint64_t dm[2] = {H, rows}, st[1] = {H * 2};
     const uint32_t bx[2] = {bk_gu, tok_rows};
     MOE_TRY(encode(&m_gu.tok, xs, 2, dm, st, bx, swz(bk_gu), "x_sorted"));
-    const uint32_t bxs[2] = {bk_sh, (uint32_t)BT};
+    const uint32_t bxs[2] = {bk_sh, sh_rows};
     MOE_TRY(encode(&m_sgu.tok, xs, 2, dm, st, bxs, swz(bk_sh), "x_sorted"));
   }
   {
     const uint64_t dm[2] = {I, rows}, st[1] = {I * 2};
     const uint32_t bx[2] = {bk_dn, tok_rows};
     MOE_TRY(encode(&m_dn.tok, hs, 2, dm, st, bx, swz(bk_dn), "h_sorted"));
-    const uint32_t bxs[2] = {bk_sh, (uint32_t)BT};
+    const uint32_t bxs[2] = {bk_sh, sh_rows};
     MOE_TRY(encode(&m_sdn.tok, hs, 2, dm, st, bxs, swz(bk_sh), "h_sorted"));
   }
   if (d->L > 0) {
@@ -759,7 +770,7 @@ LayerLayout layer_layout(const moe_lora_dims* d) {
 
 extern "C" {
 
-int moe_lora_version(void) { return 302; }
+int moe_lora_version(void) { return 303; }
 
 int moe_lora_debug_set_acc_wait_ns(uint64_t ns) {
   g_acc_wait_ns.store(ns, std::memory_order_relaxed);
@@ -787,8 +798,8 @@ const char* moe_lora_status_string(int status) {
 
 const char* moe_lora_last_error(void) { return g_err; }
 
-int32_t moe_lora_pick_block_m(int64_t T, int32_t k, int32_t E) {
-  return kTileTable[class_row(T, k, E)].block_m;
+int32_t moe_lora_pick_block_m(int64_t T, int32_t k, int32_t E, int32_t L) {
+  return kTileTable[class_row(T, k, E, L)].block_m;
 }
 
 int moe_lora_plan_query(const moe_lora_dims* d, moe_lora_plan* out) {

@@ -23,33 +23,43 @@ def lib():
 
 
 # (name, block_m the table must pick)
-EXPECTED = [("tiny", 32), ("decode", 16), ("prefill", 256), ("wide", 128), ("dense_decode", 32),
+EXPECTED = [("tiny", 32), ("decode", 16), ("prefill", 256), ("wide", 256), ("dense_decode", 32),
             ("sweep_T1", 16), ("sweep_T16", 16), ("sweep_T256", 32), ("sweep_T4096", 128)]
 
 
 @pytest.mark.parametrize("name,bm", EXPECTED)
 def test_class_of_each_workload(name, bm):
     wl = W.get(name)
-    assert ml.pick_block_m(wl.T, wl.k, wl.E) == bm
+    assert ml.pick_block_m(wl.T, wl.k, wl.E, wl.L) == bm
     p = ml.plan(dims(wl, 0))
     assert p["block_m"] == bm
     assert p["weight_streaming"] == (bm < 128)
 
 
 def test_class_boundaries():
-    """Pairs per expert above 10, 24, 95 and 2047 move to the next row."""
-    E, k = 8, 1
+    """Pairs per expert above 10, 24, 95 and 2047 move to the next row (short adapter runs:
+    255 adapters, so fewer than 20 pairs per (expert, adapter) bucket below 2048)."""
+    E, k, L = 8, 1, 255
     for ppe, bm in [(1, 16), (10, 16), (11, 32), (24, 32), (25, 64), (95, 64), (96, 128), (2047, 128), (2048, 256),
                     (5000, 256)]:
-        assert ml.pick_block_m(ppe * E, k, E) == bm, (ppe, bm)
+        assert ml.pick_block_m(ppe * E, k, E, L) == bm, (ppe, bm)
     assert ml.pick_block_m(0, 1, 8) == 16
+
+
+def test_long_runs_take_256_row_blocks_from_768_pairs_per_expert():
+    """From 768 pairs per expert, 256-row blocks when the pairs per (expert, adapter-or-none
+    bucket) T*k / (E*(L+1)) reach 20: no adapters, or few adapters for many tokens."""
+    E, k = 8, 1
+    for ppe, L, bm in [(767, 0, 128), (768, 0, 256), (1500, 0, 256), (768, 37, 256), (768, 38, 128),
+                       (1024, 32, 256), (1024, 64, 128), (96, 0, 128)]:
+        assert ml.pick_block_m(ppe * E, k, E, L) == bm, (ppe, L, bm)
 
 
 @pytest.mark.parametrize("name", [n for n, _ in EXPECTED])
 def test_auto_block_m_resolves_everywhere(name):
     """block_m = 0 gives the same capacities, workspace sizes and plan as the explicit pick."""
     wl = W.get(name)
-    bm = ml.pick_block_m(wl.T, wl.k, wl.E)
+    bm = ml.pick_block_m(wl.T, wl.k, wl.E, wl.L)
     a, b = dims(wl, 0), dims(wl, bm)
     assert ml.align_capacity(a) == ml.align_capacity(b)
     assert ml.workspace_size(a) == ml.workspace_size(b)
