@@ -339,7 +339,11 @@ def roofline_of(m, ml):
 
 # The other configurations the layer is measured on, timed after the headline (decode)
 # in the default run; each gets its own clock record and CPU baseline.
-SECONDARY = ("prefill", "wide", "sweep_T1", "sweep_T16", "sweep_T256", "sweep_T4096", "dense_decode")
+# The sweep legs run last: right after their 7.9 GB of adapter banks were freed, the
+# dense_decode leg's plain steps measured 0.33-0.38 ms against 0.188 ms on its own or
+# earlier in the run, with unchanged per-kernel times (the host's launch loop fell
+# behind the GPU), in two runs.
+SECONDARY = ("prefill", "dense_decode", "wide", "sweep_T1", "sweep_T16", "sweep_T256", "sweep_T4096")
 
 
 def _weights_key(wl: W.Workload):
