@@ -427,6 +427,37 @@ def test_route_many_experts(ml, torch, oracle, E):
             assert_align_equal(align_to_numpy(bufs), oracle.align(ids_o, lora, E, wl.L, 16))
 
 
+@pytest.mark.parametrize("E", [64, 128, 200])
+def test_route_ties_and_signed_zero(ml, torch, oracle, E):
+    """Logits drawn from a handful of values -- exact ties, +0 and -0, -inf -- so every
+    selection round meets equal candidates in many lanes.  The router's warp reductions
+    must keep the oracle's choice (larger logit; equal ones to the lower expert index;
+    -0 equal to +0) bit for bit, through the fused one-CTA route+align (T = 20) and the
+    route kernel (T = 300)."""
+    vals = np.array([-np.inf, -1.0, -0.0, 0.0, 0.5, 1.0, 1.0], dtype=np.float32)
+    g = np.random.default_rng(11)
+    for T in (20, 300):
+        wl = W.custom(name=f"tie{E}x{T}", T=T, H=64, I=64, E=E, k=8, L=2, ranks=(16, 16), lora_mode="uniform")
+        logits = vals[g.integers(0, len(vals), size=(T, E))]
+        _, lora = W.make_routing(wl, 0)
+        d = dims_of(wl, 16, ml)
+        a_bytes, _ = ml.workspace_size(d)
+        ids_o, w_o = oracle.route(logits, wl.k)
+        lg, lr = to_dev(logits, torch), to_dev(lora, torch)
+        for fused in (False, True):
+            bufs = ml.alloc_align(d)
+            ws = torch.empty(max(a_bytes, 256), dtype=torch.uint8, device="cuda")
+            ids = torch.full((T, wl.k), -9, dtype=torch.int32, device="cuda")
+            tw = torch.full((T, wl.k), -9.0, dtype=torch.float32, device="cuda")
+            if fused:
+                ml.route_align(d, lg, lr, ids, tw, bufs, ws)
+            else:
+                ml.route(lg, wl.k, ids, tw)
+            torch.cuda.synchronize()
+            assert np.array_equal(ids.cpu().numpy(), ids_o), (E, T, fused)
+            assert np.allclose(tw.cpu().numpy(), w_o, rtol=0, atol=2e-6), (E, T, fused)
+
+
 def test_empty_batch(ml, torch):
     wl = W.get("tiny")
     _, _, _, w = inputs(wl)
