@@ -69,11 +69,11 @@ def test_auto_block_m_resolves_everywhere(name):
 
 def test_decode_plan():
     """Decode layer (64 pairs over 32 experts, H = I = 2880): 16-token weight-streaming
-    tiles; the down GEMM (12 feature tiles per block) splits K three ways to give each
-    of the 152 SMs about six tiles; gate_up (23 tiles per block) needs no split; the
+    tiles; the down GEMM (12 feature tiles per block) splits K two ways to give each
+    of the 152 SMs about three tiles; gate_up (23 tiles per block) needs no split; the
     2880-long shrinks stay whole (45 K-tiles < 64)."""
     p = ml.plan(dims(W.get("decode"), 0))
-    assert p["ksplit"] == {"shrink_gu": 1, "gate_up": 1, "shrink_dn": 1, "down": 3}
+    assert p["ksplit"] == {"shrink_gu": 1, "gate_up": 1, "shrink_dn": 1, "down": 2}
     assert p["k_tile"] == {"shrink_gu": 64, "gate_up": 64, "shrink_dn": 64, "down": 64}
     assert p["launches_route_align"] == 1
     assert p["launches_forward"] == 6      # gather, 2 shrinks, gate_up, down, combine
