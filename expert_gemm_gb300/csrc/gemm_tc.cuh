@@ -160,6 +160,8 @@ struct GemmBars {
   uint64_t sched_full[4];    // tile id published (producer)
   uint64_t sched_empty[4];   // tile id read (MMA thread + one arrive per epilogue warp)
   uint64_t sched_req;        // the producer is near the end of its tile: claim the next
+  uint64_t tau_full[4];      // CTA pairs: the even CTA has written the pair's next tile id here
+  int32_t tau_val[4];
   uint64_t drain;            // all MMAs of this CTA finished (teardown)
   uint32_t tmem_base;
   int32_t abort;
@@ -431,6 +433,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(&bars->sched_empty[j], 1 + 1 + 4);   // producer, MMA issuer, epilogue warps
     }
     mbar_init(&bars->sched_req, 1);
+    for (int j = 0; j < 4; ++j) mbar_init(&bars->tau_full[j], 1);
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
     fence_barrier_init();
@@ -707,21 +710,35 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   } else if (warp == kSchedWarp) {
     // ------------------------------------------------------------ tile scheduler
-    // n_live = no more work; a CTA pair walks a fixed stride of tiles (both CTAs
-    // must take the same ones)
+    // n_live = no more work.  Both CTAs of a pair must take the same tiles: the even
+    // CTA claims each from the counter and writes its id into the odd CTA's ring, whose
+    // scheduler waits for it.  (A fixed stride of tiles per pair let slow pairs fall
+    // behind the feature group whose weights the others kept in L2.)
     const int workers = C::CTA2 ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
     for (int i = 0;; ++i) {
       const int slot = i & 3;
       int tau = n_live;
       if (lane == 0) {
-        // tile i > 0 once the producer has asked for it; the slot once its last tile is done
-        bool ok = i == 0 || mbar_wait(&bars->sched_req, (i - 1) & 1);
+        // tile i > 0 once the producer has asked for it; the slot once its last tile is
+        // done (the odd CTA of a pair follows the even CTA's claims instead)
+        bool ok = i == 0 || (C::CTA2 && rank != 0) || mbar_wait(&bars->sched_req, (i - 1) & 1);
         ok = ok && mbar_wait(&bars->sched_empty[slot], ((i >> 2) & 1) ^ 1);
         if (!ok) {
           record_timeout(bars, prm.status);
           tau = -1;
+        } else if constexpr (C::CTA2) {
+          if (rank == 0) {
+            tau = aborted(bars) ? n_live : atomicAdd(prm.tile_ctr, 1);
+            st_shared_cluster_u32(mapa_shared(&bars->tau_val[slot], 1), static_cast<uint32_t>(tau));
+            mbar_arrive_cluster(mapa_shared(&bars->tau_full[slot], 1));   // release: the id is visible
+          } else if (mbar_wait_cluster(&bars->tau_full[slot], (i >> 2) & 1)) {
+            tau = *reinterpret_cast<volatile int32_t*>(&bars->tau_val[slot]);
+          } else {
+            record_timeout(bars, prm.status);
+            tau = -1;
+          }
         } else if (!aborted(bars)) {
-          tau = C::CTA2 ? static_cast<int>(blockIdx.x >> 1) + i * workers : atomicAdd(prm.tile_ctr, 1);
+          tau = atomicAdd(prm.tile_ctr, 1);
         }
       }
       tau = __shfl_sync(0xffffffffu, tau, 0);
