@@ -60,11 +60,12 @@ struct GemmParams {
   int32_t n_ft;                 // feature tiles per token block (kGateUp, kDown)
   int32_t ksplit;               // K splits; each split stores its own partial sums
   int32_t lora_after_pdl;       // previous kernel is the shrink: wait for it only before the LoRA K-steps
-  // kShrink on 128-row token blocks: the rank-chunk groups (block, first chunk) of the
-  // block-diagonal shrink tiles and their count, built by the gather launch
+  // kShrink on token-tiled blocks: the rank-chunk groups (128-row unit, first chunk) of
+  // the block-diagonal shrink tiles and their count, built by the gather launch
   const int32_t* plan_block;
   const int32_t* plan_c0;
   const int32_t* plan_count;
+  int32_t shrink_gch;           // rank chunks per group of those tiles
   int32_t ranks[MOE_LORA_MAX_ADAPTERS];
 };
 
@@ -111,11 +112,13 @@ inline bool gather_token_order(int64_t T, int H) { return T * static_cast<int64_
 // the sorted row of every placed pair in
 // pair_row [T*k], and zeroes *status and the n_ctr tile counters of the forward's
 // GEMM launches.
-// The group table of the block-diagonal shrink (128-row token blocks): the rank chunks
-// of each block's adapter runs, in run order, cut into groups of kShrinkGroupChunks;
-// group g is (plan_block[g], plan_c0[g] = its first chunk inside the block), groups in
-// block order, plan_count[0] groups in all.  block_chunks is [blocks] scratch.
-constexpr int kShrinkGroupChunks = 16;
+// The group table of the block-diagonal shrink of token-tiled blocks.  A unit is 128
+// rows: a 128-row block, or one half of a 256-row block.  The rank chunks of the
+// adapter runs that reach a unit, in run order, are cut into groups of `gch` chunks;
+// group g is (plan_block[g] = its unit b * (block_m / 128) + half, plan_c0[g] = its
+// first chunk inside the unit), groups in unit order, plan_count[0] groups in all.
+// block_chunks is [units] scratch.
+constexpr int kShrinkGroupChunks = 16;   // the most chunks of a group (N = 256)
 struct ShrinkPlanArgs {
   const int32_t* block_runs;   // [blocks+1]
   const int32_t* runs;         // [runs][4]
@@ -123,6 +126,8 @@ struct ShrinkPlanArgs {
   int32_t* plan_block;
   int32_t* plan_c0;
   int32_t* plan_count;
+  int32_t block_m;             // 128 or 256
+  int32_t gch;                 // rank chunks per group, 1 .. kShrinkGroupChunks
   int32_t ranks[MOE_LORA_MAX_ADAPTERS];
 };
 // plan: when non-null, one extra CTA of the launch builds the group table (it reads

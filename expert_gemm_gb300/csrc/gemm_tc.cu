@@ -7,8 +7,10 @@ cudaError_t launch_gemm(int mode, int bt, const GemmMaps& maps, const GemmParams
                         int64_t max_runs, bool pdl, cudaStream_t s, bool block_diag) {
   // the block-diagonal shrink of 128-row blocks: its own kernel, fed by the group table
   if (block_diag) {
-    if (mode != kShrink || bt != 128) return cudaErrorInvalidValue;
-    return launch_gemm_t<kShrink, false, 128, true>(maps, prm, max_blocks, max_runs, pdl, s);
+    if (mode != kShrink) return cudaErrorInvalidValue;
+    if (bt == 128) return launch_gemm_t<kShrink, false, 128, true>(maps, prm, max_blocks, max_runs, pdl, s);
+    if (bt == 256) return launch_gemm_t<kShrink, false, 256, true>(maps, prm, max_blocks, max_runs, pdl, s);
+    return cudaErrorInvalidValue;
   }
 #define MOE_GEMM_CASE(BT_, SWAP_)                                                                       \
   if (bt == BT_) {                                                                                      \

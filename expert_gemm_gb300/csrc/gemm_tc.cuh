@@ -56,7 +56,8 @@ struct GemmCfg {
   // stage brings up to 32 KB of A rows (the HBM stream) per 16 KB of token rows.  Its
   // tiles come from the group table the gather launch builds.
   static constexpr bool BDIAG = BD;
-  static_assert(!BD || (MODE == kShrink && !SWAP && BT == 128), "block-diagonal tiles: the 128-row shrink");
+  static_assert(!BD || (MODE == kShrink && !SWAP && (BT == 128 || BT == 256)),
+                "block-diagonal tiles: the shrink of token-tiled blocks");
   // 256-token blocks of gate_up / down run on a CTA pair (a cluster of 2): one 2-SM
   // MMA of M = 256 tokens x N = 256 weight rows per K-step; each CTA stages its own
   // 128 token rows and half of the weight rows, and holds its tokens' accumulator.
@@ -137,7 +138,8 @@ struct ShrinkSeg {
   uint8_t cl;         // first chunk of the run in this tile
   uint8_t n;          // chunks of the run in this tile
   uint8_t pos;        // tile-local chunk of chunk cl (its A rows and accumulator columns)
-  uint8_t pad;
+  uint8_t other;      // 256-row blocks: the run has no rows in the other half, whose S rows
+                      //   of these chunks this tile writes as zeros
 };
 static_assert(sizeof(ShrinkSeg) == 16, "segment layout");
 static_assert(kShrinkGroupChunks * sizeof(ShrinkSeg) <= kMaxBlockRuns, "segments fit the run-chunk array");
@@ -207,15 +209,21 @@ __device__ __forceinline__ TileHdr decode_tile(int tau, const GemmParams& prm, u
   t.f0 = 0;
   t.srun = t.sa = t.snch = 0;
   if constexpr (C::BDIAG) {
-    // group tau: chunks [c0, c0 + 16) of block b's runs, in run order.  The lanes take
-    // 32 runs at a time: each its chunk count, a warp scan places its chunks in the
-    // block, and the runs overlapping the group become the tile's segments.
-    const int b = prm.plan_block[tau];
+    // group tau: chunks [c0, c0 + gch) of the runs that reach one 128-row unit (a block,
+    // or a half of a 256-row block), in run order.  The lanes take 32 runs at a time:
+    // each its chunk count if it reaches the unit, a warp scan places its chunks, and
+    // the runs overlapping the group become the tile's segments.
+    constexpr int UPB = BT / 128;
+    const int u = prm.plan_block[tau];
     const int c0 = prm.plan_c0[tau];
+    const int gch = prm.shrink_gch;
+    const int b = u / UPB, half = u - b * UPB;
     const int rb = prm.block_runs[b], re = prm.block_runs[b + 1];
     t.b = b;
     t.e = prm.block_expert[b];
-    t.row0 = b * BT;
+    t.row0 = b * BT + 128 * half;
+    // the other half's rows, relative to this unit's first row
+    const int oth_lo = half == 0 ? 128 : -128, oth_hi = oth_lo + 128;
     t.ks = 0;
     t.kb0 = 0;
     t.nk = nk_all;
@@ -223,14 +231,14 @@ __device__ __forceinline__ TileHdr decode_tile(int tau, const GemmParams& prm, u
     t.run0 = rb;
     ShrinkSeg* seg = tile_segs(nch_out);
     int carry = 0, nseg = 0, nch = 0;
-    for (int r0 = rb; r0 < re && carry < c0 + kShrinkGroupChunks; r0 += 32) {
+    for (int r0 = rb; r0 < re && carry < c0 + gch; r0 += 32) {
       const int j = r0 + lane;
       int a = 0, n = 0, beg = 0, end = 0;
       if (j < re) {
         a = prm.runs[4 * j + 1];
         beg = prm.runs[4 * j + 2] - t.row0;
         end = prm.runs[4 * j + 3] - t.row0;
-        n = (prm.ranks[a] + kRankChunk - 1) / kRankChunk;
+        if (beg < 128 && end > 0) n = (prm.ranks[a] + kRankChunk - 1) / kRankChunk;   // reaches the unit
       }
       int incl = n;
 #pragma unroll
@@ -240,7 +248,7 @@ __device__ __forceinline__ TileHdr decode_tile(int tau, const GemmParams& prm, u
       }
       const int cs = carry + incl - n;   // the block-local chunk where run j starts
       const int lo = cs > c0 ? cs : c0;
-      const int hi = cs + n < c0 + kShrinkGroupChunks ? cs + n : c0 + kShrinkGroupChunks;
+      const int hi = cs + n < c0 + gch ? cs + n : c0 + gch;
       const bool take = j < re && lo < hi;
       const uint32_t m = __ballot_sync(0xffffffffu, take);
       if (take) {
@@ -253,7 +261,7 @@ __device__ __forceinline__ TileHdr decode_tile(int tau, const GemmParams& prm, u
         sg.cl = static_cast<uint8_t>(lo - cs);
         sg.n = static_cast<uint8_t>(hi - lo);
         sg.pos = static_cast<uint8_t>(lo - c0);
-        sg.pad = 0;
+        sg.other = UPB == 2 && !(beg < oth_hi && end > oth_lo);
         seg[nseg + __popc(m & ((1u << lane) - 1u))] = sg;
       }
       nseg += __popc(m);
@@ -782,11 +790,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         uint32_t v[16], u[16];
         if constexpr (C::BDIAG) {
           // each segment's chunks: the run's rank columns of row m, zero outside the run
+          // (256-row blocks: this half's rows of the run's S tile, and the other half's
+          // as zeros when the run has none there)
           const ShrinkSeg* seg = tile_segs(tp->nch);
+          const int hoff = row0 - t.b * BT;
           for (int sgi = 0; sgi < t.nruns; ++sgi) {
             const ShrinkSeg sg = seg[sgi];
             const bool in_run = m >= sg.beg && m < sg.end;
-            uint16_t* srow = prm.s_out + (static_cast<size_t>(sg.run) * BT + m) * prm.r_pad;
+            uint16_t* srow = prm.s_out + (static_cast<size_t>(sg.run) * BT + hoff + m) * prm.r_pad;
+            uint16_t* sother = prm.s_out + (static_cast<size_t>(sg.run) * BT + (BT - 128 - hoff) + m) * prm.r_pad;
             for (int c = 0; c < sg.n; ++c) {
               tmem_ld16(tq + (sg.pos + c) * kRankChunk, v);
               tmem_ld_wait();
@@ -802,6 +814,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               uint4* dst = reinterpret_cast<uint4*>(srow + col0);
               dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
               dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+              if (sg.other) {
+                uint4* zd = reinterpret_cast<uint4*>(sother + col0);
+                zd[0] = make_uint4(0, 0, 0, 0);
+                zd[1] = make_uint4(0, 0, 0, 0);
+              }
             }
           }
         } else if constexpr (MODE == kShrink) {
@@ -1071,7 +1088,8 @@ cudaError_t launch_gemm_t(const GemmMaps& maps, const GemmParams& prm, int64_t m
   using C = GemmCfg<MODE, SWAP, BT, BD>;
   auto kern = moe_gemm_kernel<MODE, SWAP, BT, BD>;
   int64_t cap_tiles;
-  if constexpr (C::BDIAG) cap_tiles = max_runs + max_blocks;   // groups <= chunks / 16 + blocks <= runs + blocks
+  // groups <= unit chunks / gch + units <= (BT / 128) * (runs + blocks) for gch >= 4
+  if constexpr (C::BDIAG) cap_tiles = (BT / 128) * (max_runs + max_blocks);
   else if constexpr (MODE == kShrink) cap_tiles = max_runs * prm.ksplit * (C::HALF ? 2 : 1);
   else cap_tiles = max_blocks * prm.n_ft * prm.ksplit;
   if (cap_tiles <= 0) return cudaSuccess;

@@ -243,21 +243,29 @@ bool shrink_on_cores(const moe_lora_dims* d, const Caps& cap) {
 }
 int shrink_slices(int K) { return (K + moe::kShrinkSlice - 1) / moe::kShrinkSlice; }
 int shrink_ksplit(const moe_lora_dims* d, const Caps& cap, int K);
-// The tcgen05 shrink of 128-row token blocks can run block-diagonal tiles (several
+// The tcgen05 shrink of token-tiled blocks can run block-diagonal tiles (several
 // adapter runs side by side in N, from a group table the gather launch builds): each
-// stage then brings up to 32 KB of A rows instead of one run's 2-8 KB.  A block gives
-// one to a few such tiles against one per run, so they pay once the blocks alone fill
-// the SMs twice over (sweep T = 4096: 319 blocks, shrinks 227/96 -> 193/80 us); with
-// fewer blocks (wide: 64) the long K loops of too few tiles leave SMs idle
-// (shrinks 41/77 -> 68/161 us) and the per-run tiles stay.
+// stage then brings up to 32 KB of A rows instead of one run's 2-8 KB.  On 128-row
+// blocks a block gives one to a few such tiles against one per run, so they pay once
+// the blocks alone fill the SMs twice over (sweep T = 4096: 319 blocks, shrinks 227/96
+// -> 193/80 us); with fewer blocks (wide at 128 rows: 64) the long K loops of too few
+// tiles leave SMs idle (shrinks 41/77 -> 68/161 us) and the per-run tiles stay.  On the
+// 128-row halves of 256-row blocks, whose runs are long, they lose (wide: 42/79 -> 51/113
+// us with 8-chunk groups, 65/145 with 4; prefill 122/114 -> 138/132 us): there the
+// per-run half tiles stay, and the block-diagonal form runs only when the test hook
+// asks for it.
 std::atomic<int> g_shrink_tiles{0};   // test hook: 0 by shape, 1 block-diagonal, 2 per run
-bool block_diag_space(const moe_lora_dims* d) { return d->L > 0 && d->block_m == 128; }
+bool block_diag_space(const moe_lora_dims* d) { return d->L > 0 && (d->block_m == 128 || d->block_m == 256); }
 bool block_diag_shrink(const moe_lora_dims* d, const Caps& cap) {
   if (!block_diag_space(d)) return false;
   const int mode = g_shrink_tiles.load(std::memory_order_relaxed);
   if (mode != 0) return mode == 1;
+  if (d->block_m == 256) return false;
   return cap.blocks >= 2 * kPlanSMs;
 }
+// Rank chunks per block-diagonal group: 16 (N = 256) on 128-row blocks; 8 on the halves
+// of 256-row blocks, whose blocks are fewer (at least 4: the group table's capacity).
+int shrink_group_chunks(const moe_lora_dims* d) { return d->block_m == 256 ? 8 : 16; }
 int gate_up_ksplit(const moe_lora_dims* d, const Caps& cap);
 int down_ksplit(const moe_lora_dims* d, const Caps& cap);
 FwdLayout fwd_layout(const moe_lora_dims* d) {
@@ -285,7 +293,10 @@ FwdLayout fwd_layout(const moe_lora_dims* d) {
   // group table of the block-diagonal shrink (128-row blocks): [groups] block, [groups]
   // first chunk, [blocks] chunk counts, the group count; groups <= runs + blocks
   l.plan = off;
-  if (block_diag_space(d)) off += up256((size_t)(2 * (c.runs + c.blocks) + c.blocks + 1) * 4);
+  if (block_diag_space(d)) {
+    const size_t upb = (size_t)d->block_m / 128;   // 128-row units per block
+    off += up256((2 * upb * (size_t)(c.runs + c.blocks) + upb * (size_t)c.blocks + 1) * 4);
+  }
   l.n_ctr = kNumGemmCounters + 2 * 4 * (int)c.runs;
   l.bytes = off;
   return l;
@@ -631,17 +642,21 @@ int do_forward(const moe_lora_dims* d, const uint16_t* x, const float* topk_w, c
   moe::ShrinkPlanArgs plan{};
   if (bdiag) {
     int32_t* pb = reinterpret_cast<int32_t*>(base + l.plan);
-    const int64_t G = cap.runs + cap.blocks;
+    const int64_t upb = BT / 128;
+    const int64_t G = upb * (cap.runs + cap.blocks);
     plan.block_runs = al->block_runs;
     plan.runs = al->runs;
     plan.plan_block = pb;
     plan.plan_c0 = pb + G;
     plan.block_chunks = pb + 2 * G;
-    plan.plan_count = pb + 2 * G + cap.blocks;
+    plan.plan_count = pb + 2 * G + upb * cap.blocks;
+    plan.block_m = BT;
+    plan.gch = shrink_group_chunks(d);
     for (int a = 0; a < d->L; ++a) plan.ranks[a] = d->ranks[a];
     p.plan_block = plan.plan_block;
     p.plan_c0 = plan.plan_c0;
     p.plan_count = plan.plan_count;
+    p.shrink_gch = plan.gch;
   }
 
   auto mark = [&](int i) -> cudaError_t {

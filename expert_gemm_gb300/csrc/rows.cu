@@ -15,35 +15,45 @@ namespace {
 // output nothing reads) and the shrinks select S = 0 outside each adapter run.  The
 // same launch zeroes the call's device status word and the GEMMs' tile counters, so the
 // forward needs no memset nodes.
-// The group table of the block-diagonal shrink, built by one CTA: each block's rank
-// chunks (sum over its runs of ceil(rank / 16)), then a block-order scan of
-// ceil(chunks / 16) groups per block and one table entry per group.
+// The group table of the block-diagonal shrink, built by one CTA: each 128-row unit's
+// rank chunks (sum over the runs that reach it of ceil(rank / 16)), then a unit-order
+// scan of ceil(chunks / gch) groups per unit and one table entry per group.
 __device__ void build_shrink_plan(const ShrinkPlanArgs& pl, const int32_t* __restrict__ totals) {
   __shared__ int32_t s_warp[32];
   __shared__ int32_t s_carry;
   const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5, nw = nt >> 5;
-  const int nb = totals[1], nr = totals[2];
+  const int upb = pl.block_m / 128;   // units per block
+  const int nb = totals[1] * upb, nr = totals[2];
   for (int b = tid; b < nb; b += nt) pl.block_chunks[b] = 0;
   __syncthreads();
   // eight runs' loads in flight per thread before their atomics
   constexpr int kBatch = 8;
   for (int j0 = tid; j0 < nr; j0 += kBatch * nt) {
-    int bb[kBatch], aa[kBatch];
+    int rb[kBatch], ra[kBatch], rs[kBatch], re[kBatch];   // block, adapter, first row, end row
 #pragma unroll
     for (int q = 0; q < kBatch; ++q) {
       const int j = j0 + q * nt;
-      bb[q] = j < nr ? pl.runs[4 * j] : -1;
-      aa[q] = j < nr ? pl.runs[4 * j + 1] : 0;
+      const bool in = j < nr;
+      rb[q] = in ? pl.runs[4 * j] : -1;
+      ra[q] = in ? pl.runs[4 * j + 1] : 0;
+      rs[q] = in ? pl.runs[4 * j + 2] : 0;
+      re[q] = in ? pl.runs[4 * j + 3] : 0;
     }
 #pragma unroll
-    for (int q = 0; q < kBatch; ++q)
-      if (bb[q] >= 0) atomicAdd(pl.block_chunks + bb[q], (pl.ranks[aa[q]] + kRankChunk - 1) / kRankChunk);
+    for (int q = 0; q < kBatch; ++q) {
+      if (rb[q] < 0) continue;
+      const int n = (pl.ranks[ra[q]] + kRankChunk - 1) / kRankChunk;
+      for (int h = 0; h < upb; ++h) {   // the units the run's rows reach
+        const int u0 = rb[q] * pl.block_m + 128 * h;
+        if (rs[q] < u0 + 128 && re[q] > u0) atomicAdd(pl.block_chunks + rb[q] * upb + h, n);
+      }
+    }
   }
   if (tid == 0) s_carry = 0;
   __syncthreads();   // the block's atomics are complete and visible to the block
   for (int base = 0; base < nb; base += nt) {
     const int b = base + tid;
-    const int g = b < nb ? (__ldcg(pl.block_chunks + b) + kShrinkGroupChunks - 1) / kShrinkGroupChunks : 0;
+    const int g = b < nb ? (__ldcg(pl.block_chunks + b) + pl.gch - 1) / pl.gch : 0;
     int x = g;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -65,7 +75,7 @@ __device__ void build_shrink_plan(const ShrinkPlanArgs& pl, const int32_t* __res
     const int first = s_carry + (warp > 0 ? s_warp[warp - 1] : 0) + x - g;
     for (int i = 0; i < g; ++i) {
       pl.plan_block[first + i] = b;
-      pl.plan_c0[first + i] = i * kShrinkGroupChunks;
+      pl.plan_c0[first + i] = i * pl.gch;
     }
     __syncthreads();   // every thread has read s_carry and s_warp
     if (tid == 0) s_carry += s_warp[nw - 1];

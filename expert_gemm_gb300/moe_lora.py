@@ -155,7 +155,7 @@ def debug_set_acc_wait_ns(ns: int):
 
 
 def debug_set_shrink_tiles(mode: int):
-    """Test hook: tile form of the tcgen05 shrinks of 128-row blocks in later forward
+    """Test hook: tile form of the tcgen05 shrinks of token-tiled blocks in later forward
     calls (0 by shape, 1 block-diagonal, 2 one run per tile).  See moe_lora.h."""
     _check(load().moe_lora_debug_set_shrink_tiles(int(mode)))
 

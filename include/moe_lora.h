@@ -150,8 +150,9 @@ typedef struct moe_lora_plan {
     int32_t shrink_on_cores;      /* 1: the LoRA shrinks run on CUDA cores, split over K in
                                      ksplit[0]/ksplit[2] slices of k_tile elements (short
                                      adapter runs); 0: tcgen05 tiles                        */
-    int32_t shrink_block_diag;    /* 1: the tcgen05 shrinks of 128-row blocks take groups of
-                                     up to 16 rank chunks of a block's adapter runs per tile
+    int32_t shrink_block_diag;    /* 1: the tcgen05 shrinks of token-tiled blocks take groups
+                                     of rank chunks of the adapter runs that reach a 128-row
+                                     unit (a block, or a half of a 256-row block) per tile
                                      (N = their ranks side by side); 0: one run per tile    */
 } moe_lora_plan;
 
@@ -325,10 +326,11 @@ int moe_lora_align_static(const moe_lora_dims *d, const int32_t *topk_ids, const
 int moe_lora_debug_set_acc_wait_ns(uint64_t ns);
 
 /*
- * Test hook: the tile form of the tcgen05 shrinks of 128-row blocks in later
- * moe_lora_forward calls of this process.  0 (default): by shape -- block-diagonal
- * tiles (several adapter runs per tile) once the blocks alone fill the SMs twice, else
- * one run per tile; 1: always block-diagonal; 2: always one run per tile.  Both forms
+ * Test hook: the tile form of the tcgen05 shrinks of token-tiled blocks (block_m 128
+ * or 256) in later moe_lora_forward calls of this process.  0 (default): by shape --
+ * on 128-row blocks block-diagonal tiles (several adapter runs per tile) once the
+ * blocks alone fill the SMs twice, else one run per tile; on 256-row blocks one run per
+ * 128-row half; 1: always block-diagonal; 2: always one run per tile.  Both forms
  * compute the same S tiles (the same fp32 sums of the same products, rounded once to
  * bf16), so the layer's output does not depend on the choice.  The forward workspace
  * size does not depend on it either.  Returns MOE_LORA_EINVAL for another mode.

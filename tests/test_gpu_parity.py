@@ -194,23 +194,27 @@ SHRINK_FORM_CASES = [
 ]
 
 
+@pytest.mark.parametrize("block_m", [128, 256])
 @pytest.mark.parametrize("form", [1, 2])
 @pytest.mark.parametrize("case", SHRINK_FORM_CASES, ids=lambda c: c["name"])
-def test_shrink_tile_forms(ml, torch, oracle, case, form):
-    """The tcgen05 shrink of 128-row blocks as block-diagonal groups (form 1: up to 16
-    rank chunks of a block's runs per tile) and one run per tile (form 2), against the
-    oracle; align bit for bit.  The shape picks a form by itself (block count against the
-    SMs); the test hook forces each."""
+def test_shrink_tile_forms(ml, torch, oracle, case, form, block_m):
+    """The tcgen05 shrink of token-tiled blocks as block-diagonal groups (form 1: rank
+    chunks of the runs that reach a 128-row unit, several runs per tile; on 256-row
+    blocks a unit is a half, and a run with no rows in the other half writes that half's
+    S rows as zeros) and one run per tile (form 2: on 256-row blocks one tile per
+    half), against the oracle; align bit for bit.  The shape picks a form by itself; the
+    test hook forces each."""
     wl = W.custom(**case)
     ml.debug_set_shrink_tiles(form)
     try:
-        assert ml.plan(dims_of(wl, 128, ml))["shrink_block_diag"] == (form == 1)
-        run_case(ml, torch, oracle, wl, block_m=128)
+        assert ml.plan(dims_of(wl, block_m, ml))["shrink_block_diag"] == (form == 1)
+        run_case(ml, torch, oracle, wl, block_m=block_m)
     finally:
         ml.debug_set_shrink_tiles(0)
 
 
-def test_shrink_tile_forms_same_bytes(ml, torch):
+@pytest.mark.parametrize("block_m", [128, 256])
+def test_shrink_tile_forms_same_bytes(ml, torch, block_m):
     """Both shrink forms form each S element from the same products summed in the same K
     order in fp32, rounded once: the layer outputs are identical bit for bit."""
     wl = W.custom(**SHRINK_FORM_CASES[1])
@@ -219,7 +223,7 @@ def test_shrink_tile_forms_same_bytes(ml, torch):
     for form in (1, 2):
         ml.debug_set_shrink_tiles(form)
         try:
-            layer = ml.Layer(dims_of(wl, 128, ml), dev_weights(w, torch))
+            layer = ml.Layer(dims_of(wl, block_m, ml), dev_weights(w, torch))
             outs.append(layer.step(to_dev(logits, torch), to_dev(lora, torch), to_dev(x, torch)).clone())
             torch.cuda.synchronize()
             assert int(layer.status.item()) == 0
@@ -233,6 +237,7 @@ def test_shrink_tile_form_hook_rejects_unknown_modes(ml):
         ml.debug_set_shrink_tiles(3)
     assert ml.plan(dims_of(W.get("sweep_T4096"), 128, ml))["shrink_block_diag"]
     assert not ml.plan(dims_of(W.get("wide"), 128, ml))["shrink_block_diag"]
+    assert not ml.plan(dims_of(W.get("sweep_T16"), 16, ml))["shrink_block_diag"]   # weight-streaming
 
 
 @pytest.mark.parametrize("T,k", [(512, 8), (4097, 1)])
