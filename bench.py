@@ -311,8 +311,15 @@ def _graph_ms(torch, layer, lg, lr, xd, flush, K):
 
 
 def roofline_of(m, ml):
-    """Dominant-kernel roofline (gate_up) and the whole-layer roofline of one measurement."""
-    hbm, tc, tc_sus, src = peaks()
+    """Dominant-kernel roofline (gate_up) and the whole-layer roofline of one measurement.
+
+    Tensor-bound fractions are of the sustained bf16 rate (cuBLAS back to back for
+    seconds, under the power cap): every leg times its kernels inside a fraction of a
+    second or more of back-to-back steps, and the compute-bound legs run at the power
+    cap.  The fraction of the burst rate is reported beside it (`frac_of_burst`)."""
+    hbm, tc_burst, tc_sus, src = peaks()
+    tc = tc_sus or tc_burst
+    tc_name = "cuBLAS bf16 sustained" if tc_sus else "cuBLAS bf16 burst"
     acct, wl = m["acct"], m["wl"]
     gu_ms = float(np.mean(m["stage_ms"][:, ml.STAGES.index("gate_up")]))
     intensity = acct["gate_up_flops"] / max(acct["gate_up_bytes"], 1)
@@ -325,7 +332,7 @@ def roofline_of(m, ml):
     else:
         ach = acct["gate_up_flops"] / (gu_ms * 1e-3) / 1e12
         roof = {"bound": "tensor", "kernel": kname, "achieved": ach, "peak": tc, "unit": "TFLOP/s",
-                "frac": ach / tc, "peak_source": f"{src} (cuBLAS bf16 burst)",
+                "frac": ach / tc, "peak_source": f"{src} ({tc_name})", "frac_of_burst": ach / tc_burst,
                 "algorithmic_flops_per_launch": acct["gate_up_flops"]}
     roof["launch_ms"] = gu_ms
     roof["traffic"] = committed_traffic(wl.name, "gate_up")
@@ -333,7 +340,9 @@ def roofline_of(m, ml):
     t_bw, t_tc = acct["bytes"] / (hbm * 1e9), acct["flops"] / (tc * 1e12)
     layer = {"alg_bytes": acct["bytes"], "alg_flops": acct["flops"], "t_roof_ms": max(t_bw, t_tc) * 1e3,
              "bound": "hbm" if t_bw >= t_tc else "tensor", "frac": max(t_bw, t_tc) / layer_s,
-             "hbm_gbs_peak": hbm, "bf16_tflops_peak": tc}
+             "hbm_gbs_peak": hbm, "bf16_tflops_peak": tc, "bf16_tflops_peak_source": tc_name}
+    if t_tc > t_bw:
+        layer["frac_of_burst"] = acct["flops"] / (tc_burst * 1e12) / layer_s
     return roof, layer
 
 
