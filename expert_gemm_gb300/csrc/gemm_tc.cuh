@@ -20,7 +20,10 @@
 // Two tile orientations (template SWAP):
 //   SWAP = false (token blocks of 128 or 256 rows): MMA M = 128 tokens per accumulator
 //          (MT = BT/128 accumulators), N = 256 weight rows (gate_up: 128 gate + 128 up
-//          rows of the same features; down: 256 features).
+//          rows of the same features; down: 256 features); 256-row gate_up / down tiles
+//          run on CTA pairs (M = 256), the shrink of 256-row blocks takes one 128-row
+//          half per tile.  The shrink's N is the rank rows of one adapter run, or (BD)
+//          of a group of runs side by side.
 //   SWAP = true  (token blocks of 16/32/64 rows, few tokens per expert): MMA M = 128
 //          weight rows, N = BT tokens; two accumulators (gate/up, or two feature halves).
 //          Weights stream through the tensor core at full tile height however few
@@ -38,7 +41,9 @@
 //             through a small shared ring to the other roles.  It claims tile i + 1
 //             when the producer is a few stages from the end of tile i, so the
 //             decode's chain of dependent loads is off the producer's path while the
-//             claim stays late enough for the dynamic balance across CTAs.
+//             claim stays late enough for the dynamic balance across CTAs.  In a CTA
+//             pair the even CTA's scheduler claims and hands each id to the odd CTA's
+//             through shared::cluster, so both take the same tiles.
 #pragma once
 
 #include <cuda_bf16.h>
