@@ -191,6 +191,8 @@ SHRINK_FORM_CASES = [
     dict(name="rk48", T=160, H=448, I=320, E=4, k=2, L=4, ranks=(40, 24, 48, 8), lora_mode="uniform_with_none"),
     dict(name="manyruns", T=300, H=320, I=192, E=2, k=1, L=48, ranks=tuple(16 if a % 3 else 48 for a in range(48)),
          lora_mode="uniform_with_none"),
+    # ~95 distinct rank-64 adapters per 128-row block: ~380 rank chunks, ~24 groups of a block
+    dict(name="allruns", T=600, H=192, I=128, E=2, k=1, L=200, ranks=(64,) * 200, lora_mode="uniform"),
 ]
 
 
