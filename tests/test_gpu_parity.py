@@ -303,11 +303,15 @@ def test_invalid_ids_dropped(ml, torch, oracle):
     assert elem <= TOL, (wl.name, elem, norm)
 
 
-@pytest.mark.parametrize("case", ["decode_bm16", "gusplit_bm16", "mid_bm128", "mid_bm256"])
+@pytest.mark.parametrize("case", ["decode_bm16", "gusplit_bm16", "mid_bm128", "mid_bm256", "mid_bm128_bd",
+                                  "mid_bm256_bd"])
 def test_deterministic_bytes(ml, torch, case):
-    """No atomics on the path: repeated calls give identical output bytes, also after
-    another batch has run through the same buffers (K-split partial buffers and the
-    bf16 row path both covered)."""
+    """No floating-point atomics on the path: repeated calls give identical output bytes,
+    also after another batch has run through the same buffers (K-split partial buffers,
+    the bf16 row path, CTA pairs claiming tiles dynamically, and the block-diagonal
+    shrink whose group table is counted with integer atomics, all covered)."""
+    bd = case.endswith("_bd")
+    case = case[:-3] if bd else case
     shapes = {
         "decode": W.get("decode"),
         "gusplit": W.custom(name="gusplit", T=8, H=1024, I=512, E=2, k=1, L=2, ranks=(16, 32),
@@ -318,16 +322,20 @@ def test_deterministic_bytes(ml, torch, case):
     name, bm = case.split("_bm")
     wl = shapes[name]
     logits, lora, x, w = inputs(wl)
-    layer = ml.Layer(dims_of(wl, int(bm), ml), dev_weights(w, torch))
-    lg, lr, xd = to_dev(logits, torch), to_dev(lora, torch), to_dev(x, torch)
-    first = layer.step(lg, lr, xd).clone()
-    g = np.random.default_rng(9)
-    layer.step(to_dev(g.standard_normal(logits.shape).astype(np.float32), torch), lr,
-               to_dev(W.f32_to_bf16_bits(g.standard_normal(x.shape).astype(np.float32)), torch))
-    for _ in range(3):
-        again = layer.step(lg, lr, xd)
-        torch.cuda.synchronize()
-        assert torch.equal(first.view(torch.int16), again.view(torch.int16))
+    ml.debug_set_shrink_tiles(1 if bd else 0)
+    try:
+        layer = ml.Layer(dims_of(wl, int(bm), ml), dev_weights(w, torch))
+        lg, lr, xd = to_dev(logits, torch), to_dev(lora, torch), to_dev(x, torch)
+        first = layer.step(lg, lr, xd).clone()
+        g = np.random.default_rng(9)
+        layer.step(to_dev(g.standard_normal(logits.shape).astype(np.float32), torch), lr,
+                   to_dev(W.f32_to_bf16_bits(g.standard_normal(x.shape).astype(np.float32)), torch))
+        for _ in range(3):
+            again = layer.step(lg, lr, xd)
+            torch.cuda.synchronize()
+            assert torch.equal(first.view(torch.int16), again.view(torch.int16))
+    finally:
+        ml.debug_set_shrink_tiles(0)
     assert int(layer.status.item()) == 0
 
 
