@@ -164,10 +164,11 @@ cudaError_t launch_shrink_rows(const ShrinkRowsLaunch& a, int64_t max_runs, bool
 // pdl: launch with programmatic stream serialisation (may overlap the previous kernel).
 // block_diag (kShrink, bt 128 only): the block-diagonal shrink, whose tiles are the
 // group table's entries (prm.plan_*, built by the gather launch of the same forward).
+// deep (kGateUp / kDown, bt 16 only): the variant with a 6-deep ring, one CTA per SM.
 cudaError_t launch_gemm(int mode, int bt, const GemmMaps& maps, const GemmParams& prm, int64_t max_blocks,
-                        int64_t max_runs, bool pdl, cudaStream_t s, bool block_diag = false);
+                        int64_t max_runs, bool pdl, cudaStream_t s, bool block_diag = false, bool deep = false);
 // K elements per pipeline stage and stage count of the compiled GEMM for (mode, bt);
 // false if no kernel is compiled for it.  Host only, no device calls.
-bool gemm_stage_shape(int mode, int bt, int* k_tile, int* stages);
+bool gemm_stage_shape(int mode, int bt, int* k_tile, int* stages, bool deep = false);
 
 }  // namespace moe

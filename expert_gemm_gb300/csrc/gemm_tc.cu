@@ -4,7 +4,14 @@
 namespace moe {
 
 cudaError_t launch_gemm(int mode, int bt, const GemmMaps& maps, const GemmParams& prm, int64_t max_blocks,
-                        int64_t max_runs, bool pdl, cudaStream_t s, bool block_diag) {
+                        int64_t max_runs, bool pdl, cudaStream_t s, bool block_diag, bool deep) {
+  // the 16-token weight-streaming gate_up / down with a deeper ring
+  if (deep) {
+    if (bt != 16) return cudaErrorInvalidValue;
+    if (mode == kGateUp) return launch_gemm_t<kGateUp, true, 16, false, true>(maps, prm, max_blocks, max_runs, pdl, s);
+    if (mode == kDown) return launch_gemm_t<kDown, true, 16, false, true>(maps, prm, max_blocks, max_runs, pdl, s);
+    return cudaErrorInvalidValue;
+  }
   // the block-diagonal shrink of 128-row blocks: its own kernel, fed by the group table
   if (block_diag) {
     if (mode != kShrink) return cudaErrorInvalidValue;
@@ -30,7 +37,12 @@ cudaError_t launch_gemm(int mode, int bt, const GemmMaps& maps, const GemmParams
   return cudaErrorInvalidValue;
 }
 
-bool gemm_stage_shape(int mode, int bt, int* k_tile, int* stages) {
+bool gemm_stage_shape(int mode, int bt, int* k_tile, int* stages, bool deep) {
+  if (deep && bt == 16 && mode != kShrink) {
+    *k_tile = GemmCfg<kGateUp, true, 16, false, true>::BK;
+    *stages = GemmCfg<kGateUp, true, 16, false, true>::STAGES;
+    return true;
+  }
 #define MOE_SHAPE_CASE(BT_, SWAP_)                                                       \
   if (bt == BT_) {                                                                       \
     switch (mode) {                                                                      \

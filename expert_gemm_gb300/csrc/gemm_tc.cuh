@@ -53,7 +53,7 @@
 
 namespace moe {
 
-template <int MODE, bool SWAP, int BT, bool BD = false>
+template <int MODE, bool SWAP, int BT, bool BD = false, bool DEEP = false>
 struct GemmCfg {
   static constexpr bool kLora = MODE != kShrink;
   // BD: the block-diagonal shrink of 128-row token blocks: a tile is one group of up to
@@ -63,6 +63,9 @@ struct GemmCfg {
   static constexpr bool BDIAG = BD;
   static_assert(!BD || (MODE == kShrink && !SWAP && (BT == 128 || BT == 256)),
                 "block-diagonal tiles: the shrink of token-tiled blocks");
+  // DEEP: the 16-token weight-streaming gate_up / down with a 6-deep ring (one CTA per
+  // SM), for batches of a few pairs whose tiles are fewer than the CTAs
+  static_assert(!DEEP || (SWAP && BT == 16 && MODE != kShrink), "deep ring: 16-token weight-streaming GEMMs");
   // 256-token blocks of gate_up / down run on a CTA pair (a cluster of 2): one 2-SM
   // MMA of M = 256 tokens x N = 256 weight rows per K-step; each CTA stages its own
   // 128 token rows and half of the weight rows, and holds its tokens' accumulator.
@@ -89,7 +92,7 @@ struct GemmCfg {
   // fits beside a shrink CTA -- measured faster on the decode shapes; 32/64: 5)
   // (weight-streaming shrink: 10-16 KB stages, 8 deep, 6 for 64-token tiles)
   static constexpr int STAGES = MODE == kShrink ? (SWAP ? (BT <= 32 ? 8 : 6) : 4)
-                                : SWAP           ? (BT <= 16 ? 3 : 5)
+                                : SWAP           ? (BT <= 16 ? (DEEP ? 6 : 3) : 5)
                                 : CTA2           ? 6   // + 16 KB of output staging
                                                  : (192 * 1024) / STAGE_BYTES;
   // accumulators: non-swapped MT tiles of M=128 tokens x N; swapped NH tiles of 128 x BT
@@ -404,10 +407,10 @@ constexpr int kSchedWarp = 6;
 // The producer asks for the next tile this many stages before the end of its tile.
 constexpr int kClaimAhead = 6;
 
-template <int MODE, bool SWAP, int BT, bool BD>
+template <int MODE, bool SWAP, int BT, bool BD, bool DEEP>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     moe_gemm_kernel(const __grid_constant__ GemmMaps maps, const __grid_constant__ GemmParams prm) {
-  using C = GemmCfg<MODE, SWAP, BT, BD>;
+  using C = GemmCfg<MODE, SWAP, BT, BD, DEEP>;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t rank = C::CTA2 ? cluster_ctarank() : 0u;   // 0: issues the pair's MMAs
@@ -1087,11 +1090,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if constexpr (C::CTA2) cluster_sync();
 }
 
-template <int MODE, bool SWAP, int BT, bool BD = false>
+template <int MODE, bool SWAP, int BT, bool BD = false, bool DEEP = false>
 cudaError_t launch_gemm_t(const GemmMaps& maps, const GemmParams& prm, int64_t max_blocks, int64_t max_runs,
                           bool pdl, cudaStream_t s) {
-  using C = GemmCfg<MODE, SWAP, BT, BD>;
-  auto kern = moe_gemm_kernel<MODE, SWAP, BT, BD>;
+  using C = GemmCfg<MODE, SWAP, BT, BD, DEEP>;
+  auto kern = moe_gemm_kernel<MODE, SWAP, BT, BD, DEEP>;
   int64_t cap_tiles;
   // groups <= unit chunks / gch + units <= (BT / 128) * (runs + blocks) for gch >= 4
   if constexpr (C::BDIAG) cap_tiles = (BT / 128) * (max_runs + max_blocks);

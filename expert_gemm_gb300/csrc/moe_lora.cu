@@ -268,6 +268,13 @@ bool block_diag_shrink(const moe_lora_dims* d, const Caps& cap) {
 int shrink_group_chunks(const moe_lora_dims* d) { return d->block_m == 256 ? 8 : 16; }
 int gate_up_ksplit(const moe_lora_dims* d, const Caps& cap);
 int down_ksplit(const moe_lora_dims* d, const Caps& cap);
+// Batches of a few pairs (at most 32: one to four tokens of top-8) on 16-token tiles run
+// gate_up and down with a 6-deep ring, one CTA per SM: their tiles are fewer than the
+// CTAs, and a tile's latency, not two CTAs sharing an SM, sets the pace.  Measured 3 vs
+// 6 stages: sweep T = 1 55.3 -> 51.7 us; the decode layer (64 pairs) 282 -> 288 us and
+// sweep T = 16 (128 pairs) 165.5 -> 173.0 us, so larger batches keep 3.
+constexpr int64_t kDeepRingPairs = 32;
+bool deep_ring(const moe_lora_dims* d) { return d->block_m == 16 && d->T * d->k <= kDeepRingPairs; }
 FwdLayout fwd_layout(const moe_lora_dims* d) {
   const Caps c = capacity(d);
   FwdLayout l{};
@@ -719,7 +726,7 @@ int do_forward(const moe_lora_dims* d, const uint16_t* x, const float* topk_w, c
     if (lim != 0 && lim < moe::kWaitTimeoutNs) q.acc_wait_ns = lim;
     q.ksplit = ks_gu;
     q.g_part = gpart;
-    MOE_CUDA(moe::launch_gemm(moe::kGateUp, BT, m_gu, q, cap.blocks, cap.runs, true, s));
+    MOE_CUDA(moe::launch_gemm(moe::kGateUp, BT, m_gu, q, cap.blocks, cap.runs, true, s, false, deep_ring(d)));
     if (ks_gu > 1) MOE_CUDA(moe::launch_silu_rows(gpart, ks_gu, cap.rows, al->totals, cap.rows, d->I, hs, true, s));
   }
   MOE_CUDA(mark(1 + MOE_LORA_STAGE_GATE_UP));
@@ -744,7 +751,7 @@ int do_forward(const moe_lora_dims* d, const uint16_t* x, const float* topk_w, c
     q.ksplit = l.ks_dn;
     q.tile_ctr = ctr + 3;
     q.n_ft = (d->H + 255) / 256;
-    MOE_CUDA(moe::launch_gemm(moe::kDown, BT, m_dn, q, cap.blocks, cap.runs, true, s));
+    MOE_CUDA(moe::launch_gemm(moe::kDown, BT, m_dn, q, cap.blocks, cap.runs, true, s, false, deep_ring(d)));
   }
   MOE_CUDA(mark(1 + MOE_LORA_STAGE_DOWN));
   MOE_CUDA(moe::launch_combine(y, l.ks_dn, cap.rows, prow, al->sorted_p, al->totals, topk_w, d->T, d->k, d->H, out,
@@ -838,7 +845,7 @@ int moe_lora_plan_query(const moe_lora_dims* d, moe_lora_plan* out) {
   p.ksplit[3] = l.ks_dn;
   const int modes[4] = {moe::kShrink, moe::kGateUp, moe::kShrink, moe::kDown};
   for (int g = 0; g < 4; ++g)
-    if (!moe::gemm_stage_shape(modes[g], d->block_m, &p.k_tile[g], &p.stages[g]))
+    if (!moe::gemm_stage_shape(modes[g], d->block_m, &p.k_tile[g], &p.stages[g], deep_ring(d)))
       return fail(MOE_LORA_EUNSUPPORTED, "no GEMM compiled for block_m = %d", d->block_m);
   if (cores) {   // one K slice per CTA, no pipeline
     p.k_tile[0] = p.k_tile[2] = moe::kShrinkSlice;

@@ -133,3 +133,17 @@ def test_every_compiled_block_size_has_a_plan():
         assert p["block_m"] == bm and all(s >= 2 for s in p["stages"].values())
     with pytest.raises(ml.MoeLoraError):
         ml.plan(dims(wl, 48))
+
+
+def test_deep_ring_for_a_few_pairs():
+    """16-token tiles run gate_up and down with a 6-deep ring for batches of at most 32
+    pairs (a single token of top-8), and with 3 stages (two CTAs per SM) above."""
+    one = ml.plan(dims(W.get("sweep_T1"), 0))
+    assert one["block_m"] == 16 and one["stages"]["gate_up"] == 6 and one["stages"]["down"] == 6
+    for name in ("decode", "sweep_T16"):
+        p = ml.plan(dims(W.get(name), 0))
+        assert p["block_m"] == 16 and p["stages"]["gate_up"] == 3 and p["stages"]["down"] == 3
+    wl = W.custom(name="four", T=4, H=256, I=256, E=16, k=8, L=2, ranks=(16, 16), lora_mode="uniform")
+    assert ml.plan(dims(wl, 16))["stages"]["gate_up"] == 6
+    wl = W.custom(name="five", T=5, H=256, I=256, E=16, k=8, L=2, ranks=(16, 16), lora_mode="uniform")
+    assert ml.plan(dims(wl, 16))["stages"]["gate_up"] == 3
