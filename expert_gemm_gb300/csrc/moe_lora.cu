@@ -762,7 +762,7 @@ int do_forward(const moe_lora_dims* d, const uint16_t* x, const float* topk_w, c
 
 // ---- layer_host workspace: [align | forward | inputs | route out | align arrays | out | status]
 struct LayerLayout {
-  size_t align, fwd, logits, lora, x, ids, w, sp, eb, be, br, runs, tot, out, status, bytes;
+  size_t align, fwd, logits, lora, x, ids, w, sp, eb, be, br, runs, out, status, bytes;
 };
 LayerLayout layer_layout(const moe_lora_dims* d) {
   const AlignLayout a = align_layout(d);
@@ -782,9 +782,8 @@ LayerLayout layer_layout(const moe_lora_dims* d) {
   l.be = off;     off += up256((size_t)c.blocks * 4);
   l.br = off;     off += up256((size_t)(c.blocks + 1) * 4);
   l.runs = off;   off += up256((size_t)c.runs * 16);
-  l.tot = off;    off += up256(4 * 4);
   l.out = off;    off += up256((size_t)d->T * d->H * 2);
-  l.status = off; off += up256(4);
+  l.status = off; off += up256(8 * 4);   // {status, unused[3], totals[4]}
   l.bytes = off;
   return l;
 }
@@ -793,7 +792,7 @@ LayerLayout layer_layout(const moe_lora_dims* d) {
 
 extern "C" {
 
-int moe_lora_version(void) { return 303; }
+int moe_lora_version(void) { return 304; }
 
 int moe_lora_debug_set_acc_wait_ns(uint64_t ns) {
   g_acc_wait_ns.store(ns, std::memory_order_relaxed);
@@ -917,12 +916,56 @@ int moe_lora_forward(const moe_lora_dims* d, const uint16_t* x, const float* top
 }  // extern "C"
 
 namespace {
-// Enqueues the layer_host sequence on s without synchronising: copies in, route+align,
-// forward, out and (status, totals) back.  status_dst/totals_dst: host destinations.
+// Host buffers the kernels read or write in place instead of through a copy: pinned and
+// mapped (cudaHostAlloc, cudaHostRegister) at the same address on both sides, as pinned
+// memory is under unified addressing on a coherent CPU-GPU link, and 16-byte aligned
+// (the kernels touch them in 16-byte vectors).  Both ends of the range are checked, so
+// a buffer registered only in part takes the copy.  Up to kInPlaceMaxBytes: a copy node
+// costs a few microseconds whatever its size, while a kernel reading or writing through
+// the link runs longer the more it moves; past a few MB the copy engines win.
+constexpr size_t kInPlaceMaxBytes = 4u << 20;
+// x in place up to 1 MB of gather reads: measured through the captured layer, a
+// 16-token decode batch (369 KB of reads) gained 2 us over the copy.
+constexpr size_t kInPlaceMaxGatherBytes = 1u << 20;
+bool in_place(const void* p, size_t bytes) {
+  if (!p || bytes == 0 || bytes > kInPlaceMaxBytes || !aligned16(p)) return false;
+  const char* ends[2] = {static_cast<const char*>(p), static_cast<const char*>(p) + bytes - 1};
+  for (const char* q : ends) {
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, q) != cudaSuccess) {
+      (void)cudaGetLastError();   // an unknown pointer is not an error of this call
+      return false;
+    }
+    if (a.type != cudaMemoryTypeHost || a.devicePointer != static_cast<const void*>(q)) return false;
+  }
+  return true;
+}
+
+// Which host buffers of a layer call the kernels touch in place.  Decided before any
+// stream capture (the pointer queries are not stream work).
+struct InPlace {
+  bool logits = false, lora = false, x = false, out = false;
+};
+InPlace in_place_of(const moe_lora_dims* d, const float* logits_host, const int32_t* lora_ids_host,
+                    const uint16_t* x_host, const uint16_t* out_host) {
+  InPlace ip;
+  if (d->T <= 0) return ip;
+  const size_t T = (size_t)d->T;
+  ip.logits = in_place(logits_host, T * d->E * 4);
+  ip.lora = in_place(lora_ids_host, T * 4);
+  // the gather reads a token's row once per pair: k times its bytes over the link
+  ip.x = T * d->H * 2 * d->k <= kInPlaceMaxGatherBytes && in_place(x_host, T * d->H * 2);
+  ip.out = in_place(out_host, T * d->H * 2);
+  return ip;
+}
+
+// Enqueues the layer_host sequence on s without synchronising: inputs in (copied, or
+// read in place), route+align, forward, out back (written in place, or copied) and one
+// copy of the 32-byte record {status, unused[3], totals[4]} into status8_dst (host int32[8]).
 int layer_enqueue(const moe_lora_dims* d, const float* logits_host, const int32_t* lora_ids_host,
                   const uint16_t* x_host, const uint16_t* W_gu, const uint16_t* W_dn, const uint16_t* A_gu,
                   const uint16_t* B_gu, const uint16_t* A_dn, const uint16_t* B_dn, uint16_t* out_host,
-                  void* workspace, size_t workspace_bytes, int32_t* status_dst, int32_t* totals_dst,
+                  void* workspace, size_t workspace_bytes, int32_t* status8_dst, const InPlace& ip,
                   cudaStream_t s) {
   MOE_TRY(validate_dims(d));
   const LayerLayout l = layer_layout(d);
@@ -941,31 +984,40 @@ int layer_enqueue(const moe_lora_dims* d, const float* logits_host, const int32_
   int32_t* ids = reinterpret_cast<int32_t*>(b + l.ids);
   float* w = reinterpret_cast<float*>(b + l.w);
   uint16_t* out = reinterpret_cast<uint16_t*>(b + l.out);
-  int32_t* status = reinterpret_cast<int32_t*>(b + l.status);
+  int32_t* status = reinterpret_cast<int32_t*>(b + l.status);   // [0] status, [4..7] align totals
   moe_lora_align_buf al{reinterpret_cast<int32_t*>(b + l.sp), reinterpret_cast<int32_t*>(b + l.eb),
                         reinterpret_cast<int32_t*>(b + l.be), reinterpret_cast<int32_t*>(b + l.br),
-                        reinterpret_cast<int32_t*>(b + l.runs), reinterpret_cast<int32_t*>(b + l.tot)};
+                        reinterpret_cast<int32_t*>(b + l.runs), status + 4};
   const size_t T = (size_t)d->T;
   if (T > 0) {
-    MOE_CUDA(cudaMemcpyAsync(logits, logits_host, T * d->E * 4, cudaMemcpyHostToDevice, s));
-    MOE_CUDA(cudaMemcpyAsync(lora, lora_ids_host, T * 4, cudaMemcpyHostToDevice, s));
-    MOE_CUDA(cudaMemcpyAsync(x, x_host, T * d->H * 2, cudaMemcpyHostToDevice, s));
-    MOE_TRY(do_route_align(d, logits, lora, ids, w, &al, b + l.align, l.fwd - l.align, s));
+    const size_t lb = T * d->E * 4, rb = T * 4, xb = T * d->H * 2;
+    const float* lg = logits;
+    const int32_t* lr = lora;
+    const uint16_t* xi = x;
+    if (ip.logits) lg = logits_host;
+    else MOE_CUDA(cudaMemcpyAsync(logits, logits_host, lb, cudaMemcpyHostToDevice, s));
+    if (ip.lora) lr = lora_ids_host;
+    else MOE_CUDA(cudaMemcpyAsync(lora, lora_ids_host, rb, cudaMemcpyHostToDevice, s));
+    if (ip.x) xi = x_host;
+    else MOE_CUDA(cudaMemcpyAsync(x, x_host, xb, cudaMemcpyHostToDevice, s));
+    uint16_t* o = ip.out ? out_host : out;
+    MOE_TRY(do_route_align(d, lg, lr, ids, w, &al, b + l.align, l.fwd - l.align, s));
+    MOE_TRY(do_forward(d, xi, w, &al, W_gu, W_dn, A_gu, B_gu, A_dn, B_dn, o, b + l.fwd, l.logits - l.fwd, status, s,
+                       nullptr));
+    if (o == out) MOE_CUDA(cudaMemcpyAsync(out_host, out, xb, cudaMemcpyDeviceToHost, s));
   } else {
     MOE_TRY(do_align(d, ids, lora, &al, b + l.align, l.fwd - l.align, s));
+    MOE_TRY(do_forward(d, x, w, &al, W_gu, W_dn, A_gu, B_gu, A_dn, B_dn, out, b + l.fwd, l.logits - l.fwd, status, s,
+                       nullptr));
   }
-  MOE_TRY(do_forward(d, x, w, &al, W_gu, W_dn, A_gu, B_gu, A_dn, B_dn, out, b + l.fwd, l.logits - l.fwd, status, s,
-                      nullptr));
-  if (T > 0) MOE_CUDA(cudaMemcpyAsync(out_host, out, T * d->H * 2, cudaMemcpyDeviceToHost, s));
-  MOE_CUDA(cudaMemcpyAsync(status_dst, status, 4, cudaMemcpyDeviceToHost, s));
-  MOE_CUDA(cudaMemcpyAsync(totals_dst, al.totals, 16, cudaMemcpyDeviceToHost, s));
+  MOE_CUDA(cudaMemcpyAsync(status8_dst, status, 32, cudaMemcpyDeviceToHost, s));
   return MOE_LORA_OK;
 }
 }  // namespace
 
 struct moe_lora_graph {
   cudaGraphExec_t exec = nullptr;
-  int32_t* status_host = nullptr;   // [0] device status, [4..7] align totals
+  int32_t* status_host = nullptr;   // {status, unused[3], totals[4]}, copied in by each run
 };
 
 extern "C" {
@@ -976,12 +1028,14 @@ int moe_lora_layer_host(const moe_lora_dims* d, const float* logits_host, const 
                         void* workspace, size_t workspace_bytes, int64_t* dropped, void* stream) {
   MOE_RESOLVE(d);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  int32_t host_status = 0, tot[4] = {0, 0, 0, 0};
+  int32_t rec[8] = {0, 0, 0, 0, 0, 0, 0, 0};   // {status, unused[3], totals[4]}
+  MOE_TRY(validate_dims(d));
+  const InPlace ip = in_place_of(d, logits_host, lora_ids_host, x_host, out_host);
   MOE_TRY(layer_enqueue(d, logits_host, lora_ids_host, x_host, W_gu, W_dn, A_gu, B_gu, A_dn, B_dn, out_host,
-                        workspace, workspace_bytes, &host_status, tot, s));
+                        workspace, workspace_bytes, rec, ip, s));
   MOE_CUDA(cudaStreamSynchronize(s));
-  if (dropped) *dropped = tot[3];
-  if (host_status != 0) return fail(MOE_LORA_EDEVICE, "device status 0x%x", host_status);
+  if (dropped) *dropped = rec[4 + 3];
+  if (rec[0] != 0) return fail(MOE_LORA_EDEVICE, "device status 0x%x", rec[0]);
   return MOE_LORA_OK;
 }
 
@@ -996,15 +1050,18 @@ int moe_lora_layer_graph_create(const moe_lora_dims* d, const float* logits_host
   MOE_TRY(check_ptr(status_host, "status_host", false));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (!s) return fail(MOE_LORA_EINVAL, "graph capture needs a non-default stream");
-  // one eager run: validation and the kernels' one-time set-up happen outside the capture
+  // one eager run: validation, the in-place decisions and the kernels' one-time
+  // set-up happen outside the capture
+  MOE_TRY(validate_dims(d));
+  const InPlace ip = in_place_of(d, logits_host, lora_ids_host, x_host, out_host);
   MOE_TRY(layer_enqueue(d, logits_host, lora_ids_host, x_host, W_gu, W_dn, A_gu, B_gu, A_dn, B_dn, out_host,
-                        workspace, workspace_bytes, status_host, status_host + 4, s));
+                        workspace, workspace_bytes, status_host, ip, s));
   MOE_CUDA(cudaStreamSynchronize(s));
   if (status_host[0] != 0) return fail(MOE_LORA_EDEVICE, "device status 0x%x", status_host[0]);
   cudaGraph_t g = nullptr;
   MOE_CUDA(cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal));
   const int st = layer_enqueue(d, logits_host, lora_ids_host, x_host, W_gu, W_dn, A_gu, B_gu, A_dn, B_dn, out_host,
-                               workspace, workspace_bytes, status_host, status_host + 4, s);
+                               workspace, workspace_bytes, status_host, ip, s);
   const cudaError_t ce = cudaStreamEndCapture(s, &g);
   if (st != MOE_LORA_OK) {
     if (g) cudaGraphDestroy(g);

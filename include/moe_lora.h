@@ -234,11 +234,16 @@ int moe_lora_forward(const moe_lora_dims *d, const uint16_t *x, const float *top
                      int32_t *dev_status, void *stream, void *const *stage_events);
 
 /*
- * The whole layer from HOST inputs to a HOST output: copies logits [T][E] fp32,
+ * The whole layer from HOST inputs to a HOST output: brings logits [T][E] fp32,
  * lora_ids [T] int32 and x [T][H] bf16 to the device, runs route, align and
- * forward on `stream`, copies out [T][H] bf16 back and synchronises the stream.
- * Weights are device pointers (resident).  Host buffers should be pinned for the
- * copies to be asynchronous.  workspace: device scratch of at least
+ * forward on `stream`, returns out [T][H] bf16 and synchronises the stream.
+ * Weights are device pointers (resident).  A host buffer of at most 4 MB that is
+ * pinned and mapped at the same address on both sides (cudaHostAlloc or
+ * cudaHostRegister memory under unified addressing, as on a coherent CPU-GPU link)
+ * and 16-byte aligned is read or written in place by the kernels over the link
+ * (x only while T*k*H*2 <= 1 MB: the gather reads a token's row once per pair);
+ * any other host buffer goes through a copy on `stream` (pinned memory keeps those
+ * copies asynchronous).  workspace: device scratch of at least
  * moe_lora_layer_workspace_size().  Returns MOE_LORA_EDEVICE if the device
  * reported a timeout.  *dropped (may be NULL) receives the dropped-pair count.
  */
@@ -252,14 +257,15 @@ int moe_lora_layer_host(const moe_lora_dims *d, const float *logits_host,
                         int64_t *dropped, void *stream);
 
 /*
- * The moe_lora_layer_host sequence (host->device copies, route, align, forward,
- * device->host copies) captured once as a CUDA graph and replayed per step: one
- * launch instead of three copies, the kernels and two copies issued from the CPU.
+ * The moe_lora_layer_host sequence (inputs in, route, align, forward, output back,
+ * each host buffer read or written in place or copied as moe_lora_layer_host
+ * decides) captured once as a CUDA graph and replayed per step: one launch instead
+ * of every copy and kernel issued from the CPU.
  * The pages capture GPU operation sequences with CUDA graphs to cut kernel-launch
  * and CPU overhead ([AWS] "Execution optimizations").
  *   create: same arguments as moe_lora_layer_host, with every host buffer pinned
  *           (cudaHostAlloc / cudaHostRegister) and status_host an extra pinned int32[8]
- *           that each run fills with the device status word and the align totals.
+ *           that each run fills with {device status word, 3 unused, align totals[4]}.
  *           Runs the layer once eagerly (validation, kernel set-up), then captures it
  *           on `stream`.  *graph receives the handle.
  *   run:    launches the graph on `stream` and synchronises it; the host buffers'

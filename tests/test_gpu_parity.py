@@ -522,6 +522,29 @@ def test_layer_host_entry(ml, torch, oracle, name):
     assert elem <= TOL, (wl.name, elem, norm)
 
 
+@pytest.mark.parametrize("name", ["decode", "sweep_T4096"])
+def test_layer_host_in_place_and_copied_buffers_agree(ml, torch, name):
+    """moe_lora_layer_host reads pinned host inputs and writes a pinned host output in
+    place (at most 4 MB each) and copies pageable ones: decode's pinned buffers are all
+    in place, its pageable ones all copied; at T = 4096 the 16 MB x and out are copied
+    while the 2 MB logits are read in place.  Every path gives the bytes of the
+    device-buffer step."""
+    wl = W.get(name)
+    logits, lora, x, w = inputs(wl)
+    layer = ml.Layer(dims_of(wl, 0, ml), dev_weights(w, torch))
+    ref = layer.step(to_dev(logits, torch), to_dev(lora, torch), to_dev(x, torch)).clone()
+    torch.cuda.synchronize()
+    ref_h = ref.view(torch.int16).cpu()
+    for pinned in (True, False):
+        host = lambda a: torch.from_numpy(np.ascontiguousarray(a)).clone()   # noqa: E731
+        lg, lr, xh = host(logits), host(lora), host(x.view(np.int16))
+        out_h = torch.full((wl.T, wl.H), 0x7fc1, dtype=torch.int16)
+        if pinned:
+            lg, lr, xh, out_h = lg.pin_memory(), lr.pin_memory(), xh.pin_memory(), out_h.pin_memory()
+        assert layer.step_host(lg, lr, xh, out_h) == 0
+        assert torch.equal(out_h, ref_h), (name, pinned)
+
+
 @pytest.mark.parametrize("name", ["tiny", "decode", "sweep_T256"])
 def test_layer_graph_replay(ml, torch, oracle, name):
     """moe_lora_layer_graph_*: the captured host-to-host layer gives moe_lora_layer_host's
