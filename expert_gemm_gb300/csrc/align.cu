@@ -483,7 +483,8 @@ __global__ void __launch_bounds__(1024) align_scatter_kernel(AlignLaunch a) {
 // through global memory (the decode front end is latency, not bandwidth).
 //
 // small_keys: the keys of the P pairs sorted in keys[CH]; returns the invalid-pair count.
-__device__ int small_keys(const AlignLaunch& a, const int32_t* ids, uint32_t* keys) {
+// lora: the tokens' adapter ids (a.lora_ids, or a shared copy of them).
+__device__ int small_keys(const AlignLaunch& a, const int32_t* ids, const int32_t* lora, uint32_t* keys) {
   __shared__ int32_t s_invalid;
   const int CH = 1 << a.ch_log2;
   const int LB = a.L + 1;
@@ -494,7 +495,7 @@ __device__ int small_keys(const AlignLaunch& a, const int32_t* ids, uint32_t* ke
     uint32_t key = kInvalidKey;
     if (i < a.P) {
       const int e = ids[i];
-      const int ad = a.lora_ids[i / a.k];
+      const int ad = lora[i / a.k];
       if (e >= 0 && e < a.E && ad >= -1 && ad < a.L)
         key = (static_cast<uint32_t>(e * LB + ad + 1) << a.ch_log2) | static_cast<uint32_t>(i);
       else
@@ -597,9 +598,11 @@ __device__ void small_layout(const AlignLaunch& a, const uint32_t* keys, int n_i
 __global__ void __launch_bounds__(1024) align_small_kernel(AlignLaunch a) {
   extern __shared__ uint32_t keys[];
   int32_t* s_runblk = reinterpret_cast<int32_t*>(keys + (1 << a.ch_log2));
-  const int inval = small_keys(a, a.topk_ids, keys);
+  const int inval = small_keys(a, a.topk_ids, a.lora_ids, keys);
   small_layout(a, keys, inval, s_runblk);
 }
+
+constexpr int kRouteAlignLoraTokens = 32;   // adapter ids staged in shared memory up to this T
 
 // Route and align in one CTA (one chunk): each warp routes tokens into shared memory,
 // the expert ids are copied out to topk_ids, and the align phases read them from
@@ -608,14 +611,20 @@ __global__ void __launch_bounds__(1024) route_align_small_kernel(AlignLaunch a, 
                                                                  float* __restrict__ topk_w,
                                                                  int32_t* __restrict__ topk_ids) {
   extern __shared__ uint32_t keys[];
+  __shared__ int32_t s_lora[kRouteAlignLoraTokens];
   int32_t* s_ids = reinterpret_cast<int32_t*>(keys + (1 << a.ch_log2));
   const int T = static_cast<int>(a.P / a.k);
   const int lane = threadIdx.x & 31;
+  // the adapter ids are fetched while the warps route, not after: the two input reads
+  // (from DRAM, or host memory over the link) overlap instead of following each other
+  const bool stage_lora = T <= kRouteAlignLoraTokens;
+  if (stage_lora && static_cast<int>(threadIdx.x) < T) s_lora[threadIdx.x] = a.lora_ids[threadIdx.x];
   for (int t = threadIdx.x >> 5; t < T; t += blockDim.x >> 5)
     route_token(logits + static_cast<int64_t>(t) * a.E, a.E, a.k, lane, s_ids + t * a.k, topk_w + t * a.k);
   __syncthreads();
   for (int p = threadIdx.x; p < a.P; p += blockDim.x) topk_ids[p] = s_ids[p];
-  const int inval = small_keys(a, s_ids, keys);   // ends with a barrier: s_ids is free again
+  // ends with a barrier: s_ids is free again
+  const int inval = small_keys(a, s_ids, stage_lora ? s_lora : a.lora_ids, keys);
   small_layout(a, keys, inval, s_ids);
 }
 
