@@ -527,8 +527,8 @@ def test_layer_host_in_place_and_copied_buffers_agree(ml, torch, name):
     """moe_lora_layer_host reads pinned host inputs and writes a pinned host output in
     place (at most 4 MB each) and copies pageable ones: decode's pinned buffers are all
     in place, its pageable ones all copied; at T = 4096 the 16 MB x and out are copied
-    while the 2 MB logits are read in place.  Every path gives the bytes of the
-    device-buffer step."""
+    while the 2 MB logits are read in place; pinned views 4 bytes off a 16-byte boundary
+    are copied.  Every path gives the bytes of the device-buffer step."""
     wl = W.get(name)
     logits, lora, x, w = inputs(wl)
     layer = ml.Layer(dims_of(wl, 0, ml), dev_weights(w, torch))
@@ -543,6 +543,15 @@ def test_layer_host_in_place_and_copied_buffers_agree(ml, torch, name):
             lg, lr, xh, out_h = lg.pin_memory(), lr.pin_memory(), xh.pin_memory(), out_h.pin_memory()
         assert layer.step_host(lg, lr, xh, out_h) == 0
         assert torch.equal(out_h, ref_h), (name, pinned)
+    # pinned but not 16-byte aligned (each view starts 4 bytes into its buffer): copied
+    lg_b = torch.empty(logits.size + 1, dtype=torch.float32).pin_memory()
+    lg_b[1:].copy_(torch.from_numpy(logits.reshape(-1)))
+    x_b = torch.empty(x.size + 2, dtype=torch.int16).pin_memory()
+    x_b[2:].copy_(torch.from_numpy(x.view(np.int16).reshape(-1)))
+    out_b = torch.full((wl.T * wl.H + 2,), 0x7fc1, dtype=torch.int16).pin_memory()
+    lr_h = torch.from_numpy(np.ascontiguousarray(lora)).clone().pin_memory()
+    assert layer.step_host(lg_b[1:], lr_h, x_b[2:], out_b[2:]) == 0
+    assert torch.equal(out_b[2:].view(wl.T, wl.H), ref_h), name
 
 
 @pytest.mark.parametrize("name", ["tiny", "decode", "sweep_T256"])
