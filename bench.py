@@ -384,7 +384,7 @@ def secondary_steps(ms_est: float, k_arg: int) -> int:
 def run_secondary(torch, ml, name, wd, w_host, rank, world, flush, args):
     """One secondary configuration: device timing, roofline, clocks, oracle baseline."""
     wl = W.get(name)
-    bm = ml.pick_block_m(wl.T, wl.k, wl.E, wl.L)
+    bm = ml.pick_block_m(wl.T, wl.k, wl.E, wl.L, wl.H, wl.I)
     probe = measure(torch, ml, wl, wd, rank, 3, 3, bm, world, flush, graph=False, e2e=False)
     k = secondary_steps(probe["ms"], args.steps)
     m = measure(torch, ml, wl, wd, rank, k, 3, bm, world, flush, graph=False, e2e=False,
@@ -412,7 +412,7 @@ def run_ours(args, rank, world, local_rank):
     w_host = W.make_weights(wl, 0)                # same weights on every replica, own batch per rank
     wd = _upload(torch, w_host)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
-    bm = args.block_m or ml.pick_block_m(wl.T, wl.k, wl.E, wl.L)
+    bm = args.block_m or ml.pick_block_m(wl.T, wl.k, wl.E, wl.L, wl.H, wl.I)
     m = measure(torch, ml, wl, wd, rank, args.steps, args.warmup, bm, world, flush,
                 graph=not args.no_graph, clocks=ClockSampler(local_rank))
     roof, layer = roofline_of(m, ml)

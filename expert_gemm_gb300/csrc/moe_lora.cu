@@ -117,7 +117,13 @@ int validate_dims(const moe_lora_dims* d) {
 // short runs carries twice the LoRA expand chunks of a 128-row one.  Measured, 128 vs
 // 256 rows: the wide layer (32 adapters) at 768 / 1024 pairs per expert 1.445 / 1.791
 // vs 1.398 / 1.736 ms, at 512 1.075 vs 1.094 ms; the sweep layer (64 adapters) at 512 /
-// 1024 pairs per expert 1.34 / 2.05 vs 1.80 / 2.48 ms.
+// 1024 pairs per expert 1.34 / 2.05 vs 1.80 / 2.48 ms.  16-row tiles (two CTAs an SM)
+// beat 32-row ones up to 24 pairs per expert on every layer measured (µs, 16 vs 32 rows:
+// sweep layer at 16 / 24 pairs 332 / 388 vs 345 / 400, decode layer at 16 pairs 342 vs
+// 357, dense MLP at 16 tokens 182 vs 187).  An expert whose weights exceed the L2 is
+// streamed from DRAM once per block of it, so there the smallest tile that holds the
+// expert's pairs wins: a 786 MB dense MLP at 32 tokens 187 us on 32 rows against 249 on
+// 16 and 241 on 64, at 64 tokens 246 us on 64 rows against 264 on 32 and 290 on 128.
 struct TileClass {
   double ppe_above;       // the class holds shapes whose T*k/E exceeds this
   int block_m;            // token tile: < 128 weight-streaming, >= 128 token-tiled
@@ -128,21 +134,30 @@ struct TileClass {
   int shrink_cores;       // 1: the shrinks run on CUDA cores (short runs, split over K), else tcgen05
 };
 constexpr TileClass kTileTable[] = {
-    {-1.0, 16, 2, 3, 64, 8, 1},    // up to 10 pairs per expert (decode batches; down split 2
+    {-1.0, 16, 2, 3, 64, 8, 1},    // up to 24 pairs per expert (decode batches; down split 2
                                    //   ways on the decode layer: 283.9 -> 281.9 us against 3)
-    {10.0, 32, 2, 6, 64, 8, 1},    // 10 .. 24
+    {24.0, 32, 2, 6, 64, 8, 1},    // no class of its own (row 64 shares its bound): experts
+                                   //   larger than the L2 with 17 .. 32 pairs
     {24.0, 64, 2, 6, 64, 8, 1},    // 24 .. 95
     {95.0, 128, 1, 1, 0, 1, 0},    // 95 .. 2047: token-tiled, compute-bound, no K split
     {2047.0, 256, 1, 1, 0, 1, 0},  // more than 2047: 256-token blocks on CTA pairs
 };
 constexpr int kTableRows = sizeof(kTileTable) / sizeof(kTileTable[0]);
 
-// Row of the shape class of (T, k, E).
+// Row of the shape class of (T, k, E, L, H, I); H or I <= 0: expert size unknown.
 constexpr double kLongRunsPpe = 768.0;     // from here 256-row blocks can win ...
 constexpr double kLongRunsPerBucket = 20.0; // ... when the runs are this long
-int class_row(int64_t T, int32_t k, int32_t E, int32_t L) {
+constexpr double kL2Bytes = 129e6;                 // GB300 L2
+constexpr double kLargeExpertMaxPpe = 128.0;       // the large-expert rule up to one 128-row block
+int class_row(int64_t T, int32_t k, int32_t E, int32_t L, int64_t H, int64_t I) {
   if (E <= 0 || k <= 0 || T <= 0) return 0;
   const double ppe = (double)T * k / E;
+  // an expert's weights (gate_up 2*I*H, down H*I, bf16) larger than the L2
+  if (H > 0 && I > 0 && 3.0 * H * I * 2.0 > kL2Bytes && ppe <= kLargeExpertMaxPpe) {
+    int row = 0;
+    while (row + 1 < kTableRows && kTileTable[row].block_m < ppe) ++row;
+    return row;
+  }
   int row = 0;
   for (int i = 0; i < kTableRows; ++i)
     if (ppe > kTileTable[i].ppe_above) row = i;
@@ -164,7 +179,7 @@ int block_row(int block_m) {
 int resolve(const moe_lora_dims* in, moe_lora_dims* out) {
   if (!in) return fail(MOE_LORA_EINVAL, "dims is NULL");
   *out = *in;
-  if (out->block_m == 0) out->block_m = kTileTable[class_row(out->T, out->k, out->E, out->L)].block_m;
+  if (out->block_m == 0) out->block_m = kTileTable[class_row(out->T, out->k, out->E, out->L, out->H, out->I)].block_m;
   return MOE_LORA_OK;
 }
 #define MOE_RESOLVE(d)                           \
@@ -820,8 +835,8 @@ const char* moe_lora_status_string(int status) {
 
 const char* moe_lora_last_error(void) { return g_err; }
 
-int32_t moe_lora_pick_block_m(int64_t T, int32_t k, int32_t E, int32_t L) {
-  return kTileTable[class_row(T, k, E, L)].block_m;
+int32_t moe_lora_pick_block_m(int64_t T, int32_t k, int32_t E, int32_t L, int32_t H, int32_t I) {
+  return kTileTable[class_row(T, k, E, L, H, I)].block_m;
 }
 
 int moe_lora_plan_query(const moe_lora_dims* d, moe_lora_plan* out) {

@@ -71,7 +71,7 @@ def load(path: str = LIB_PATH):
     lib.moe_lora_align_capacity.argtypes = [DP, C.POINTER(i64), C.POINTER(i64), C.POINTER(i64)]
     lib.moe_lora_workspace_size.argtypes = [DP, C.POINTER(sz), C.POINTER(sz)]
     lib.moe_lora_layer_workspace_size.argtypes = [DP, C.POINTER(sz)]
-    lib.moe_lora_pick_block_m.argtypes = [i64, i32, i32, i32]
+    lib.moe_lora_pick_block_m.argtypes = [i64, i32, i32, i32, i32, i32]
     lib.moe_lora_pick_block_m.restype = i32
     lib.moe_lora_route.argtypes = [vp, i64, i32, i32, vp, vp, vp]
     lib.moe_lora_align.argtypes = [DP, vp, vp, AP, vp, sz, vp]
@@ -160,9 +160,10 @@ def debug_set_shrink_tiles(mode: int):
     _check(load().moe_lora_debug_set_shrink_tiles(int(mode)))
 
 
-def pick_block_m(T: int, k: int, E: int, L: int = 0) -> int:
-    """The tile table's block_m for T tokens, top-k over E experts, L adapters."""
-    return load().moe_lora_pick_block_m(T, k, E, L)
+def pick_block_m(T: int, k: int, E: int, L: int = 0, H: int = 0, I: int = 0) -> int:
+    """The tile table's block_m for T tokens, top-k over E experts, L adapters, experts of
+    hidden size H and intermediate size I (0: unknown, the large-expert rule is left out)."""
+    return load().moe_lora_pick_block_m(T, k, E, L, H, I)
 
 
 def plan(d: LayerDims) -> dict:

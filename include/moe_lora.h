@@ -89,7 +89,7 @@ typedef struct moe_lora_dims {
     int32_t r_max;    /* storage rank: rows of A and of B; multiple of 8, <= 64         */
     int32_t block_m;  /* rows per align block: 16, 32, 64 (weight-streaming kernels)    */
                       /* or 128, 256 (token-tiled kernels); 0 = the tile table's choice */
-                      /* for (T, k, E, L) (moe_lora_pick_block_m, moe_lora_plan_query)  */
+                      /* for the dims (moe_lora_pick_block_m, moe_lora_plan_query)      */
     const int32_t *ranks; /* HOST array [L]: rank of adapter a, 1 <= ranks[a] <= r_max  */
 } moe_lora_dims;
 
@@ -125,14 +125,17 @@ int moe_lora_align_capacity(const moe_lora_dims *d, int64_t *max_rows, int64_t *
  * with forward's region at offset align_bytes).  Returns a status. */
 int moe_lora_workspace_size(const moe_lora_dims *d, size_t *align_bytes, size_t *forward_bytes);
 
-/* The compiled-in tile table's block_m for T*k pairs over E experts and L adapters: the
- * shape class is the pairs per expert T*k/E (16, 32, 64 weight-streaming up to 10, 24,
- * 95 pairs per expert; 128 token-tiled up to 2047; 256, token-tiled on CTA pairs,
- * above), and from 768 pairs per expert also 256 when the adapter runs are long, i.e.
- * T*k / (E*(L+1)) >= 20.  The pages pick tuned tile configurations per shape ([AWS]
- * "Tuning kernel configurations for Amazon SageMaker AI and Amazon Bedrock"; [KO]
- * "Amazon 전용 튜닝").  Host only. */
-int32_t moe_lora_pick_block_m(int64_t T, int32_t k, int32_t E, int32_t L);
+/* The compiled-in tile table's block_m for T*k pairs over E experts, L adapters and
+ * experts of hidden size H and intermediate size I: the shape class is the pairs per
+ * expert T*k/E (16, 64 weight-streaming up to 24, 95 pairs per expert; 128 token-tiled
+ * up to 2047; 256, token-tiled on CTA pairs, above), and from 768 pairs per expert
+ * also 256 when the adapter runs are long, i.e. T*k / (E*(L+1)) >= 20.  An expert whose
+ * bf16 weights (3*H*I*2 bytes) exceed the L2 takes, up to 128 pairs per expert, the
+ * smallest of 16, 32, 64, 128 that holds T*k/E pairs (each block of it streams the
+ * expert from DRAM).  H or I <= 0 leaves that rule out.  The pages pick tuned tile
+ * configurations per shape ([AWS] "Tuning kernel configurations for Amazon SageMaker
+ * AI and Amazon Bedrock"; [KO] "Amazon 전용 튜닝").  Host only. */
+int32_t moe_lora_pick_block_m(int64_t T, int32_t k, int32_t E, int32_t L, int32_t H, int32_t I);
 
 /* What the calls will launch for these dims: the tile-table row and the per-GEMM
  * choices.  GEMM index: 0 gate_up shrink, 1 gate_up, 2 down shrink, 3 down. */

@@ -33,7 +33,7 @@ def run_case(ml, torch, oracle, wl, block_m=None, tokens=None, logits=None, lora
     logits0, lora0, x, w = inputs(wl)
     logits = logits0 if logits is None else logits
     lora = lora0 if lora is None else lora
-    bm = block_m or ml.pick_block_m(wl.T, wl.k, wl.E, wl.L)
+    bm = block_m or ml.pick_block_m(wl.T, wl.k, wl.E, wl.L, wl.H, wl.I)
     d = dims_of(wl, bm, ml)
     guards = Guarded(torch)
     layer = guards.guard_layer(ml.Layer(d, dev_weights(w, torch)))
@@ -112,7 +112,7 @@ def test_dense_decode_config(ml, torch, oracle):
     """The dense 32B-class MLP at decode size (H=5120, I=25600), every output element; its
     shrinks are tcgen05 tiles split over K (fp32 partials summed by the last split)."""
     wl = W.get("dense_decode")
-    p = ml.plan(dims_of(wl, ml.pick_block_m(wl.T, wl.k, wl.E, wl.L), ml))
+    p = ml.plan(dims_of(wl, ml.pick_block_m(wl.T, wl.k, wl.E, wl.L, wl.H, wl.I), ml))
     assert not p["shrink_on_cores"] and p["ksplit"]["shrink_gu"] > 1 and p["ksplit"]["shrink_dn"] > 1
     run_case(ml, torch, oracle, wl)
 
@@ -345,7 +345,7 @@ def test_route_align_matches_separate_calls(ml, torch, name):
     gives the same bytes as moe_lora_route followed by moe_lora_align."""
     wl = W.get(name)
     logits, lora = W.make_routing(wl, 0)
-    bm = ml.pick_block_m(wl.T, wl.k, wl.E, wl.L)
+    bm = ml.pick_block_m(wl.T, wl.k, wl.E, wl.L, wl.H, wl.I)
     d = dims_of(wl, bm, ml)
     a_bytes, _ = ml.workspace_size(d)
     lg, lr = to_dev(logits, torch), to_dev(lora, torch)
@@ -508,7 +508,7 @@ def test_layer_host_entry(ml, torch, oracle, name):
     """moe_lora_layer_host: host inputs in, host output back, same result."""
     wl = W.get(name)
     logits, lora, x, w = inputs(wl)
-    bm = ml.pick_block_m(wl.T, wl.k, wl.E, wl.L)
+    bm = ml.pick_block_m(wl.T, wl.k, wl.E, wl.L, wl.H, wl.I)
     layer = ml.Layer(dims_of(wl, bm, ml), dev_weights(w, torch))
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()   # noqa: E731
     lg, lr, xh = pin(logits), pin(lora), pin(x.view(np.int16))

@@ -23,27 +23,46 @@ def lib():
 
 
 # (name, block_m the table must pick)
-EXPECTED = [("tiny", 32), ("decode", 16), ("prefill", 256), ("wide", 256), ("dense_decode", 32),
-            ("sweep_T1", 16), ("sweep_T16", 16), ("sweep_T256", 32), ("sweep_T4096", 128)]
+EXPECTED = [("tiny", 16), ("decode", 16), ("prefill", 256), ("wide", 256), ("dense_decode", 16),
+            ("sweep_T1", 16), ("sweep_T16", 16), ("sweep_T256", 16), ("sweep_T4096", 128)]
 
 
 @pytest.mark.parametrize("name,bm", EXPECTED)
 def test_class_of_each_workload(name, bm):
     wl = W.get(name)
-    assert ml.pick_block_m(wl.T, wl.k, wl.E, wl.L) == bm
+    assert ml.pick_block_m(wl.T, wl.k, wl.E, wl.L, wl.H, wl.I) == bm
     p = ml.plan(dims(wl, 0))
     assert p["block_m"] == bm
     assert p["weight_streaming"] == (bm < 128)
 
 
 def test_class_boundaries():
-    """Pairs per expert above 10, 24, 95 and 2047 move to the next row (short adapter runs:
-    255 adapters, so fewer than 20 pairs per (expert, adapter) bucket below 2048)."""
+    """Pairs per expert above 24, 95 and 2047 move to the next row (short adapter runs:
+    255 adapters, so fewer than 20 pairs per (expert, adapter) bucket below 2048); the
+    32-row tile is no class of its own.  Experts of the sweep layer (9.4 MB) are far below
+    the L2."""
     E, k, L = 8, 1, 255
-    for ppe, bm in [(1, 16), (10, 16), (11, 32), (24, 32), (25, 64), (95, 64), (96, 128), (2047, 128), (2048, 256),
+    for ppe, bm in [(1, 16), (10, 16), (11, 16), (24, 16), (25, 64), (95, 64), (96, 128), (2047, 128), (2048, 256),
                     (5000, 256)]:
         assert ml.pick_block_m(ppe * E, k, E, L) == bm, (ppe, bm)
+        assert ml.pick_block_m(ppe * E, k, E, L, 2048, 768) == bm, (ppe, bm)
     assert ml.pick_block_m(0, 1, 8) == 16
+
+
+def test_experts_larger_than_the_l2_take_the_smallest_tile_that_holds_their_pairs():
+    """A dense MLP of H = 5120, I = 25600 (786 MB of bf16 weights) streams from DRAM once
+    per block of it: up to 128 pairs per expert the smallest of 16/32/64/128 rows that
+    holds them, the table beyond; without H and I the rule is left out."""
+    H, I = 5120, 25600
+    for T, bm in [(1, 16), (16, 16), (17, 32), (32, 32), (33, 64), (64, 64), (65, 128), (128, 128), (129, 128),
+                  (3000, 256)]:
+        assert ml.pick_block_m(T, 1, 1, 8, H, I) == bm, (T, bm)
+    assert ml.pick_block_m(32, 1, 1, 8) == 64
+    # the wide layer's experts (270 MB): 8 experts, top-2
+    assert ml.pick_block_m(100, 2, 8, 32, 4096, 11008) == 32
+    assert ml.pick_block_m(4096, 2, 8, 32, 4096, 11008) == 256
+    # the decode layer's experts (50 MB) stay on the table
+    assert ml.pick_block_m(256, 4, 32, 8, 2880, 2880) == 64
 
 
 def test_long_runs_take_256_row_blocks_from_768_pairs_per_expert():
@@ -59,7 +78,7 @@ def test_long_runs_take_256_row_blocks_from_768_pairs_per_expert():
 def test_auto_block_m_resolves_everywhere(name):
     """block_m = 0 gives the same capacities, workspace sizes and plan as the explicit pick."""
     wl = W.get(name)
-    bm = ml.pick_block_m(wl.T, wl.k, wl.E, wl.L)
+    bm = ml.pick_block_m(wl.T, wl.k, wl.E, wl.L, wl.H, wl.I)
     a, b = dims(wl, 0), dims(wl, bm)
     assert ml.align_capacity(a) == ml.align_capacity(b)
     assert ml.workspace_size(a) == ml.workspace_size(b)

@@ -80,7 +80,7 @@ def test_align_static_matches_align_twice(ml):
         pytest.skip("no CUDA device")
     for name in ("decode", "sweep_T256", "sweep_T4096", "wide"):
         wl = W.get(name)
-        bm = ml.pick_block_m(wl.T, wl.k, wl.E, wl.L)
+        bm = ml.pick_block_m(wl.T, wl.k, wl.E, wl.L, wl.H, wl.I)
         d = _dims(ml, wl, bm)
         a_bytes, _ = ml.workspace_size(d)
         assert a_bytes <= ml.STATIC_SCRATCH_BYTES
