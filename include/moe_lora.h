@@ -276,7 +276,9 @@ int moe_lora_layer_host(const moe_lora_dims *d, const float *logits_host,
  *           the dropped-pair count; returns MOE_LORA_EDEVICE if the device reported
  *           a timeout.
  *   destroy: releases the graph.  Buffers, weights and workspace stay the caller's;
- *           none of them may move or be freed while the graph exists.
+ *           none of them may move or be freed while the graph exists, and the host
+ *           buffers stay pinned (not unregistered): the kernels captured at create
+ *           time may read or write them in place.
  */
 typedef struct moe_lora_graph moe_lora_graph;
 int moe_lora_layer_graph_create(const moe_lora_dims *d, const float *logits_host,
