@@ -16,6 +16,7 @@ the same workload.
 from __future__ import annotations
 
 import argparse
+import gc
 import json
 import os
 import statistics
@@ -381,18 +382,29 @@ def secondary_steps(ms_est: float, k_arg: int) -> int:
     return max(10, min(k_arg, 5000), min(k, 5000))
 
 
+def secondary_warmup(ms_est: float) -> int:
+    """Untimed steps before a secondary leg: about 0.1 s of them (at least 3, at most 1000),
+    so that the host's launch loop runs ahead of the GPU when the timed steps start.  The
+    legs of a few tens of microseconds are host-launch sensitive: with 3 warm-up steps
+    right after the sweep layer's 7.9 GB of adapter banks were drawn and uploaded, the
+    one-token leg once measured 59.4 us a step with unchanged per-kernel times (52.7 us in
+    other runs)."""
+    return max(3, min(1000, int(0.1e3 / (max(ms_est, 1e-3) + 0.07))))
+
+
 def run_secondary(torch, ml, name, wd, w_host, rank, world, flush, args):
     """One secondary configuration: device timing, roofline, clocks, oracle baseline."""
     wl = W.get(name)
     bm = ml.pick_block_m(wl.T, wl.k, wl.E, wl.L, wl.H, wl.I)
     probe = measure(torch, ml, wl, wd, rank, 3, 3, bm, world, flush, graph=False, e2e=False)
     k = secondary_steps(probe["ms"], args.steps)
-    m = measure(torch, ml, wl, wd, rank, k, 3, bm, world, flush, graph=False, e2e=False,
+    wu = secondary_warmup(probe["ms"])
+    m = measure(torch, ml, wl, wd, rank, k, wu, bm, world, flush, graph=False, e2e=False,
                 clocks=ClockSampler(int(os.environ.get("LOCAL_RANK", "0"))))
     roof, layer = roofline_of(m, ml)
     res = {"workload": workload_config(wl, world)["workload"], "T": wl.T,
            "value": job_throughput(wl.T, world, m["ms"]), "unit": "tokens/s", "ms_per_step": m["ms"],
-           "steps": k, "warmup": 3, "block_m": bm, "roofline": roof, "layer_roofline": layer,
+           "steps": k, "warmup": wu, "block_m": bm, "roofline": roof, "layer_roofline": layer,
            "stage_ms": {n: float(np.mean(m["stage_ms"][:, j])) for j, n in enumerate(ml.STAGES)},
            "touched": {k_: m["acct"][k_] for k_ in ("experts", "adapter_expert_pairs", "valid_pairs")},
            "clocks": clock_summary(m["clocks"], m["ms"]), "gpu_launches": probe["launches"] + m["launches"],
@@ -461,9 +473,12 @@ def run_ours(args, rank, world, local_rank):
                 del wd
                 wd = None
                 torch.cuda.empty_cache()
+                w_host = None
+                gc.collect()
                 w_host = W.make_weights(sw, 0)
                 wd = _upload(torch, w_host)
                 cur_key = _weights_key(sw)
+                time.sleep(1.0)   # let the host settle after gigabytes of fresh pages
             r = run_secondary(torch, ml, name, wd, w_host, rank, world, flush, args)
             res["secondary"][name] = r
             res["gpu_launches"] += r["gpu_launches"]
