@@ -483,6 +483,10 @@ def test_empty_batch(ml, torch):
                torch.empty((0, wl.H), dtype=torch.bfloat16, device="cuda"))
     torch.cuda.synchronize()
     assert layer.bufs["totals"].cpu().tolist() == [0, 0, 0, 0]
+    # the host-buffer entry point with no tokens: nothing in, nothing out, status clean
+    assert layer.step_host(torch.empty((0, wl.E), dtype=torch.float32),
+                           torch.empty(0, dtype=torch.int32), torch.empty((0, wl.H), dtype=torch.int16),
+                           torch.empty((0, wl.H), dtype=torch.int16)) == 0
 
 
 def test_repeat_calls_reuse_buffers(ml, torch, oracle):
