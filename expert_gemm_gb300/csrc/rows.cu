@@ -84,11 +84,15 @@ __device__ void build_shrink_plan(const ShrinkPlanArgs& pl, const int32_t* __res
   if (tid == 0) *pl.plan_count = s_carry;
 }
 
+// COPY: also copy each pair's token row (row order); without, only the row map, the
+// counters and the group table (its own instantiation: the copy loop's registers would
+// halve the CTAs an SM holds for the map-only pass).
+template <bool COPY>
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ sorted_p,
                                                           const int32_t* __restrict__ totals, int64_t max_rows, int vec_per_row,
                                                           int k, int P, uint4* __restrict__ xs,
                                                           int32_t* __restrict__ pair_row, int32_t* __restrict__ status,
-                                                          int32_t* __restrict__ ctr, int n_ctr, bool copy_rows,
+                                                          int32_t* __restrict__ ctr, int n_ctr,
                                                           const __grid_constant__ ShrinkPlanArgs plan, int plan_ctas) {
   // Launched as a programmatic dependent of whatever precedes the forward (the align):
   // its launch overlaps that kernel's tail, its reads wait for it.
@@ -109,7 +113,7 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
   uint4* dst = xs + row * vec_per_row;
   if (p < P) {
     if (lane == 0) pair_row[p] = static_cast<int32_t>(row);
-    if (!copy_rows) return;
+    if constexpr (!COPY) return;
     const uint4* src = x + static_cast<int64_t>(p / k) * vec_per_row;
     // every load of a lane in flight before its first store: one memory round trip for
     // rows of up to 512 vectors (H <= 4096), then one per further 512 (decode step
@@ -335,9 +339,9 @@ cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* sorted_p, const
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    err = cudaLaunchKernelEx(&cfg, gather_rows_kernel, reinterpret_cast<const uint4*>(x), sorted_p, totals, max_rows,
-                             H / 8, k, P, reinterpret_cast<uint4*>(x_sorted), pair_row, status, ctr, n_ctr,
-                             !token_order, pl, plan_ctas);
+    auto kern = token_order ? gather_rows_kernel<false> : gather_rows_kernel<true>;
+    err = cudaLaunchKernelEx(&cfg, kern, reinterpret_cast<const uint4*>(x), sorted_p, totals, max_rows, H / 8, k, P,
+                             reinterpret_cast<uint4*>(x_sorted), pair_row, status, ctr, n_ctr, pl, plan_ctas);
   }
   if (err != cudaSuccess || !token_order) return err;
   const int64_t T = P / k;
